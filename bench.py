@@ -1,0 +1,480 @@
+"""Benchmark of the SpMM hot path: C = A * B with A in BCSR and in WCSR.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  part 1  WCSR uniform   A 16384 x 16384 bf16, density 1 %, window 16,
+                         B 16384 x 256 bf16, C fp32   (WCSR kernel + split reduce)
+  part 2  BCSR weight    A 18944 x 3584 bf16, 64x64 blocks, 90 % zero,
+                         B 3584 x 65536 bf16, C bf16   (BCSR kernel)
+Metric: effective TFLOP/s = sum of 2*nnz*N over the parts / device time
+("AsyncSparse", Section IV: throughput counts the original nonzeros only).
+Roofline of a kernel: t_roof = max(2*stored*N / P_tensor, bytes_min / BW_hbm),
+bytes_min = stored values + format indices + B once + C once.
+
+Timing: W warm-up steps, then K timed steps; L2 is flushed (a 256 MiB write)
+before every launch, outside the CUDA-event brackets; each launch is bracketed
+by events on the stream it runs on.  Multi-GPU (torchrun): each rank runs its
+own copy of the step on its own GPU (independent problems, weak scaling, no
+collective on the data path); the reported time is the max over ranks.
+
+--impl reference times the CPU oracle (fp64, OpenMP) on the host cores on a
+bounded sample of the same workload per step.
+--sweep prints one line per benchmark configuration (not the driver line).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import spmm_workloads as W  # noqa: E402
+
+METRIC = "SpMM effective TFLOP/s (2*nnz*N/t), BCSR and WCSR"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
+# valid only for the kernel source it was taken on (sha256 of the file).
+MEASURED_TRAFFIC = {}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def src_sha(name):
+    p = os.path.join(ROOT, "sparse_dense_matrix_bcsr_gb300", "csrc", name)
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+# ---------------------------------------------------------------- workloads
+STEP_PARTS = (("wcsr_uniform", W.wcsr_uniform), ("bcsr_weight", W.bcsr_weight))
+
+
+def part_model(w, info):
+    """Algorithmic FLOPs and bytes of one launch on workload w."""
+    out_sz = 4 if w.out_dtype == "f32" else 2
+    eff_flops = 2.0 * w.nnz * w.n
+    stored_flops = 2.0 * info["stored"] * w.n
+    bytes_min = 2.0 * info["stored"] + info["idx_bytes"] + 2.0 * w.k * w.n + out_sz * w.m * w.n
+    return eff_flops, stored_flops, bytes_min
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        load = [x for x in sm if mx and x > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world):
+    import torch
+    import sparse_dense_matrix_bcsr_gb300 as S
+    from sparse_dense_matrix_bcsr_gb300 import build as lib_build
+
+    lib_build.build()
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream()
+    sptr = stream.cuda_stream
+    peaks = load_peaks()
+
+    parts = []
+    for name, fn in STEP_PARTS:
+        w = fn()
+        create = S.spmm_bcsr_create if w.fmt == "bcsr" else S.spmm_wcsr_create
+        h = create(w.m, w.k, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.b_row, w.b_col)
+        info = S.spmm_format_info(h)
+        B = w.B()
+        dB = torch.from_numpy(B.view(np.int16)).to(f"cuda:{dev}").view(
+            torch.bfloat16 if w.dtype == "bf16" else torch.float16)
+        dC = torch.empty((w.m, w.n), dtype=torch.float32 if w.out_dtype == "f32" else torch.bfloat16,
+                         device=f"cuda:{dev}")
+        eff, stored_fl, bytes_min = part_model(w, info)
+        parts.append(dict(name=name, w=w, h=h, info=info, B=B, dB=dB, dC=dC, eff=eff, stored_flops=stored_fl,
+                          bytes_min=bytes_min, launches=1 + (1 if info.get("n_split_windows", 0) else 0),
+                          kernel="bcsr_kernel.cu" if w.fmt == "bcsr" else "wcsr_kernel.cu"))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=f"cuda:{dev}")
+
+    def one_step(times):
+        for p in parts:
+            with torch.cuda.stream(stream):
+                flush.fill_(1.0)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            S.spmm_run(p["h"], p["dB"].data_ptr(), p["dC"].data_ptr(), p["w"].n, sptr)
+            e1.record(stream)
+            times.setdefault(p["name"], []).append((e0, e1))
+
+    for _ in range(args.warmup):
+        one_step({})
+    stream.synchronize()
+    for p in parts:
+        st = S.spmm_check(p["h"], sptr)
+        if st != S.SPMM_OK:
+            raise RuntimeError(f"{p['name']}: device status {st}")
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+        tdist.barrier()
+    torch.cuda.synchronize()
+    times = {}
+    with ClockSampler(dev) as clk:
+        t_wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            one_step(times)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    if dist:
+        tdist.barrier()
+    for p in parts:
+        st = S.spmm_check(p["h"], sptr)
+        if st != S.SPMM_OK:
+            raise RuntimeError(f"{p['name']}: device status {st}")
+
+    per_part = {}
+    for p in parts:
+        ms = [a.elapsed_time(b) for a, b in times[p["name"]]]
+        per_part[p["name"]] = ms
+    step_ms = [sum(per_part[p["name"]][i] for p in parts) for i in range(args.steps)]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    eff_per_step = sum(p["eff"] for p in parts)
+    value = eff_per_step * args.steps * world / (total_ms * 1e-3) / 1e12
+
+    # roofline of each part; the dominant kernel (largest time share) is reported
+    breakdown = []
+    for p in parts:
+        ms = per_part[p["name"]]
+        t = statistics.mean(ms) * 1e-3
+        t_tc = p["stored_flops"] / (peaks["bf16_tflops"] * 1e12)
+        t_hbm = p["bytes_min"] / (peaks["hbm_gbs"] * 1e9)
+        bound = "hbm" if t_hbm >= t_tc else "tensor"
+        if bound == "hbm":
+            achieved, peak, unit = p["bytes_min"] / t / 1e9, peaks["hbm_gbs"], "GB/s"
+        else:
+            achieved, peak, unit = p["stored_flops"] / t / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        tr = MEASURED_TRAFFIC.get(p["kernel"])
+        traffic = tr["bytes_per_launch"] if tr and tr.get("src_sha") == src_sha(p["kernel"]) else None
+        breakdown.append({
+            "part": p["name"], "workload": p["w"].describe(), "kernel": p["kernel"],
+            "ms_mean": round(statistics.mean(ms), 5), "ms_median": round(statistics.median(ms), 5),
+            "ms_min": round(min(ms), 5), "eff_tflops": round(p["eff"] / t / 1e12, 3),
+            "roofline": {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "t_roof_us": round(max(t_tc, t_hbm) * 1e6, 2), "t_tensor_us": round(t_tc * 1e6, 2),
+                         "t_hbm_us": round(t_hbm * 1e6, 2), "bytes_min": int(p["bytes_min"]),
+                         "stored_flops": p["stored_flops"], "peak_source": peaks["source"] + " (burst)"},
+            "format": {k: p["info"][k] for k in ("nnz", "stored", "padding", "n_units", "n_tasks",
+                                                 "n_split_windows")},
+        })
+    dom = max(breakdown, key=lambda b: b["ms_mean"])
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hosts = []
+        for p in parts:
+            hb = torch.from_numpy(p["B"].view(np.int16)).pin_memory()
+            hc = torch.empty(p["dC"].shape, dtype=p["dC"].dtype).pin_memory()
+            hosts.append((hb, hc))
+        for _ in range(max(1, min(args.warmup, 2))):
+            for p, (hb, hc) in zip(parts, hosts):
+                S.spmm_run_host_ptr(p["h"], hb.data_ptr(), hc.data_ptr(), p["w"].n, sptr)
+        e2e_steps = max(1, min(args.steps, 5))
+        if dist:
+            tdist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            for p, (hb, hc) in zip(parts, hosts):
+                S.spmm_run_host_ptr(p["h"], hb.data_ptr(), hc.data_ptr(), p["w"].n, sptr)
+        t_e2e = time.perf_counter() - t0
+        if dist:
+            t = torch.tensor([t_e2e], dtype=torch.float64)
+            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+            t_e2e = float(t.item())
+        e2e = {"value": round(eff_per_step * e2e_steps * world / t_e2e / 1e12, 4), "unit": UNIT,
+               "h2d_bytes_per_step": int(sum(hb.numel() * 2 for hb, _ in hosts)),
+               "d2h_bytes_per_step": int(sum(hc.numel() * hc.element_size() for _, hc in hosts)),
+               "steps": e2e_steps}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(parts_workloads=[p["w"] for p in parts], budget_s=args.cpu_seconds)
+
+    for p in parts:
+        S.spmm_destroy(p["h"])
+
+    clocks = clk.summary()
+    gpu_launches = args.steps * sum(p["launches"] for p in parts)
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 in, fp32 accumulate",
+        "data": "synthetic (seeded; shapes and distributions of the benchmark configurations)",
+        "config": {"workload": " + ".join(p["w"].describe() for p in parts),
+                   "parts": [p["name"] for p in parts], "l2": "flushed before every launch (256 MiB write)",
+                   "parallelism": f"replicated problem per GPU x{world}"},
+        "roofline": {k: dom["roofline"][k] for k in ("bound", "achieved", "peak", "unit", "frac", "traffic")},
+        "roofline_kernel": dom["kernel"],
+        "parts": breakdown,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches, "clocks": clocks,
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    return line
+
+
+# ---------------------------------------------------------------- oracle arm
+def cpu_baseline_sample(parts_workloads, budget_s=10.0, offset=0):
+    """Time the oracle's fp64 SpMM on a row sample of each part, sized to
+    about budget_s seconds of CPU work in total; returns the cpu_baseline dict."""
+    import oracle
+    oracle.build()
+    threads = oracle.num_threads()
+    flops = 0.0
+    t = 0.0
+    desc = []
+    for w in parts_workloads:
+        B = w.B()
+        per_row = 2.0 * w.nnz / max(w.m, 1) * w.n
+        # calibrate on a small slice, then take a slice worth budget/len(parts)
+        rows = max(1, min(w.m, int(2e8 / max(per_row, 1))))
+        r0 = (offset * rows) % max(w.m - rows + 1, 1)
+        dt = _time_rows(oracle, w, B, r0, rows, threads)
+        rate = (2.0 * (w.row_ptr[r0 + rows] - w.row_ptr[r0]) * w.n) / max(dt, 1e-9)
+        want = budget_s / len(parts_workloads)
+        rows2 = max(1, min(w.m, int(want * rate / max(per_row, 1))))
+        r0 = (offset * rows2) % max(w.m - rows2 + 1, 1)
+        dt = _time_rows(oracle, w, B, r0, rows2, threads)
+        fl = 2.0 * (w.row_ptr[r0 + rows2] - w.row_ptr[r0]) * w.n
+        flops += fl
+        t += dt
+        desc.append(f"{w.name}: rows {r0}..{r0 + rows2 - 1} of {w.m} ({fl / 2 / w.n:.0f} nnz x N={w.n})")
+    return {"value": round(flops / t / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "; ".join(desc), "seconds": round(t, 3)}
+
+
+def _time_rows(oracle, w, B, r0, rows, threads):
+    rp = w.row_ptr[r0:r0 + rows + 1] - w.row_ptr[r0]
+    ci = w.col_idx[w.row_ptr[r0]:w.row_ptr[r0 + rows]]
+    vv = w.vals[w.row_ptr[r0]:w.row_ptr[r0 + rows]]
+    t0 = time.perf_counter()
+    oracle.spmm_csr(rows, w.k, rp, ci, vv, oracle.BF16 if w.dtype == "bf16" else oracle.F16, B,
+                    threads=threads, with_abs=False)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    ws = [fn() for _, fn in STEP_PARTS]
+    per_step_s = max(1.0, min(6.0, 150.0 / max(args.steps + args.warmup, 1)))
+    for i in range(args.warmup):
+        cpu_baseline_sample(ws, budget_s=per_step_s, offset=i)
+    fl = 0.0
+    tt = 0.0
+    last = None
+    for i in range(args.steps):
+        r = cpu_baseline_sample(ws, budget_s=per_step_s, offset=args.warmup + i)
+        fl += r["value"] * 1e12 * r["seconds"]
+        tt += r["seconds"]
+        last = r
+    value = fl / tt / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp64 (oracle)",
+        "data": "synthetic (seeded), row samples per step",
+        "config": {"workload": " + ".join(w.describe() for w in ws), "parts": [n for n, _ in STEP_PARTS],
+                   "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": last["cores"], "kind": "oracle",
+                         "sample": f"per step ~{per_step_s:.1f} s of rows, e.g. " + last["sample"]},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+# ---------------------------------------------------------------- sweep
+def run_sweep(args):
+    """One JSON line per benchmark configuration on this GPU (ours only)."""
+    import torch
+    import sparse_dense_matrix_bcsr_gb300 as S
+    from sparse_dense_matrix_bcsr_gb300 import build as lib_build
+    lib_build.build()
+    peaks = load_peaks()
+    stream = torch.cuda.Stream()
+    sptr = stream.cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    cfgs = []
+    sel = args.sweep.split(",") if args.sweep not in ("all", "") else None
+    builders = [("bcsr_tiny", lambda: [W.bcsr_tiny()]), ("wcsr_uniform", lambda: [W.wcsr_uniform()]),
+                ("wcsr_irregular", lambda: [W.wcsr_irregular()]), ("bcsr_weight", lambda: [W.bcsr_weight()]),
+                ("bcsr_sweep", lambda: [W.bcsr_sweep(s, n) for s in W.BCSR_SWEEP_SPARSITY for n in W.SWEEP_N]),
+                ("wcsr_sweep", lambda: [W.wcsr_sweep(d, n) for d in W.WCSR_SWEEP_DENSITY for n in W.SWEEP_N])]
+    for name, b in builders:
+        if sel and name not in sel:
+            continue
+        cfgs.append((name, b))
+    for name, b in cfgs:
+        cache = {}
+        for w in b():
+            key = (w.fmt, w.m, w.k, w.nnz, int(w.row_ptr[w.m // 2]))
+            if key not in cache:
+                for hh in cache.values():
+                    S.spmm_destroy(hh)
+                cache.clear()
+                create = S.spmm_bcsr_create if w.fmt == "bcsr" else S.spmm_wcsr_create
+                cache[key] = create(w.m, w.k, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.b_row, w.b_col)
+            h = cache[key]
+            info = S.spmm_format_info(h)
+            dB = torch.from_numpy(w.B().view(np.int16)).cuda().view(torch.bfloat16 if w.dtype == "bf16" else torch.float16)
+            dC = torch.empty((w.m, w.n), dtype=torch.float32 if w.out_dtype == "f32" else torch.bfloat16, device="cuda")
+            ms_cold, ms_warm = [], []
+            for i in range(args.warmup + args.steps):
+                with torch.cuda.stream(stream):
+                    flush.fill_(1.0)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                S.spmm_run(h, dB.data_ptr(), dC.data_ptr(), w.n, sptr)
+                e1.record(stream)
+                e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e2.record(stream)
+                S.spmm_run(h, dB.data_ptr(), dC.data_ptr(), w.n, sptr)
+                e3.record(stream)
+                if i >= args.warmup:
+                    ms_cold.append((e0, e1))
+                    ms_warm.append((e2, e3))
+            stream.synchronize()
+            assert S.spmm_check(h, sptr) == S.SPMM_OK
+            cold = statistics.median(a.elapsed_time(b) for a, b in ms_cold)
+            warm = statistics.median(a.elapsed_time(b) for a, b in ms_warm)
+            eff, stored_fl, bytes_min = part_model(w, info)
+            t = cold * 1e-3
+            t_tc = stored_fl / (peaks["bf16_tflops"] * 1e12)
+            t_hbm = bytes_min / (peaks["hbm_gbs"] * 1e9)
+            print(json.dumps({
+                "config": w.name, "workload": w.describe(), "fmt": w.fmt, "N": w.n, "nnz": w.nnz,
+                "stored": info["stored"], "fill": round(w.nnz / max(info["stored"], 1), 4),
+                "ms_cold_median": round(cold, 5), "ms_warm_median": round(warm, 5),
+                "eff_tflops": round(eff / t / 1e12, 3), "eff_tflops_warm": round(eff / (warm * 1e-3) / 1e12, 3),
+                "roofline_frac": round(max(t_tc, t_hbm) / t, 4), "bound": "hbm" if t_hbm >= t_tc else "tensor",
+                "t_roof_us": round(max(t_tc, t_hbm) * 1e6, 2), "n_tasks": info["n_tasks"],
+                "n_split_windows": info["n_split_windows"]}), flush=True)
+        for hh in cache.values():
+            S.spmm_destroy(hh)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sweep", default=None, help="comma list of configs, or 'all'")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.sweep is None and args.impl == "ours":
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.sweep is not None:
+        run_sweep(args)
+        return
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

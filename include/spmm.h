@@ -1,0 +1,215 @@
+/*
+ * spmm.h -- C ABI of the GB300 (sm_103a) sparse x dense matrix multiply
+ * library: C = A * B with A sparse (m x k), B dense (k x N, row-major) and
+ * C dense (m x N, row-major), after "AsyncSparse: Accelerating Sparse
+ * Matrix-Matrix Multiplication on Asynchronous GPU Architectures"
+ * (Liu, Pu, Zhang).
+ *
+ * Two storage formats of A are offered, both from Section II-C and Fig. 2:
+ *   BCSR  A cut into b_row x b_col blocks; blocks holding a nonzero are kept
+ *         dense.  For block sparsity (Section III-C, Fig. 4).
+ *   WCSR  rows grouped into windows of b_row rows; a window keeps the union
+ *         of its rows' column indices (padded with -1 to a multiple of b_col)
+ *         and a packed dense [b_row x columns] value tile.  For irregular
+ *         sparsity (Sections II-C and III-B/C).
+ *
+ * Handles are created from a host CSR (the formats are built on the host and
+ * uploaded), then run any number of times against device-resident B and C.
+ *
+ * Ownership: pointers passed to *_create are borrowed for the call only.  A
+ * handle owns its device copies of the format, its task list and its split
+ * workspace; spmm_destroy frees them.  B and C passed to spmm_run are
+ * caller-owned device memory.  A handle must not be used by two host threads
+ * at once; runs of one handle on different streams must not overlap on the
+ * GPU (they share the split workspace).
+ *
+ * Errors: every call returns an spmm_status; spmm_last_error() gives a
+ * message for the last failure on the calling thread.  spmm_run is
+ * asynchronous and only reports launch-time errors; errors detected on the
+ * device (a bounded wait that ran out, an index check) are recorded in a
+ * status word that spmm_check reads.
+ */
+#ifndef SPMM_GB300_H
+#define SPMM_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct spmm_handle_s *spmm_handle;
+
+typedef enum {
+    SPMM_OK = 0,
+    SPMM_ERR_INVALID_ARG = 1,  /* bad CSR, null pointer, bad size */
+    SPMM_ERR_UNSUPPORTED = 2,  /* valid but not handled (N % 8, alignment, no sm_103 GPU ...) */
+    SPMM_ERR_CUDA = 3,         /* a CUDA runtime / driver call failed */
+    SPMM_ERR_OOM = 4,          /* device or host allocation failed */
+    SPMM_ERR_TIMEOUT = 5,      /* a bounded wait inside a kernel ran out */
+    SPMM_ERR_DEVICE_CHECK = 6  /* a kernel's own index check failed */
+} spmm_status;
+
+typedef enum { SPMM_F16 = 0, SPMM_BF16 = 1, SPMM_F32 = 2 } spmm_dtype;
+
+typedef enum { SPMM_FORMAT_BCSR = 0, SPMM_FORMAT_WCSR = 1 } spmm_format;
+
+/* Statistics of a handle's format (spmm_format_info). */
+typedef struct {
+    int32_t format;          /* spmm_format */
+    int32_t b_row, b_col;    /* block rows x cols (BCSR); window height, column padding (WCSR) */
+    int64_t m, k, nnz;
+    int64_t n_groups;        /* block rows (BCSR) or windows (WCSR): ceil(m / b_row) */
+    int64_t n_units;         /* stored blocks (BCSR) or padded column positions P_total (WCSR) */
+    int64_t stored;          /* stored values: n_units*b_row*b_col (BCSR), b_row*P_total (WCSR) */
+    int64_t padding;         /* stored - nnz: explicit zeros kept by the format */
+    int64_t idx_bytes;       /* bytes of the index arrays on the device (ptr + idx) */
+    int64_t val_bytes;       /* bytes of the value array on the device */
+    int64_t n_tasks;         /* WCSR: work items after window splitting; BCSR: n_groups */
+    int64_t n_split_windows; /* WCSR: windows split across several tasks; BCSR: 0 */
+    int64_t split_cols;      /* WCSR: maximum packed columns per task; BCSR: 0 */
+} spmm_info;
+
+/*
+ * spmm_bcsr_create -- build a BCSR handle from a host CSR.
+ * Paper: Section II-C "Block Compressed Sparse Row" and Fig. 2.  A block
+ * (b_row x b_col) is kept iff it holds at least one CSR entry; kept blocks are
+ * ordered by ascending block column within each block row and stored dense,
+ * row-major, zero-filled.  The number of block rows is ceil(m / b_row).
+ *   out       receives the handle (set to NULL on failure).
+ *   m, k      A's shape, 0 <= m, k < 2^31.
+ *   row_ptr   host int64[m+1], row_ptr[0] = 0, non-decreasing.
+ *   col_idx   host int32[row_ptr[m]], each in [0, k), strictly ascending per row.
+ *   vals      host 16-bit values (in_t bits), row_ptr[m] of them.  Every entry
+ *             is structural: an explicit 0 still keeps its block.
+ *   in_t      SPMM_F16 or SPMM_BF16 (type of A and of B at run time).
+ *   out_t     SPMM_F32 or SPMM_BF16 (type of C); accumulation is fp32.
+ *   b_row, b_col  block shape, 1..256 each.  spmm_run needs 64 x 64.
+ * Errors: INVALID_ARG for a bad CSR or shape; OOM; CUDA (no device, upload).
+ */
+spmm_status spmm_bcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64_t *row_ptr,
+                             const int32_t *col_idx, const void *vals, spmm_dtype in_t,
+                             spmm_dtype out_t, int b_row, int b_col);
+
+/*
+ * spmm_wcsr_create -- build a WCSR handle from a host CSR.
+ * Paper: Section II-C "Window Compressed Sparse Row" and Fig. 2.  Window w
+ * covers rows [w*window_h, (w+1)*window_h); its column list is the ascending
+ * union of those rows' columns followed by -1 entries up to a multiple of
+ * col_pad; window_row_ptr counts padded positions.  Values are one row-major
+ * array [window_h][P_total]: element (r, p) is A[window_h*w + r][col(p)] for
+ * the window w owning position p, 0 where absent or padded.
+ * Arguments as for spmm_bcsr_create; window_h and col_pad in 1..256.
+ * spmm_run needs window_h == 16 and col_pad a multiple of 16.
+ * Large windows are split into tasks of at most split_cols packed columns
+ * (chosen from the device's SM count; see spmm_set_split_cols).
+ */
+spmm_status spmm_wcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64_t *row_ptr,
+                             const int32_t *col_idx, const void *vals, spmm_dtype in_t,
+                             spmm_dtype out_t, int window_h, int col_pad);
+
+/*
+ * spmm_run -- C = A * B on the GPU, enqueued on `stream` (a cudaStream_t;
+ * NULL = the legacy default stream).  Paper: BCSR kernel Section III-C
+ * (Fig. 4), WCSR kernel Sections III-B/III-C.
+ *   B  device pointer, k x N row-major, in_t, 16-byte aligned.
+ *   C  device pointer, m x N row-major, out_t, 16-byte aligned; fully
+ *      overwritten (rows of A without entries give 0).
+ *   N  number of columns of B and C, N > 0 and N % 8 == 0 (TMA row stride).
+ * A WCSR handle whose windows are split uses an fp32 workspace that grows
+ * (cudaMalloc, outside any launch) on the first run with a larger N; results
+ * are bitwise reproducible run to run (fixed reduction order).
+ * Errors: INVALID_ARG (null handle/pointers, N <= 0); UNSUPPORTED (N % 8,
+ * alignment, format parameters the kernels do not take, device not sm_103);
+ * OOM (workspace); CUDA (launch).  Asynchronous: see spmm_check.
+ */
+spmm_status spmm_run(spmm_handle h, const void *B, void *C, int64_t N, void *stream);
+
+/*
+ * spmm_run_host -- the same product with B and C in HOST memory: copies B to
+ * the device, runs, copies C back, all on `stream`, and waits for the stream.
+ * Device staging buffers are owned by the handle and grow on demand.  Pinned
+ * host memory gives the fastest copies.  Errors as spmm_run, plus device
+ * errors recorded by the kernels (it calls spmm_check).
+ */
+spmm_status spmm_run_host(spmm_handle h, const void *B_host, void *C_host, int64_t N, void *stream);
+
+/* spmm_destroy -- free the handle and its device memory (waits for the device). */
+spmm_status spmm_destroy(spmm_handle h);
+
+/* spmm_format_info -- statistics of the handle's format, written to *info. */
+spmm_status spmm_format_info(spmm_handle h, spmm_info *info);
+
+/*
+ * spmm_export_format -- host copies of the three format arrays, for
+ * comparison with an independent converter.
+ *   ptr_out   int64[n_groups + 1]   block_row_ptr / window_row_ptr
+ *   idx_out   int32[n_units]        block_col_idx / window_col_idx (-1 = padding)
+ *   vals_out  uint16[stored]        blocks (n_units x b_row x b_col) / values (b_row x P_total)
+ * Any of the three may be NULL to skip it.
+ */
+spmm_status spmm_export_format(spmm_handle h, int64_t *ptr_out, int32_t *idx_out, uint16_t *vals_out);
+
+/*
+ * spmm_bcsr_convert -- host-only CSR -> BCSR with the converter that
+ * spmm_bcsr_create uses (no GPU needed).  Paper: Section II-C and Fig. 2.
+ * Call once with block_col_idx == NULL to get *n_blocks, then again with
+ *   block_row_ptr  int64[ceil(m/b_row) + 1]
+ *   block_col_idx  int32[*n_blocks]
+ *   blocks         uint16[*n_blocks * b_row * b_col] (may be NULL: skip values)
+ * Errors: INVALID_ARG for a bad CSR or shape.
+ */
+spmm_status spmm_bcsr_convert(int64_t m, int64_t k, const int64_t *row_ptr, const int32_t *col_idx,
+                              const void *vals, int b_row, int b_col, int64_t *n_blocks,
+                              int64_t *block_row_ptr, int32_t *block_col_idx, uint16_t *blocks);
+
+/*
+ * spmm_wcsr_convert -- host-only CSR -> WCSR with the converter that
+ * spmm_wcsr_create uses.  Paper: Section II-C and Fig. 2.  Call once with
+ * window_col_idx == NULL to get *p_total, then again with
+ *   window_row_ptr  int64[ceil(m/window_h) + 1]
+ *   window_col_idx  int32[*p_total]  (-1 = padding)
+ *   values          uint16[window_h * *p_total] row-major (may be NULL)
+ * Errors: INVALID_ARG for a bad CSR or shape.
+ */
+spmm_status spmm_wcsr_convert(int64_t m, int64_t k, const int64_t *row_ptr, const int32_t *col_idx,
+                              const void *vals, int window_h, int col_pad, int64_t *p_total,
+                              int64_t *window_row_ptr, int32_t *window_col_idx, uint16_t *values);
+
+/*
+ * spmm_check -- wait for `stream`, then read and clear the handle's device
+ * status word.  Returns SPMM_ERR_TIMEOUT if a kernel's bounded wait ran out,
+ * SPMM_ERR_DEVICE_CHECK if a kernel's index check failed, SPMM_ERR_CUDA for a
+ * sticky CUDA error, else SPMM_OK.
+ */
+spmm_status spmm_check(spmm_handle h, void *stream);
+
+/*
+ * spmm_set_split_cols -- WCSR only: rebuild the task list so that no task
+ * holds more than `cols` packed columns (rounded up to a multiple of 64;
+ * cols <= 0 restores the automatic choice).  Windows longer than that are
+ * split; their partial sums are added in a fixed order by a second kernel.
+ */
+spmm_status spmm_set_split_cols(spmm_handle h, int64_t cols);
+
+/*
+ * spmm_selftest_wait_timeout -- failure-detection self test.  Launches one
+ * CTA whose thread waits on an mbarrier that nothing arrives at, with a limit
+ * of timeout_ns nanoseconds, through the same bounded-wait routine the SpMM
+ * kernels use; the kernel then records a timeout and returns.  Waits for the
+ * stream and returns the recorded status in *dev_status (SPMM_ERR_TIMEOUT
+ * when the bound works).  timeout_ns must be in [1000, 10^10].
+ */
+spmm_status spmm_selftest_wait_timeout(int64_t timeout_ns, void *stream, int32_t *dev_status);
+
+/* spmm_status_str -- static English name of a status. */
+const char *spmm_status_str(spmm_status s);
+
+/* spmm_last_error -- message for the last failing call on this thread ("" if none). */
+const char *spmm_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPMM_GB300_H */

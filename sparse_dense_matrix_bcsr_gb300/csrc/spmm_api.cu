@@ -1,0 +1,570 @@
+// spmm_api.cu -- the C ABI (include/spmm.h): handle life cycle, validation,
+// upload, TMA descriptor encoding, WCSR task decomposition and launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/spmm.h"
+#include "format.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+using spmm::HostFormat;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+spmm_status fail(spmm_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+spmm_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(e == cudaErrorMemoryAllocation ? SPMM_ERR_OOM : SPMM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CUDA_TRY(call, what)                      \
+  do {                                            \
+    cudaError_t e_ = (call);                      \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+constexpr uint64_t kDefaultWaitLimitNs = 4000000000ull;  // 4 s per mbarrier wait
+
+// ---------------------------------------------------------------- driver entry
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major tensor of 16-bit elements: `rows` x `cols`, row pitch
+// `pitch_elems`; boxes of box_rows x box_cols (box_cols * 2 <= 128 bytes),
+// 128-byte swizzle, out-of-bounds elements read as zero.
+spmm_status encode_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t rows, uint64_t cols,
+                      uint64_t pitch_elems, uint32_t box_rows, uint32_t box_cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(SPMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch_elems * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPMM_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return SPMM_OK;
+}
+
+}  // namespace
+
+struct spmm_handle_s {
+  int format = 0;
+  int64_t m = 0, k = 0, nnz = 0;
+  int b_row = 0, b_col = 0;
+  spmm_dtype in_t = SPMM_BF16, out_t = SPMM_F32;
+  int device = 0;
+  int num_sms = 0;
+  bool sm103 = false;
+  int64_t n_groups = 0, n_units = 0, stored = 0;
+
+  int64_t *d_ptr = nullptr;
+  int32_t *d_idx = nullptr;
+  uint16_t *d_vals = nullptr;
+  size_t vals_bytes = 0;
+  CUtensorMap tm_vals;
+
+  const void *b_cached = nullptr;
+  int64_t n_cached = -1;
+  CUtensorMap tm_B;
+
+  // WCSR work decomposition
+  int64_t split_cols = 0;
+  bool split_auto = true;
+  std::vector<spmm::WcsrTask> tasks;
+  std::vector<spmm::WcsrSplit> splits;
+  int64_t n_slots = 0;
+  spmm::WcsrTask *d_tasks = nullptr;
+  spmm::WcsrSplit *d_splits = nullptr;
+  float *d_ws = nullptr;
+  size_t ws_bytes = 0;
+
+  uint32_t *d_status = nullptr;
+  uint64_t wait_limit_ns = kDefaultWaitLimitNs;
+
+  void *d_bstage = nullptr;
+  size_t bstage_bytes = 0;
+  void *d_cstage = nullptr;
+  size_t cstage_bytes = 0;
+};
+
+namespace {
+
+size_t elem_size(spmm_dtype t) { return t == SPMM_F32 ? 4 : 2; }
+
+spmm_status check_common(spmm_handle *out, int64_t m, int64_t k, const int64_t *row_ptr, const int32_t *col_idx,
+                         const void *vals, spmm_dtype in_t, spmm_dtype out_t, int a, int b) {
+  if (out) *out = nullptr;
+  if (!out) return fail(SPMM_ERR_INVALID_ARG, "out is NULL");
+  if (m < 0 || k < 0 || m >= (1ll << 31) || k >= (1ll << 31)) return fail(SPMM_ERR_INVALID_ARG, "m, k must be in [0, 2^31)");
+  if (!row_ptr) return fail(SPMM_ERR_INVALID_ARG, "row_ptr is NULL");
+  const int64_t nnz = row_ptr[m];
+  if (nnz > 0 && (!col_idx || !vals)) return fail(SPMM_ERR_INVALID_ARG, "col_idx or vals is NULL");
+  if (in_t != SPMM_F16 && in_t != SPMM_BF16) return fail(SPMM_ERR_INVALID_ARG, "in_t must be F16 or BF16");
+  if (out_t != SPMM_F32 && out_t != SPMM_BF16) return fail(SPMM_ERR_INVALID_ARG, "out_t must be F32 or BF16");
+  if (a < 1 || a > 256 || b < 1 || b > 256) return fail(SPMM_ERR_INVALID_ARG, "block / window parameters must be in [1, 256]");
+  std::string why = spmm::check_csr(m, k, row_ptr, col_idx);
+  if (!why.empty()) return fail(SPMM_ERR_INVALID_ARG, "invalid CSR: %s", why.c_str());
+  return SPMM_OK;
+}
+
+void free_handle(spmm_handle h) {
+  if (!h) return;
+  cudaFree(h->d_ptr);
+  cudaFree(h->d_idx);
+  cudaFree(h->d_vals);
+  cudaFree(h->d_tasks);
+  cudaFree(h->d_splits);
+  cudaFree(h->d_ws);
+  cudaFree(h->d_status);
+  cudaFree(h->d_bstage);
+  cudaFree(h->d_cstage);
+  delete h;
+}
+
+spmm_status upload_common(spmm_handle h, const HostFormat &f) {
+  CUDA_TRY(cudaGetDevice(&h->device), "cudaGetDevice");
+  cudaDeviceProp prop;
+  CUDA_TRY(cudaGetDeviceProperties(&prop, h->device), "cudaGetDeviceProperties");
+  h->num_sms = prop.multiProcessorCount;
+  h->sm103 = prop.major == 10 && prop.minor == 3;
+  CUDA_TRY(cudaMalloc(&h->d_ptr, f.ptr.size() * sizeof(int64_t)), "cudaMalloc(ptr)");
+  CUDA_TRY(cudaMemcpy(h->d_ptr, f.ptr.data(), f.ptr.size() * sizeof(int64_t), cudaMemcpyHostToDevice), "upload ptr");
+  const size_t ni = std::max<size_t>(f.idx.size(), 1);
+  CUDA_TRY(cudaMalloc(&h->d_idx, ni * sizeof(int32_t)), "cudaMalloc(idx)");
+  if (!f.idx.empty())
+    CUDA_TRY(cudaMemcpy(h->d_idx, f.idx.data(), f.idx.size() * sizeof(int32_t), cudaMemcpyHostToDevice), "upload idx");
+  // At least one zero 64 x 64 tile so a tensor map can always be encoded.
+  h->vals_bytes = std::max<size_t>(f.vals.size() * 2, 64 * 64 * 2);
+  CUDA_TRY(cudaMalloc(&h->d_vals, h->vals_bytes), "cudaMalloc(values)");
+  CUDA_TRY(cudaMemset(h->d_vals, 0, h->vals_bytes), "cudaMemset(values)");
+  if (!f.vals.empty())
+    CUDA_TRY(cudaMemcpy(h->d_vals, f.vals.data(), f.vals.size() * 2, cudaMemcpyHostToDevice), "upload values");
+  CUDA_TRY(cudaMalloc(&h->d_status, sizeof(uint32_t)), "cudaMalloc(status)");
+  CUDA_TRY(cudaMemset(h->d_status, 0, sizeof(uint32_t)), "cudaMemset(status)");
+  return SPMM_OK;
+}
+
+// Split windows longer than split_cols packed columns into tasks; order the
+// tasks longest first so the block scheduler starts the long ones early.
+spmm_status build_tasks(spmm_handle h, const std::vector<int64_t> &wptr) {
+  int64_t T = h->split_cols;
+  if (h->split_auto) {
+    const int64_t sms = std::max(h->num_sms, 1);
+    const int64_t target = (h->n_units + sms * 4 - 1) / (sms * 4);
+    T = std::max<int64_t>(512, (target + 63) / 64 * 64);
+  }
+  h->split_cols = T;
+  std::vector<spmm::WcsrTask> tasks;
+  std::vector<spmm::WcsrSplit> splits;
+  int32_t slot = 0;
+  const int64_t nw = h->n_groups;
+  for (int64_t w = 0; w < nw; ++w) {
+    const int64_t b = wptr[w], e = wptr[w + 1];
+    if (e - b <= T) {
+      tasks.push_back({static_cast<int32_t>(w), -1, b, e});
+    } else {
+      const int32_t ns = static_cast<int32_t>((e - b + T - 1) / T);
+      splits.push_back({static_cast<int32_t>(w), slot, ns, 0});
+      for (int32_t s = 0; s < ns; ++s)
+        tasks.push_back({static_cast<int32_t>(w), slot + s, b + s * T, std::min(e, b + (s + 1) * T)});
+      slot += ns;
+    }
+  }
+  std::stable_sort(tasks.begin(), tasks.end(), [](const spmm::WcsrTask &x, const spmm::WcsrTask &y) {
+    return (x.p_end - x.p_begin) > (y.p_end - y.p_begin);
+  });
+  if (tasks.size() >= (1u << 31)) return fail(SPMM_ERR_UNSUPPORTED, "too many tasks");
+  cudaFree(h->d_tasks);
+  cudaFree(h->d_splits);
+  h->d_tasks = nullptr;
+  h->d_splits = nullptr;
+  CUDA_TRY(cudaMalloc(&h->d_tasks, std::max<size_t>(tasks.size(), 1) * sizeof(spmm::WcsrTask)), "cudaMalloc(tasks)");
+  if (!tasks.empty())
+    CUDA_TRY(cudaMemcpy(h->d_tasks, tasks.data(), tasks.size() * sizeof(spmm::WcsrTask), cudaMemcpyHostToDevice),
+             "upload tasks");
+  CUDA_TRY(cudaMalloc(&h->d_splits, std::max<size_t>(splits.size(), 1) * sizeof(spmm::WcsrSplit)), "cudaMalloc(splits)");
+  if (!splits.empty())
+    CUDA_TRY(cudaMemcpy(h->d_splits, splits.data(), splits.size() * sizeof(spmm::WcsrSplit), cudaMemcpyHostToDevice),
+             "upload splits");
+  h->tasks.swap(tasks);
+  h->splits.swap(splits);
+  h->n_slots = slot;
+  return SPMM_OK;
+}
+
+spmm_status check_run_args(spmm_handle h, const void *B, void *C, int64_t N) {
+  if (!h) return fail(SPMM_ERR_INVALID_ARG, "handle is NULL");
+  if (N <= 0 || N >= (1ll << 31)) return fail(SPMM_ERR_INVALID_ARG, "N must be in (0, 2^31)");
+  if (!B || !C) return fail(SPMM_ERR_INVALID_ARG, "B or C is NULL");
+  if (N % 8 != 0) return fail(SPMM_ERR_UNSUPPORTED, "N must be a multiple of 8 (16-byte rows of B)");
+  if (N > 65535ll * 128) return fail(SPMM_ERR_UNSUPPORTED, "N above 65535 * 128 exceeds the launch grid");
+  if ((reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C)) & 15)
+    return fail(SPMM_ERR_UNSUPPORTED, "B and C must be 16-byte aligned");
+  if (!h->sm103) return fail(SPMM_ERR_UNSUPPORTED, "the kernels need an sm_103 (GB300) device");
+  return SPMM_OK;
+}
+
+spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStream_t s) {
+  if (h->m == 0) return SPMM_OK;
+  const bool in_bf16 = h->in_t == SPMM_BF16;
+  const bool out_bf16 = h->out_t == SPMM_BF16;
+  if (h->format == SPMM_FORMAT_BCSR) {
+    if (h->b_row != 64 || h->b_col != 64) return fail(SPMM_ERR_UNSUPPORTED, "the BCSR kernel takes 64 x 64 blocks");
+    if (h->b_cached != B || h->n_cached != N) {
+      spmm_status st = encode_2d(&h->tm_B, B, in_bf16, static_cast<uint64_t>(std::max<int64_t>(h->k, 1)),
+                                 static_cast<uint64_t>(N), static_cast<uint64_t>(N), 64, 64);
+      if (st != SPMM_OK) return st;
+      h->b_cached = B;
+      h->n_cached = N;
+    }
+    spmm::BcsrParams p;
+    p.block_row_ptr = h->d_ptr;
+    p.block_col_idx = h->d_idx;
+    p.C = C;
+    p.ldc = N;
+    p.M = static_cast<int32_t>(h->m);
+    p.N = static_cast<int32_t>(N);
+    p.n_block_rows = static_cast<int32_t>(h->n_groups);
+    p.status = h->d_status;
+    p.wait_limit_ns = h->wait_limit_ns;
+    cudaError_t e = spmm::launch_bcsr(h->tm_vals, h->tm_B, p, in_bf16, out_bf16, s);
+    if (e != cudaSuccess) return cuda_fail(e, "BCSR kernel launch");
+    return SPMM_OK;
+  }
+  // WCSR
+  if (h->b_row != 16 || h->b_col % 16 != 0)
+    return fail(SPMM_ERR_UNSUPPORTED, "the WCSR kernel takes window height 16 and column padding a multiple of 16");
+  const size_t need = static_cast<size_t>(h->n_slots) * 16 * static_cast<size_t>(N) * sizeof(float);
+  if (need > h->ws_bytes) {
+    cudaFree(h->d_ws);
+    h->d_ws = nullptr;
+    h->ws_bytes = 0;
+    CUDA_TRY(cudaMalloc(&h->d_ws, need), "cudaMalloc(split workspace)");
+    h->ws_bytes = need;
+  }
+  spmm::WcsrParams p;
+  p.tasks = h->d_tasks;
+  p.window_col_idx = h->d_idx;
+  p.B = B;
+  p.C = C;
+  p.workspace = h->d_ws;
+  p.P_total = h->n_units;
+  p.M = static_cast<int32_t>(h->m);
+  p.N = static_cast<int32_t>(N);
+  p.K = static_cast<int32_t>(h->k);
+  p.n_tasks = static_cast<int32_t>(h->tasks.size());
+  p.status = h->d_status;
+  p.wait_limit_ns = h->wait_limit_ns;
+  cudaError_t e = spmm::launch_wcsr(h->tm_vals, p, in_bf16, out_bf16, s);
+  if (e != cudaSuccess) return cuda_fail(e, "WCSR kernel launch");
+  e = spmm::launch_wcsr_reduce(h->d_splits, static_cast<int32_t>(h->splits.size()), h->d_ws, C, p.M, p.N, out_bf16, s);
+  if (e != cudaSuccess) return cuda_fail(e, "WCSR reduce launch");
+  return SPMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *spmm_status_str(spmm_status s) {
+  switch (s) {
+    case SPMM_OK: return "SPMM_OK";
+    case SPMM_ERR_INVALID_ARG: return "SPMM_ERR_INVALID_ARG";
+    case SPMM_ERR_UNSUPPORTED: return "SPMM_ERR_UNSUPPORTED";
+    case SPMM_ERR_CUDA: return "SPMM_ERR_CUDA";
+    case SPMM_ERR_OOM: return "SPMM_ERR_OOM";
+    case SPMM_ERR_TIMEOUT: return "SPMM_ERR_TIMEOUT";
+    case SPMM_ERR_DEVICE_CHECK: return "SPMM_ERR_DEVICE_CHECK";
+  }
+  return "unknown spmm_status";
+}
+
+const char *spmm_last_error(void) { return g_last_error.c_str(); }
+
+spmm_status spmm_bcsr_convert(int64_t m, int64_t k, const int64_t *row_ptr, const int32_t *col_idx, const void *vals,
+                              int b_row, int b_col, int64_t *n_blocks, int64_t *block_row_ptr, int32_t *block_col_idx,
+                              uint16_t *blocks) {
+  spmm_handle dummy;
+  spmm_status st = check_common(&dummy, m, k, row_ptr, col_idx, vals, SPMM_BF16, SPMM_F32, b_row, b_col);
+  if (st != SPMM_OK) return st;
+  if (!n_blocks) return fail(SPMM_ERR_INVALID_ARG, "n_blocks is NULL");
+  HostFormat f;
+  spmm::build_bcsr(m, k, row_ptr, col_idx, block_col_idx && blocks ? static_cast<const uint16_t *>(vals) : nullptr,
+                   b_row, b_col, f);
+  *n_blocks = f.n_units;
+  if (!block_col_idx) return SPMM_OK;
+  if (block_row_ptr) std::memcpy(block_row_ptr, f.ptr.data(), f.ptr.size() * sizeof(int64_t));
+  if (!f.idx.empty()) std::memcpy(block_col_idx, f.idx.data(), f.idx.size() * sizeof(int32_t));
+  if (blocks && !f.vals.empty()) std::memcpy(blocks, f.vals.data(), f.vals.size() * 2);
+  return SPMM_OK;
+}
+
+spmm_status spmm_wcsr_convert(int64_t m, int64_t k, const int64_t *row_ptr, const int32_t *col_idx, const void *vals,
+                              int window_h, int col_pad, int64_t *p_total, int64_t *window_row_ptr,
+                              int32_t *window_col_idx, uint16_t *values) {
+  spmm_handle dummy;
+  spmm_status st = check_common(&dummy, m, k, row_ptr, col_idx, vals, SPMM_BF16, SPMM_F32, window_h, col_pad);
+  if (st != SPMM_OK) return st;
+  if (!p_total) return fail(SPMM_ERR_INVALID_ARG, "p_total is NULL");
+  HostFormat f;
+  spmm::build_wcsr(m, k, row_ptr, col_idx, window_col_idx && values ? static_cast<const uint16_t *>(vals) : nullptr,
+                   window_h, col_pad, f);
+  *p_total = f.n_units;
+  if (!window_col_idx) return SPMM_OK;
+  if (window_row_ptr) std::memcpy(window_row_ptr, f.ptr.data(), f.ptr.size() * sizeof(int64_t));
+  if (!f.idx.empty()) std::memcpy(window_col_idx, f.idx.data(), f.idx.size() * sizeof(int32_t));
+  if (values && !f.vals.empty()) std::memcpy(values, f.vals.data(), f.vals.size() * 2);
+  return SPMM_OK;
+}
+
+spmm_status spmm_bcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64_t *row_ptr, const int32_t *col_idx,
+                             const void *vals, spmm_dtype in_t, spmm_dtype out_t, int b_row, int b_col) {
+  spmm_status st = check_common(out, m, k, row_ptr, col_idx, vals, in_t, out_t, b_row, b_col);
+  if (st != SPMM_OK) return st;
+  HostFormat f;
+  spmm::build_bcsr(m, k, row_ptr, col_idx, static_cast<const uint16_t *>(vals), b_row, b_col, f);
+  if (f.n_units * b_row >= (1ll << 31)) return fail(SPMM_ERR_UNSUPPORTED, "too many stored blocks");
+  spmm_handle h = new spmm_handle_s;
+  h->format = SPMM_FORMAT_BCSR;
+  h->m = m;
+  h->k = k;
+  h->nnz = row_ptr[m];
+  h->b_row = b_row;
+  h->b_col = b_col;
+  h->in_t = in_t;
+  h->out_t = out_t;
+  h->n_groups = static_cast<int64_t>(f.ptr.size()) - 1;
+  h->n_units = f.n_units;
+  h->stored = f.n_units * b_row * b_col;
+  st = upload_common(h, f);
+  if (st == SPMM_OK && b_row == 64 && b_col == 64)
+    st = encode_2d(&h->tm_vals, h->d_vals, in_t == SPMM_BF16, static_cast<uint64_t>(std::max<int64_t>(f.n_units, 1) * 64),
+                   64, 64, 64, 64);
+  if (st != SPMM_OK) {
+    free_handle(h);
+    return st;
+  }
+  *out = h;
+  return SPMM_OK;
+}
+
+spmm_status spmm_wcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64_t *row_ptr, const int32_t *col_idx,
+                             const void *vals, spmm_dtype in_t, spmm_dtype out_t, int window_h, int col_pad) {
+  spmm_status st = check_common(out, m, k, row_ptr, col_idx, vals, in_t, out_t, window_h, col_pad);
+  if (st != SPMM_OK) return st;
+  HostFormat f;
+  spmm::build_wcsr(m, k, row_ptr, col_idx, static_cast<const uint16_t *>(vals), window_h, col_pad, f);
+  if (f.n_units >= (1ll << 31)) return fail(SPMM_ERR_UNSUPPORTED, "too many packed columns");
+  spmm_handle h = new spmm_handle_s;
+  h->format = SPMM_FORMAT_WCSR;
+  h->m = m;
+  h->k = k;
+  h->nnz = row_ptr[m];
+  h->b_row = window_h;
+  h->b_col = col_pad;
+  h->in_t = in_t;
+  h->out_t = out_t;
+  h->n_groups = static_cast<int64_t>(f.ptr.size()) - 1;
+  h->n_units = f.n_units;
+  h->stored = f.n_units * window_h;
+  st = upload_common(h, f);
+  if (st == SPMM_OK && window_h == 16 && col_pad % 16 == 0)
+    st = encode_2d(&h->tm_vals, h->d_vals, in_t == SPMM_BF16, 16,
+                   static_cast<uint64_t>(f.n_units > 0 ? f.n_units : 64),
+                   static_cast<uint64_t>(f.n_units > 0 ? f.n_units : 64), 16, 64);
+  if (st == SPMM_OK) st = build_tasks(h, f.ptr);
+  if (st != SPMM_OK) {
+    free_handle(h);
+    return st;
+  }
+  *out = h;
+  return SPMM_OK;
+}
+
+spmm_status spmm_set_split_cols(spmm_handle h, int64_t cols) {
+  if (!h) return fail(SPMM_ERR_INVALID_ARG, "handle is NULL");
+  if (h->format != SPMM_FORMAT_WCSR) return fail(SPMM_ERR_INVALID_ARG, "split columns apply to WCSR handles only");
+  CUDA_TRY(cudaSetDevice(h->device), "cudaSetDevice");
+  std::vector<int64_t> wptr(static_cast<size_t>(h->n_groups + 1));
+  CUDA_TRY(cudaMemcpy(wptr.data(), h->d_ptr, wptr.size() * sizeof(int64_t), cudaMemcpyDeviceToHost), "download ptr");
+  CUDA_TRY(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  if (cols <= 0) {
+    h->split_auto = true;
+  } else {
+    h->split_auto = false;
+    h->split_cols = (cols + 63) / 64 * 64;
+  }
+  return build_tasks(h, wptr);
+}
+
+spmm_status spmm_run(spmm_handle h, const void *B, void *C, int64_t N, void *stream) {
+  spmm_status st = check_run_args(h, B, C, N);
+  if (st != SPMM_OK) return st;
+  return run_device(h, B, C, N, static_cast<cudaStream_t>(stream));
+}
+
+spmm_status spmm_check(spmm_handle h, void *stream) {
+  if (!h) return fail(SPMM_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  CUDA_TRY(cudaMemcpyAsync(&word, h->d_status, sizeof word, cudaMemcpyDeviceToHost, s), "read status");
+  CUDA_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+  if (word) {
+    CUDA_TRY(cudaMemsetAsync(h->d_status, 0, sizeof(uint32_t), s), "clear status");
+    CUDA_TRY(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+    if (word & spmm::kDevTimeout) return fail(SPMM_ERR_TIMEOUT, "a kernel's bounded wait ran out");
+    return fail(SPMM_ERR_DEVICE_CHECK, "a kernel's index check failed (status 0x%x)", word);
+  }
+  return SPMM_OK;
+}
+
+spmm_status spmm_run_host(spmm_handle h, const void *B_host, void *C_host, int64_t N, void *stream) {
+  if (!h) return fail(SPMM_ERR_INVALID_ARG, "handle is NULL");
+  if (!B_host || !C_host) return fail(SPMM_ERR_INVALID_ARG, "B or C is NULL");
+  if (N <= 0) return fail(SPMM_ERR_INVALID_ARG, "N must be positive");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t bb = static_cast<size_t>(h->k) * N * elem_size(h->in_t);
+  const size_t cb = static_cast<size_t>(h->m) * N * elem_size(h->out_t);
+  if (!h->d_bstage || bb > h->bstage_bytes) {
+    cudaFree(h->d_bstage);
+    h->d_bstage = nullptr;
+    h->bstage_bytes = 0;
+    CUDA_TRY(cudaMalloc(&h->d_bstage, std::max<size_t>(bb, 16)), "cudaMalloc(B staging)");
+    h->bstage_bytes = std::max<size_t>(bb, 16);
+  }
+  if (!h->d_cstage || cb > h->cstage_bytes) {
+    cudaFree(h->d_cstage);
+    h->d_cstage = nullptr;
+    h->cstage_bytes = 0;
+    CUDA_TRY(cudaMalloc(&h->d_cstage, std::max<size_t>(cb, 16)), "cudaMalloc(C staging)");
+    h->cstage_bytes = std::max<size_t>(cb, 16);
+  }
+  void *dB = h->d_bstage;
+  void *dC = h->d_cstage;
+  spmm_status st = check_run_args(h, dB, dC, N);
+  if (st != SPMM_OK) return st;
+  if (bb) CUDA_TRY(cudaMemcpyAsync(dB, B_host, bb, cudaMemcpyHostToDevice, s), "copy B to device");
+  st = run_device(h, dB, dC, N, s);
+  if (st != SPMM_OK) return st;
+  if (cb) CUDA_TRY(cudaMemcpyAsync(C_host, dC, cb, cudaMemcpyDeviceToHost, s), "copy C to host");
+  return spmm_check(h, stream);
+}
+
+spmm_status spmm_destroy(spmm_handle h) {
+  if (!h) return fail(SPMM_ERR_INVALID_ARG, "handle is NULL");
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  free_handle(h);
+  return SPMM_OK;
+}
+
+spmm_status spmm_format_info(spmm_handle h, spmm_info *info) {
+  if (!h || !info) return fail(SPMM_ERR_INVALID_ARG, "handle or info is NULL");
+  std::memset(info, 0, sizeof *info);
+  info->format = h->format;
+  info->b_row = h->b_row;
+  info->b_col = h->b_col;
+  info->m = h->m;
+  info->k = h->k;
+  info->nnz = h->nnz;
+  info->n_groups = h->n_groups;
+  info->n_units = h->n_units;
+  info->stored = h->stored;
+  info->padding = h->stored - h->nnz;
+  info->idx_bytes = (h->n_groups + 1) * 8 + h->n_units * 4;
+  info->val_bytes = h->stored * 2;
+  if (h->format == SPMM_FORMAT_WCSR) {
+    info->n_tasks = static_cast<int64_t>(h->tasks.size());
+    info->n_split_windows = static_cast<int64_t>(h->splits.size());
+    info->split_cols = h->split_cols;
+  } else {
+    info->n_tasks = h->n_groups;
+  }
+  return SPMM_OK;
+}
+
+spmm_status spmm_export_format(spmm_handle h, int64_t *ptr_out, int32_t *idx_out, uint16_t *vals_out) {
+  if (!h) return fail(SPMM_ERR_INVALID_ARG, "handle is NULL");
+  CUDA_TRY(cudaSetDevice(h->device), "cudaSetDevice");
+  CUDA_TRY(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+  if (ptr_out)
+    CUDA_TRY(cudaMemcpy(ptr_out, h->d_ptr, (h->n_groups + 1) * sizeof(int64_t), cudaMemcpyDeviceToHost), "download ptr");
+  if (idx_out && h->n_units)
+    CUDA_TRY(cudaMemcpy(idx_out, h->d_idx, h->n_units * sizeof(int32_t), cudaMemcpyDeviceToHost), "download idx");
+  if (vals_out && h->stored)
+    CUDA_TRY(cudaMemcpy(vals_out, h->d_vals, h->stored * 2, cudaMemcpyDeviceToHost), "download values");
+  return SPMM_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- self test
+namespace spmm {
+namespace {
+__global__ void wait_selftest_kernel(uint32_t *status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_addr(&bar);
+  mbar_init(b, 1);
+  fence_barrier_init();
+  // Nothing arrives: the phase never completes and the bounded wait gives up.
+  if (!mbar_wait(b, 0, limit_ns)) atomicOr(status, kDevTimeout);
+}
+}  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 1, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+}  // namespace spmm
+
+extern "C" spmm_status spmm_selftest_wait_timeout(int64_t timeout_ns, void *stream, int32_t *dev_status) {
+  if (!dev_status) return fail(SPMM_ERR_INVALID_ARG, "dev_status is NULL");
+  if (timeout_ns < 1000 || timeout_ns > 10000000000ll) return fail(SPMM_ERR_INVALID_ARG, "timeout_ns out of range");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t *d = nullptr;
+  CUDA_TRY(cudaMalloc(&d, sizeof(uint32_t)), "cudaMalloc(status)");
+  uint32_t word = 0;
+  cudaError_t e = cudaMemsetAsync(d, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = spmm::launch_wait_selftest(d, static_cast<uint64_t>(timeout_ns), s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&word, d, sizeof word, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  cudaFree(d);
+  if (e != cudaSuccess) return cuda_fail(e, "wait self test");
+  *dev_status = (word & spmm::kDevTimeout) ? SPMM_ERR_TIMEOUT : SPMM_OK;
+  return SPMM_OK;
+}

@@ -1,0 +1,345 @@
+// wcsr_kernel.cu -- WCSR SpMM for sm_103a.
+//
+// Method: "AsyncSparse", Section III-B (the packed value tile of a window is
+// contiguous and loaded by TMA; the matching rows of B are gathered through
+// window_col_idx by all threads into shared memory with the 128-byte swizzle
+// applied by hand) and Section III-C (task-based decomposition: long windows
+// are split into fixed-size sub-tasks and the CTA index names a task).  The
+// paper adds split partial sums with atomicAdd; here a split task writes an
+// fp32 partial and a second kernel adds a window's partials in slot order, so
+// results are bitwise reproducible.
+//
+// As in the BCSR kernel the product is computed transposed: the 128 columns of
+// an accumulator are the MMA's M (TMEM lanes) and the 16 rows of a window are
+// the MMA's N, so a 16-row window is a legal tcgen05 shape (M >= 64 would
+// otherwise waste 3/4 of the MMA).
+//
+// CTA = one task x one tile of BN = 128*NACC columns; 5 warps:
+//   warps 0..3  gather producers (cp.async, 16 B per copy), warp 0 lane 0
+//               also issues the TMA for the value tile; afterwards the same
+//               warps are the epilogue (warp w reads TMEM sub-partition w)
+//   warp 4      TMEM allocator and MMA issuer
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace spmm {
+namespace {
+
+constexpr int kH = 16;                       // window height
+constexpr int kKC = 64;                      // packed columns per stage
+constexpr int kValBytes = kH * kKC * 2;      // 2 KB value tile per stage
+constexpr int kChunkBytes = kKC * 64 * 2;    // 64 gathered rows x 64 columns
+constexpr int kProducerWarps = 4;
+constexpr int kThreads = 32 * (kProducerWarps + 1);
+constexpr int kLag = 2;                      // cp.async groups kept in flight per thread
+
+template <int NACC, int Q>
+struct Cfg {
+  static constexpr int kBN = 128 * NACC;
+  static constexpr int kChunks = 2 * NACC;
+  static constexpr int kStageBytes = kValBytes + kChunks * kChunkBytes;
+  static constexpr int kTmemCols = 32;  // NACC * 16 <= 32
+  static constexpr int kSmemBytes = Q * kStageBytes + 1024 + 1024;
+  static_assert(kLag < Q, "the producer must not wait on a stage it has not released");
+};
+
+template <bool OUT_BF16>
+__device__ __forceinline__ void store_out(void *C, int64_t off, float v) {
+  if constexpr (OUT_BF16)
+    reinterpret_cast<__nv_bfloat16 *>(C)[off] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<float *>(C)[off] = v;
+}
+
+template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    wcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmV, const WcsrParams p) {
+  using C_ = Cfg<NACC, Q>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Q * C_::kStageBytes);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Q + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WcsrTask task = p.tasks[blockIdx.x];
+  const int n0 = blockIdx.y * C_::kBN;
+  const int nvalid = min(C_::kBN, p.N - n0);
+  const int nacc = min(NACC, (nvalid + 127) / 128);
+  const int64_t ncols = task.p_end - task.p_begin;
+  const int nstages = static_cast<int>((ncols + kKC - 1) / kKC);
+
+  const uint32_t full0 = smem_addr(&bars[0]);
+  const uint32_t empty0 = smem_addr(&bars[Q]);
+  const uint32_t accum_bar = smem_addr(&bars[2 * Q]);
+  const uint32_t drain_bar = smem_addr(&bars[2 * Q + 1]);
+
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < Q; ++q) {
+      mbar_init(full0 + 8 * q, kProducerWarps + 1);  // one arrive per gather warp + the TMA arrive
+      mbar_init(empty0 + 8 * q, 1);
+    }
+    mbar_init(accum_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == kProducerWarps) {
+    tmem_alloc(smem_addr(tmem_slot), C_::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < kProducerWarps) {
+    // ------------------------------------------------------------ gather
+    // Copy layout: one 16-byte piece = 8 consecutive columns of one B row.
+    // A row of the tile has BN/8 pieces; 32/(BN/8/...) rows per warp step.
+    constexpr int kPiecesPerRow = C_::kBN / 8;             // 16 or 32
+    constexpr int kRowsPerStep = 32 / kPiecesPerRow;       // rows one warp copies per instruction
+    constexpr int kRowsPerWarp = kKC / kProducerWarps;     // 16
+    const int piece = lane % kPiecesPerRow;
+    const int sub = lane / kPiecesPerRow;
+    const int ncol = n0 + piece * 8;                       // first column of this lane's piece
+    const bool col_ok = ncol < p.N;
+    const uint16_t *Bp = reinterpret_cast<const uint16_t *>(p.B);
+    const int chunk = piece / 8;                           // 64-column chunk of the piece
+    const uint32_t unit = static_cast<uint32_t>(piece % 8);
+
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    int s = 0;
+    for (; s < nstages; ++s) {
+      if (lane == 0) ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns) && !*abort_flag;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const int64_t pbase = task.p_begin + static_cast<int64_t>(s) * kKC;
+      const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
+      if (warp == 0 && lane == 0) {
+        const uint32_t fb = full0 + 8 * stage;
+        mbar_arrive_expect_tx(fb, kValBytes);
+        tma_load_2d(st, &tmV, fb, static_cast<int32_t>(pbase), 0);
+      }
+      // Column indices of this warp's 16 rows of the stage.
+      const int64_t my_p = pbase + warp * kRowsPerWarp + (lane & 15);
+      const int32_t my_idx = (lane < 16 && my_p < task.p_end) ? p.window_col_idx[my_p] : -2;
+      const uint32_t gath = st + kValBytes + chunk * kChunkBytes;
+#pragma unroll
+      for (int rr = 0; rr < kRowsPerWarp; rr += kRowsPerStep) {
+        const int rloc = rr + sub;                         // row within this warp's 16
+        const int32_t col = __shfl_sync(0xffffffffu, my_idx, rloc);
+        if (col != -2) {                                   // -2: past the task's end, not read by the MMA
+          const int k = warp * kRowsPerWarp + rloc;        // row within the stage
+          const uint32_t dst = gath + k * 128 + ((unit ^ static_cast<uint32_t>(k & 7)) << 4);
+          const bool live = col_ok && col >= 0;
+          const void *src = live ? static_cast<const void *>(Bp + static_cast<int64_t>(col) * p.N + ncol)
+                                 : static_cast<const void *>(Bp);
+          cp_async_16(dst, src, live ? 16u : 0u);
+        }
+      }
+      cp_async_commit();
+      if (s >= kLag) {
+        cp_async_wait<kLag>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full0 + 8 * ((stage + Q - kLag) % Q));
+      }
+      if (++stage == Q) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    // Release the stages still pending.
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    __syncwarp();
+    {
+      const int done = s;  // stages issued
+      const int first = done > kLag ? done - kLag : 0;
+      for (int t = first; t < done; ++t)
+        if (lane == 0) mbar_arrive(full0 + 8 * (t % Q));
+    }
+    if (!ok && lane == 0) {
+      atomicOr(p.status, kDevTimeout);
+      *abort_flag = 1;
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nstages > 0) {
+      constexpr uint32_t idesc = idesc_f16(IN_BF16, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, kH);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int s = 0; s < nstages; ++s) {
+        if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t vals = smem_addr(smem + stage * C_::kStageBytes);  // MMA operand B (K-major)
+        const uint32_t gath = vals + kValBytes;                           // MMA operand A (MN-major)
+        const int64_t left = ncols - static_cast<int64_t>(s) * kKC;
+        const int ksteps = left >= kKC ? 4 : static_cast<int>(left / 16);
+        for (int kk = 0; kk < ksteps; ++kk) {
+          const uint64_t bdesc = smem_desc_sw128(vals + kk * 32, 16, 1024);
+#pragma unroll
+          for (int a = 0; a < NACC; ++a) {
+            if (a < nacc) {
+              const uint64_t adesc = smem_desc_sw128(gath + a * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
+              umma_f16(tmem + a * kH, adesc, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+        }
+        umma_commit(empty0 + 8 * stage);
+        if (++stage == Q) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) {
+        umma_commit(accum_bar);
+      } else {
+        atomicOr(p.status, kDevTimeout);
+        *abort_flag = 1;
+        umma_commit(drain_bar);
+        mbar_wait(drain_bar, 0, 1000000ull);
+        mbar_arrive(accum_bar);
+      }
+    }
+    __syncwarp();
+  }
+
+  if (warp < kProducerWarps) {
+    // ------------------------------------------------------------ epilogue
+    const int sp = warp;  // warps 0..3 own TMEM sub-partitions 0..3
+    const int row0 = task.window * kH;
+    const bool to_ws = task.slot >= 0;
+    float *ws = to_ws ? p.workspace + static_cast<int64_t>(task.slot) * kH * p.N : nullptr;
+    bool have = nstages > 0;
+    if (have) {
+      if (!mbar_wait(accum_bar, 0, p.wait_limit_ns)) {
+        atomicOr(p.status, kDevTimeout);
+        *abort_flag = 1;
+        have = false;
+      } else if (*abort_flag) {
+        have = false;
+      }
+      tc_fence_after_sync();
+    }
+    for (int a = 0; a < nacc; ++a) {
+      const int n = n0 + a * 128 + sp * 32 + lane;
+      uint32_t v[16];
+      if (have) {
+        tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(sp * 32) << 16) + a * kH, v);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0u;
+      }
+      if (n < p.N) {
+#pragma unroll
+        for (int i = 0; i < kH; ++i) {
+          if (to_ws) {
+            ws[static_cast<int64_t>(i) * p.N + n] = __uint_as_float(v[i]);
+          } else if (row0 + i < p.M) {
+            store_out<OUT_BF16>(p.C, static_cast<int64_t>(row0 + i) * p.N + n, __uint_as_float(v[i]));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kProducerWarps) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, C_::kTmemCols);
+  }
+}
+
+template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
+cudaError_t launch_variant(const CUtensorMap &tmV, const WcsrParams &p, cudaStream_t stream) {
+  using C_ = Cfg<NACC, Q>;
+  auto kern = wcsr_spmm_kernel<NACC, Q, IN_BF16, OUT_BF16>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(p.n_tasks, (p.N + C_::kBN - 1) / C_::kBN);
+  kern<<<grid, kThreads, C_::kSmemBytes, stream>>>(tmV, p);
+  return cudaGetLastError();
+}
+
+template <int NACC, int Q>
+cudaError_t launch_dtypes(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
+                          cudaStream_t s) {
+  if (in_bf16)
+    return out_bf16 ? launch_variant<NACC, Q, true, true>(tmV, p, s) : launch_variant<NACC, Q, true, false>(tmV, p, s);
+  return out_bf16 ? launch_variant<NACC, Q, false, true>(tmV, p, s) : launch_variant<NACC, Q, false, false>(tmV, p, s);
+}
+
+// One thread per 4 consecutive columns of one row of one split window;
+// blockIdx.x names the split window, threads stride over its 16 x N partials.
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(256) wcsr_reduce_kernel(const WcsrSplit *splits, const float *ws, void *C,
+                                                          int32_t M, int32_t N) {
+  const WcsrSplit sp = splits[blockIdx.x];
+  const int64_t per = static_cast<int64_t>(kH) * N;
+  for (int64_t e = (static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x) * 4; e < per;
+       e += static_cast<int64_t>(gridDim.y) * blockDim.x * 4) {
+    const int r = static_cast<int>(e / N);
+    const int row = sp.window * kH + r;
+    if (row >= M) break;  // rows only grow with e
+    const float *src = ws + static_cast<int64_t>(sp.slot_begin) * per + e;
+    float4 acc = *reinterpret_cast<const float4 *>(src);
+    for (int s = 1; s < sp.n_slots; ++s) {
+      const float4 v = *reinterpret_cast<const float4 *>(src + s * per);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int64_t off = static_cast<int64_t>(row) * N + (e - static_cast<int64_t>(r) * N);
+    if constexpr (OUT_BF16) {
+      __nv_bfloat16 *c = reinterpret_cast<__nv_bfloat16 *>(C) + off;
+      c[0] = __float2bfloat16_rn(acc.x);
+      c[1] = __float2bfloat16_rn(acc.y);
+      c[2] = __float2bfloat16_rn(acc.z);
+      c[3] = __float2bfloat16_rn(acc.w);
+    } else {
+      *reinterpret_cast<float4 *>(reinterpret_cast<float *>(C) + off) = acc;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_wcsr(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
+                        cudaStream_t stream) {
+  if (p.n_tasks == 0 || p.N == 0) return cudaSuccess;
+  if (p.N <= 128) return launch_dtypes<1, 6>(tmV, p, in_bf16, out_bf16, stream);
+  return launch_dtypes<2, 4>(tmV, p, in_bf16, out_bf16, stream);
+}
+
+cudaError_t launch_wcsr_reduce(const WcsrSplit *splits, int32_t n_splits, const float *workspace, void *C,
+                               int32_t M, int32_t N, bool out_bf16, cudaStream_t stream) {
+  if (n_splits == 0 || N == 0) return cudaSuccess;
+  const int64_t per4 = (static_cast<int64_t>(kH) * N) / 4;  // N % 8 == 0
+  const int64_t blocks = (per4 + 255) / 256;
+  dim3 grid(n_splits, static_cast<unsigned>(blocks < 1024 ? blocks : 1024));
+  if (out_bf16)
+    wcsr_reduce_kernel<true><<<grid, 256, 0, stream>>>(splits, workspace, C, M, N);
+  else
+    wcsr_reduce_kernel<false><<<grid, 256, 0, stream>>>(splits, workspace, C, M, N);
+  return cudaGetLastError();
+}
+
+}  // namespace spmm

@@ -1,0 +1,127 @@
+"""BCSR kernel parity with the oracle on the GPU (through the C ABI).
+
+Small cases span several 64-row block rows and 128/256-column tiles with
+ragged tails and are compared element by element; the full-size benchmark
+workloads are compared on seeded samples of outputs that the oracle computes
+one by one, and checked for full coverage (no NaN left in a NaN-filled C)."""
+import numpy as np
+import pytest
+
+import oracle
+import spmm_workloads as W
+from spmm_testlib import assert_parity, ensure_library, ocode, run_library
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_library()
+
+
+def full_check(m, k, n, rp, ci, vals, dt, out_dt, B, runs=1):
+    outs, info = run_library("bcsr", m, k, rp, ci, vals, dt, out_dt, B, runs=runs)
+    C_ref, S_ref = oracle.spmm_csr(m, k, rp, ci, vals, ocode(dt), B)
+    for C in outs:
+        assert_parity(C, C_ref, S_ref, f"bcsr {m}x{k} N={n}")
+    return outs, info
+
+
+@pytest.mark.parametrize("m,k,n,keep,dt,out_dt", [
+    (512, 512, 128, 0.5, "f16", "f32"),     # the BCSR tiny workload's shape
+    (300, 200, 72, 0.6, "bf16", "f32"),     # ragged M, K, N < 128
+    (640, 448, 264, 0.4, "bf16", "f32"),    # N spans two 256-wide tiles + tail
+    (256, 1024, 8, 0.3, "bf16", "f32"),     # N = 8
+    (192, 320, 256, 1.0, "f16", "bf16"),    # dense blocks everywhere, bf16 C
+    (130, 130, 136, 0.5, "bf16", "bf16"),   # partial last block row / column
+])
+def test_bcsr_parity_small(m, k, n, keep, dt, out_dt):
+    rng = np.random.default_rng(m * 31 + n)
+    rp, ci = W.block_pattern(rng, m, k, 64, 64, keep=keep)
+    vals = W.draw_values(rng, len(ci), "u1", dt)
+    B = W.dense_bits(rng, (k, n), "u1", dt)
+    full_check(m, k, n, rp, ci, vals, dt, out_dt, B)
+
+
+def test_bcsr_tiny_workload():
+    w = W.bcsr_tiny()
+    outs, info = full_check(w.m, w.k, w.n, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.B(), runs=2)
+    assert np.array_equal(outs[0], outs[1])  # deterministic
+    assert info["padding"] == 0  # every block is fully populated
+
+
+def test_bcsr_scattered_entries_and_empty_block_rows():
+    """Sparse entries inside blocks (padding zeros stored) and block rows with no block."""
+    rng = np.random.default_rng(5)
+    m, k, n = 448, 384, 200
+    rp, ci, vals = W.random_csr(rng, m, k, 0.01, "bf16")
+    # empty out rows 64..191 (two whole block rows)
+    keep = np.ones(len(ci), bool)
+    keep[rp[64]:rp[192]] = False
+    rows = np.repeat(np.arange(m), np.diff(rp))[keep]
+    rp2 = np.zeros(m + 1, np.int64)
+    np.cumsum(np.bincount(rows, minlength=m), out=rp2[1:])
+    full_check(m, k, n, rp2, ci[keep], vals[keep], "bf16", "f32", W.dense_bits(rng, (k, n), "n1", "bf16"))
+
+
+def test_bcsr_identity_exact():
+    m = 320
+    n = 136
+    rp = np.arange(m + 1, dtype=np.int64)
+    ci = np.arange(m, dtype=np.int32)
+    one = W.f32_to_bf16_bits(np.ones(m, np.float32))
+    rng = np.random.default_rng(3)
+    B = W.dense_bits(rng, (m, n), "n1", "bf16")
+    outs, _ = run_library("bcsr", m, m, rp, ci, one, "bf16", "f32", B)
+    assert np.array_equal(outs[0], W.bits_to_f32(B, "bf16").astype(np.float64))
+
+
+def test_bcsr_one_nonzero_per_row_exact():
+    """Products of two 16-bit floats are exact in fp32: C = a_i * B[c_i]."""
+    rng = np.random.default_rng(4)
+    m, k, n = 200, 500, 64
+    rp = np.arange(m + 1, dtype=np.int64)
+    ci = np.sort(rng.integers(0, k, m)).astype(np.int32)
+    vals = W.draw_values(rng, m, "u1", "f16")
+    B = W.dense_bits(rng, (k, n), "u1", "f16")
+    outs, _ = run_library("bcsr", m, k, rp, ci, vals, "f16", "f32", B)
+    ref = vals.view(np.float16).astype(np.float64)[:, None] * B.view(np.float16).astype(np.float64)[ci]
+    assert np.array_equal(outs[0], ref)
+
+
+def test_bcsr_all_zero_matrix_writes_zeros():
+    m, k, n = 130, 70, 24
+    rp = np.zeros(m + 1, np.int64)
+    B = W.dense_bits(np.random.default_rng(1), (k, n), "u1", "bf16")
+    outs, _ = run_library("bcsr", m, k, rp, np.zeros(0, np.int32), np.zeros(0, np.uint16), "bf16", "f32", B)
+    assert np.array_equal(outs[0], np.zeros((m, n)))
+
+
+def sampled_check(w, nsamp=6000, seed=0):
+    import torch
+    outs, info = run_library("bcsr", w.m, w.k, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.B(),
+                             keep_device=True)
+    C = outs[0]
+    assert not torch.isnan(C).any().item(), "C not fully written"
+    rng = np.random.default_rng(seed)
+    rows = rng.integers(0, w.m, nsamp)
+    cols = rng.integers(0, w.n, nsamp)
+    Cs = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
+    ref, S = oracle.spmm_csr_sample(w.m, w.k, w.row_ptr, w.col_idx, w.vals, ocode(w.dtype), w.B(), rows, cols)
+    assert_parity(Cs, ref, S, w.name)
+    return info
+
+
+@pytest.mark.parametrize("sp", W.BCSR_SWEEP_SPARSITY)
+def test_bcsr_sweep_full_size_sampled(sp):
+    for n in (8, 256):
+        sampled_check(W.bcsr_sweep(sp, n))
+
+
+def test_bcsr_weight_like_full_size_sampled():
+    w = W.bcsr_weight()
+    info = sampled_check(w, nsamp=20000)
+    assert info["n_units"] == 1658

@@ -1,0 +1,118 @@
+"""WCSR kernel (and its split-window reduction) parity with the oracle on
+the GPU, through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+import spmm_workloads as W
+from spmm_testlib import assert_parity, ensure_library, ocode, run_library
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    ensure_library()
+
+
+def full_check(m, k, n, rp, ci, vals, dt, out_dt, B, split_cols=None, runs=1):
+    outs, info = run_library("wcsr", m, k, rp, ci, vals, dt, out_dt, B, split_cols=split_cols, runs=runs)
+    C_ref, S_ref = oracle.spmm_csr(m, k, rp, ci, vals, ocode(dt), B)
+    for C in outs:
+        assert_parity(C, C_ref, S_ref, f"wcsr {m}x{k} N={n}")
+    return outs, info
+
+
+@pytest.mark.parametrize("m,k,n,d,dt,out_dt", [
+    (512, 512, 128, 0.05, "bf16", "f32"),
+    (1000, 3000, 256, 0.01, "bf16", "f32"),
+    (333, 777, 72, 0.03, "f16", "f32"),       # ragged window, N < 128
+    (256, 2048, 264, 0.02, "bf16", "bf16"),   # two column tiles + tail, bf16 C
+    (64, 64, 8, 0.2, "bf16", "f32"),          # N = 8
+])
+def test_wcsr_parity_small(m, k, n, d, dt, out_dt):
+    rng = np.random.default_rng(m + 17 * n)
+    rp, ci, vals = W.random_csr(rng, m, k, d, dt)
+    B = W.dense_bits(rng, (k, n), "n1", dt)
+    full_check(m, k, n, rp, ci, vals, dt, out_dt, B)
+
+
+@pytest.mark.parametrize("split,n", [(64, 256), (128, 128), (512, 72)])
+def test_wcsr_split_windows(split, n):
+    """Force long windows to be split; the two-pass sum must match and be
+    bitwise reproducible."""
+    rng = np.random.default_rng(split)
+    m, k = 400, 5000
+    rp, ci = W.powerlaw_pattern(rng, m, k, 1.3, 1, 1500, 300, 0.7)
+    vals = W.draw_values(rng, len(ci), "u1", "bf16")
+    B = W.dense_bits(rng, (k, n), "u1", "bf16")
+    outs, info = full_check(m, k, n, rp, ci, vals, "bf16", "f32", B, split_cols=split, runs=2)
+    assert info["n_split_windows"] > 0
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_wcsr_empty_windows_and_identity():
+    m = 300
+    n = 24
+    rp = np.arange(m + 1, dtype=np.int64)
+    ci = np.arange(m, dtype=np.int32)
+    one = W.f32_to_bf16_bits(np.ones(m, np.float32))
+    # drop rows 32..95 (four windows) to get empty windows
+    keep = np.ones(m, bool)
+    keep[32:96] = False
+    rows = np.nonzero(keep)[0]
+    rp2 = np.zeros(m + 1, np.int64)
+    np.cumsum(np.bincount(rows, minlength=m), out=rp2[1:])
+    B = W.dense_bits(np.random.default_rng(2), (m, n), "n1", "bf16")
+    outs, _ = run_library("wcsr", m, m, rp2, ci[keep], one[keep], "bf16", "f32", B)
+    ref = W.bits_to_f32(B, "bf16").astype(np.float64)
+    ref[32:96] = 0
+    assert np.array_equal(outs[0], ref)
+
+
+def test_wcsr_one_nonzero_per_row_exact():
+    rng = np.random.default_rng(9)
+    m, k, n = 257, 900, 136
+    rp = np.arange(m + 1, dtype=np.int64)
+    ci = rng.integers(0, k, m).astype(np.int32)
+    vals = W.draw_values(rng, m, "u1", "f16")
+    B = W.dense_bits(rng, (k, n), "u1", "f16")
+    outs, _ = run_library("wcsr", m, k, rp, ci, vals, "f16", "f32", B, split_cols=64)
+    ref = vals.view(np.float16).astype(np.float64)[:, None] * B.view(np.float16).astype(np.float64)[ci]
+    assert np.array_equal(outs[0], ref)
+
+
+def sampled_check(w, nsamp=8000, seed=0, split_cols=None):
+    import torch
+    outs, info = run_library("wcsr", w.m, w.k, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.B(),
+                             keep_device=True, split_cols=split_cols)
+    C = outs[0]
+    assert not torch.isnan(C).any().item(), "C not fully written"
+    rng = np.random.default_rng(seed)
+    rows = rng.integers(0, w.m, nsamp)
+    cols = rng.integers(0, w.n, nsamp)
+    Cs = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
+    ref, S = oracle.spmm_csr_sample(w.m, w.k, w.row_ptr, w.col_idx, w.vals, ocode(w.dtype), w.B(), rows, cols)
+    assert_parity(Cs, ref, S, w.name)
+    return info
+
+
+def test_wcsr_uniform_full_size():
+    w = W.wcsr_uniform()
+    outs, info = full_check(w.m, w.k, w.n, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.B())
+    assert info["n_groups"] == 1024
+
+
+def test_wcsr_irregular_full_size_sampled():
+    w = W.wcsr_irregular()
+    info = sampled_check(w, nsamp=20000)
+    assert info["n_split_windows"] > 0  # the longest windows are split
+
+
+@pytest.mark.parametrize("dens", W.WCSR_SWEEP_DENSITY)
+def test_wcsr_sweep_full_size_sampled(dens):
+    for n in (8, 256):
+        sampled_check(W.wcsr_sweep(dens, n))
