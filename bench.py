@@ -174,6 +174,10 @@ def run_ours(args, rank, world):
             e1.record(stream)
             times.setdefault(p["name"], []).append((e0, e1))
 
+    clk = ClockSampler(dev).__enter__()
+    t_first = time.perf_counter()
+    while not clk.lines and time.perf_counter() - t_first < 2.0:
+        time.sleep(0.05)  # let nvidia-smi produce its first sample
     for _ in range(args.warmup):
         one_step({})
     stream.synchronize()
@@ -188,7 +192,7 @@ def run_ours(args, rank, world):
         tdist.barrier()
     torch.cuda.synchronize()
     times = {}
-    with ClockSampler(dev) as clk:
+    with clk:
         t_wall0 = time.perf_counter()
         for _ in range(args.steps):
             one_step(times)
@@ -299,30 +303,41 @@ def run_ours(args, rank, world):
 
 # ---------------------------------------------------------------- oracle arm
 def cpu_baseline_sample(parts_workloads, budget_s=10.0, offset=0):
-    """Time the oracle's fp64 SpMM on a row sample of each part, sized to
-    about budget_s seconds of CPU work in total; returns the cpu_baseline dict."""
+    """Time the oracle's fp64 SpMM on a row sample of each part, about
+    budget_s seconds of CPU work in total (whole matrices are repeated when
+    they take less); returns the cpu_baseline dict."""
     import oracle
     oracle.build()
     threads = oracle.num_threads()
     flops = 0.0
     t = 0.0
     desc = []
+    want = budget_s / len(parts_workloads)
     for w in parts_workloads:
         B = w.B()
         per_row = 2.0 * w.nnz / max(w.m, 1) * w.n
-        # calibrate on a small slice, then take a slice worth budget/len(parts)
-        rows = max(1, min(w.m, int(2e8 / max(per_row, 1))))
-        r0 = (offset * rows) % max(w.m - rows + 1, 1)
-        dt = _time_rows(oracle, w, B, r0, rows, threads)
-        rate = (2.0 * (w.row_ptr[r0 + rows] - w.row_ptr[r0]) * w.n) / max(dt, 1e-9)
-        want = budget_s / len(parts_workloads)
-        rows2 = max(1, min(w.m, int(want * rate / max(per_row, 1))))
-        r0 = (offset * rows2) % max(w.m - rows2 + 1, 1)
-        dt = _time_rows(oracle, w, B, r0, rows2, threads)
-        fl = 2.0 * (w.row_ptr[r0 + rows2] - w.row_ptr[r0]) * w.n
+        rows = max(1, min(w.m, int(5e7 / max(per_row, 1))))
+        while True:
+            r0 = (offset * rows) % max(w.m - rows + 1, 1)
+            dt = _time_rows(oracle, w, B, r0, rows, threads)
+            if rows >= w.m or dt >= 0.25 * want:
+                break
+            rows = min(w.m, rows * 4)
+        reps = 1
+        if dt < want:
+            if rows < w.m:
+                rows = min(w.m, int(rows * want / max(dt, 1e-6)))
+                r0 = (offset * rows) % max(w.m - rows + 1, 1)
+            else:
+                reps = max(1, int(want / max(dt, 1e-6)))
+        tt = 0.0
+        for _ in range(reps):
+            tt += _time_rows(oracle, w, B, r0, rows, threads)
+        fl = 2.0 * float(w.row_ptr[r0 + rows] - w.row_ptr[r0]) * w.n * reps
         flops += fl
-        t += dt
-        desc.append(f"{w.name}: rows {r0}..{r0 + rows2 - 1} of {w.m} ({fl / 2 / w.n:.0f} nnz x N={w.n})")
+        t += tt
+        desc.append(f"{w.name}: rows {r0}..{r0 + rows - 1} of {w.m} x{reps} "
+                    f"({int(w.row_ptr[r0 + rows] - w.row_ptr[r0])} nnz, N={w.n})")
     return {"value": round(flops / t / 1e12, 6), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": "; ".join(desc), "seconds": round(t, 3)}
 
@@ -442,8 +457,8 @@ def run_sweep(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

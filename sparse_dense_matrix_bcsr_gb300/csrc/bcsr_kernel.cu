@@ -12,7 +12,13 @@
 // runs over the 128 TMEM lanes, and the 64 rows of a block row are the MMA's
 // N.  B tiles are MN-major MMA operands, blocks K-major ones.
 //
-// CTA = one block row x one tile of BN = 128*NACC columns of C; 6 warps:
+// Work unit ("tile") = one block row x one tile of BN = 128*NACC columns of
+// C.  The kernel is persistent: CTA c takes tiles c, c + G, c + 2G, ... (G =
+// grid size), consecutive tile ids share a column tile so that concurrently
+// running CTAs read the same slice of B from L2.  Two TMEM accumulators
+// alternate between tiles, so the epilogue of one tile overlaps the loads and
+// MMAs of the next (the paper's non-persistent grid cannot overlap them when
+// one CTA fills an SM).  6 warps:
 //   warp 0      TMA producer (lane 0 issues; the warp shares index loads)
 //   warp 1      TMEM allocator and MMA issuer (lane 0 issues)
 //   warps 2..5  epilogue: TMEM -> registers -> C (warp w reads lanes of
@@ -30,15 +36,16 @@ constexpr int kBlk = 64;                      // block rows = block cols = K per
 constexpr int kBlkBytes = kBlk * kBlk * 2;    // one 64x64 16-bit block
 constexpr int kChunkBytes = 64 * 64 * 2;      // 64 rows (k) x 64 columns (n) of B
 constexpr int kThreads = 192;
+constexpr int kEpiWarps = 4;
 
 template <int NACC, int Q>
 struct Cfg {
   static constexpr int kBN = 128 * NACC;
   static constexpr int kChunks = 2 * NACC;
   static constexpr int kStageBytes = kBlkBytes + kChunks * kChunkBytes;
-  static constexpr int kTmemCols = NACC == 1 ? 64 : 128;
-  static constexpr int kBarBytes = 1024;
-  static constexpr int kSmemBytes = Q * kStageBytes + kBarBytes + 1024;  // + alignment slack
+  static constexpr int kAccCols = 64 * NACC;               // TMEM columns of one accumulator set
+  static constexpr int kTmemCols = NACC == 1 ? 128 : 256;  // two sets
+  static constexpr int kSmemBytes = Q * kStageBytes + 1024 + 1024;  // + barriers + alignment slack
 };
 
 template <bool OUT_BF16>
@@ -57,32 +64,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Q * C_::kStageBytes);
-  // bars[0..Q): full, bars[Q..2Q): empty, bars[2Q]: accumulator ready, bars[2Q+1]: drain
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Q + 2);
+  // bars: full[Q], empty[Q], acc_full[2], acc_empty[2], drain
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Q + 5);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int br = blockIdx.x;
-  const int n0 = blockIdx.y * C_::kBN;
-  const int64_t jb = p.block_row_ptr[br];
-  const int64_t je = p.block_row_ptr[br + 1];
-  const int nblk = static_cast<int>(je - jb);
-  const int nvalid = min(C_::kBN, p.N - n0);
-  const int nch = min(C_::kChunks, (nvalid + 63) / 64);   // B chunks that hold valid columns
-  const int nacc = min(NACC, (nvalid + 127) / 128);       // accumulators that hold valid columns
+  const int64_t n_tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + C_::kBN - 1) / C_::kBN);
 
   const uint32_t full0 = smem_addr(&bars[0]);
   const uint32_t empty0 = smem_addr(&bars[Q]);
-  const uint32_t accum_bar = smem_addr(&bars[2 * Q]);
-  const uint32_t drain_bar = smem_addr(&bars[2 * Q + 1]);
+  const uint32_t accf0 = smem_addr(&bars[2 * Q]);
+  const uint32_t acce0 = smem_addr(&bars[2 * Q + 2]);
+  const uint32_t drain_bar = smem_addr(&bars[2 * Q + 4]);
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < Q; ++q) {
       mbar_init(full0 + 8 * q, 1);
       mbar_init(empty0 + 8 * q, 1);
     }
-    mbar_init(accum_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, kEpiWarps);
+    }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -103,31 +107,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stage = 0, phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    for (int64_t jbase = jb; jbase < je && ok; jbase += 32) {
-      // The warp loads the next 32 block-column indices at once.
-      const int64_t jl = jbase + lane;
-      const int32_t my_col = jl < je ? p.block_col_idx[jl] : 0;
-      const int cnt = (je - jbase) < 32 ? static_cast<int>(je - jbase) : 32;
-      for (int t = 0; t < cnt; ++t) {
-        const int32_t bcol = __shfl_sync(0xffffffffu, my_col, t);
-        if (lane == 0) {
-          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns) || *abort_flag) {
-            ok = false;
-          } else {
-            const uint32_t fb = full0 + 8 * stage;
-            const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
-            mbar_arrive_expect_tx(fb, kBlkBytes + nch * kChunkBytes);
-            tma_load_2d(st, &tmA, fb, 0, static_cast<int32_t>((jbase + t) * kBlk));
-            for (int c = 0; c < nch; ++c)
-              tma_load_2d(st + kBlkBytes + c * kChunkBytes, &tmB, fb, n0 + c * 64, bcol * kBlk);
-            ++issued;
+    for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      const int br = static_cast<int>(t % p.n_block_rows);
+      const int n0 = static_cast<int>(t / p.n_block_rows) * C_::kBN;
+      const int nch = min(C_::kChunks, (p.N - n0 + 63) / 64);
+      const int64_t jb = p.block_row_ptr[br];
+      const int64_t je = p.block_row_ptr[br + 1];
+      for (int64_t jbase = jb; jbase < je && ok; jbase += 32) {
+        // The warp loads the next 32 block-column indices at once.
+        const int64_t jl = jbase + lane;
+        const int32_t my_col = jl < je ? p.block_col_idx[jl] : 0;
+        const int cnt = (je - jbase) < 32 ? static_cast<int>(je - jbase) : 32;
+        for (int i = 0; i < cnt; ++i) {
+          const int32_t bcol = __shfl_sync(0xffffffffu, my_col, i);
+          if (lane == 0) {
+            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns) || *abort_flag) {
+              ok = false;
+            } else {
+              const uint32_t fb = full0 + 8 * stage;
+              const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
+              mbar_arrive_expect_tx(fb, kBlkBytes + nch * kChunkBytes);
+              tma_load_2d(st, &tmA, fb, 0, static_cast<int32_t>((jbase + i) * kBlk));
+              for (int c = 0; c < nch; ++c)
+                tma_load_2d(st + kBlkBytes + c * kChunkBytes, &tmB, fb, n0 + c * 64, bcol * kBlk);
+              ++issued;
+            }
           }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        if (++stage == Q) {
-          stage = 0;
-          phase ^= 1u;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (++stage == Q) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
     }
@@ -141,82 +152,118 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nblk > 0) {
+    if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(IN_BF16, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, 64);
       uint32_t stage = 0, phase = 0;
+      uint32_t tcount = 0;  // non-empty tiles processed
       bool ok = true;
-      for (int t = 0; t < nblk; ++t) {
-        if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns) || *abort_flag) {
+      for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        const int br = static_cast<int>(t % p.n_block_rows);
+        const int n0 = static_cast<int>(t / p.n_block_rows) * C_::kBN;
+        const int nacc = min(NACC, (p.N - n0 + 127) / 128);
+        const int nblk = static_cast<int>(p.block_row_ptr[br + 1] - p.block_row_ptr[br]);
+        if (nblk == 0) continue;
+        const uint32_t buf = tcount & 1u;
+        const uint32_t use = tcount >> 1;
+        // Wait until the epilogue has drained this accumulator set.
+        if (!mbar_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, p.wait_limit_ns) || *abort_flag) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        const uint32_t a_blk = smem_addr(smem + stage * C_::kStageBytes);  // A block: MMA operand B
-        const uint32_t b_til = a_blk + kBlkBytes;                          // B tile:  MMA operand A
+        const uint32_t acc = tmem + buf * C_::kAccCols;
+        for (int j = 0; j < nblk; ++j) {
+          if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_blk = smem_addr(smem + stage * C_::kStageBytes);  // A block: MMA operand B
+          const uint32_t b_til = a_blk + kBlkBytes;                          // B tile:  MMA operand A
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t bdesc = smem_desc_sw128(a_blk + kk * 32, 16, 1024);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bdesc = smem_desc_sw128(a_blk + kk * 32, 16, 1024);
 #pragma unroll
-          for (int a = 0; a < NACC; ++a) {
-            if (a < nacc) {
-              const uint64_t adesc = smem_desc_sw128(b_til + a * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
-              umma_f16(tmem + a * 64, adesc, bdesc, idesc, (t > 0 || kk > 0) ? 1u : 0u);
+            for (int a = 0; a < NACC; ++a) {
+              if (a < nacc) {
+                const uint64_t adesc =
+                    smem_desc_sw128(b_til + a * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
+                umma_f16(acc + a * 64, adesc, bdesc, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+              }
             }
           }
+          umma_commit(empty0 + 8 * stage);  // frees the stage once these MMAs have read it
+          if (++stage == Q) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        umma_commit(empty0 + 8 * stage);  // frees the stage once these MMAs have read it
-        if (++stage == Q) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (!ok) break;
+        umma_commit(accf0 + 8 * buf);  // accumulator set ready for the epilogue
+        ++tcount;
       }
-      if (ok) {
-        umma_commit(accum_bar);
-      } else {
+      if (!ok) {
         atomicOr(p.status, kDevTimeout);
         *abort_flag = 1;
         umma_commit(drain_bar);
         mbar_wait(drain_bar, 0, 1000000ull);
-        mbar_arrive(accum_bar);  // release the epilogue
+        // release the epilogue of the tile that will not complete
+        mbar_arrive(accf0);
+        mbar_arrive(accf0 + 8);
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
     const int sp = warp & 3;  // TMEM sub-partition this warp may read
-    const int row0 = br * kBlk;
-    if (nblk == 0) {
-      for (int a = 0; a < nacc; ++a) {
-        const int n = n0 + a * 128 + sp * 32 + lane;
-        if (n < p.N)
-          for (int r = 0; r < kBlk && row0 + r < p.M; ++r)
-            store_c<OUT_BF16>(p.C, static_cast<int64_t>(row0 + r) * p.ldc + n, 0.0f);
-      }
-    } else {
-      const bool ok = mbar_wait(accum_bar, 0, p.wait_limit_ns);
-      if (!ok) {
-        atomicOr(p.status, kDevTimeout);
-        *abort_flag = 1;
-      } else if (!*abort_flag) {
-        tc_fence_after_sync();
+    uint32_t tcount = 0;
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
+      const int br = static_cast<int>(t % p.n_block_rows);
+      const int n0 = static_cast<int>(t / p.n_block_rows) * C_::kBN;
+      const int nacc = min(NACC, (p.N - n0 + 127) / 128);
+      const int nblk = static_cast<int>(p.block_row_ptr[br + 1] - p.block_row_ptr[br]);
+      const int row0 = br * kBlk;
+      if (nblk == 0) {
         for (int a = 0; a < nacc; ++a) {
           const int n = n0 + a * 128 + sp * 32 + lane;
-          const bool nok = n < p.N;
+          if (n < p.N)
+            for (int r = 0; r < kBlk && row0 + r < p.M; ++r)
+              store_c<OUT_BF16>(p.C, static_cast<int64_t>(row0 + r) * p.ldc + n, 0.0f);
+        }
+        continue;
+      }
+      const uint32_t buf = tcount & 1u;
+      const uint32_t use = tcount >> 1;
+      if (!mbar_wait(accf0 + 8 * buf, use & 1u, p.wait_limit_ns)) {
+        atomicOr(p.status, kDevTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      if (*abort_flag) break;
+      tc_fence_after_sync();
+      const uint32_t acc = tmem + buf * C_::kAccCols + (static_cast<uint32_t>(sp * 32) << 16);
+      for (int a = 0; a < nacc; ++a) {
+        const int n = n0 + a * 128 + sp * 32 + lane;
+        const bool nok = n < p.N;
 #pragma unroll
-          for (int cb = 0; cb < kBlk / 16; ++cb) {
-            uint32_t v[16];
-            tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(sp * 32) << 16) + a * 64 + cb * 16, v);
-            tmem_ld_wait();
-            if (nok) {
+        for (int cb = 0; cb < kBlk / 16; ++cb) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(acc + a * 64 + cb * 16, v);
+          tmem_ld_wait();
+          if (nok) {
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int r = row0 + cb * 16 + i;
-                if (r < p.M) store_c<OUT_BF16>(p.C, static_cast<int64_t>(r) * p.ldc + n, __uint_as_float(v[i]));
-              }
+            for (int i = 0; i < 16; ++i) {
+              const int r = row0 + cb * 16 + i;
+              if (r < p.M) store_c<OUT_BF16>(p.C, static_cast<int64_t>(r) * p.ldc + n, __uint_as_float(v[i]));
             }
           }
         }
       }
+      // This warp's reads of the accumulator set are complete.
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8 * buf);
+      ++tcount;
     }
   }
 
@@ -239,8 +286,9 @@ cudaError_t launch_variant(const CUtensorMap &tmA, const CUtensorMap &tmB, const
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(p.n_block_rows, (p.N + C_::kBN - 1) / C_::kBN);
-  kern<<<grid, kThreads, C_::kSmemBytes, stream>>>(tmA, tmB, p);
+  const int64_t tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + C_::kBN - 1) / C_::kBN);
+  const int64_t grid = tiles < p.max_ctas ? tiles : p.max_ctas;
+  kern<<<static_cast<unsigned>(grid), kThreads, C_::kSmemBytes, stream>>>(tmA, tmB, p);
   return cudaGetLastError();
 }
 

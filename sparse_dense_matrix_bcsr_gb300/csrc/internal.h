@@ -15,6 +15,7 @@ struct BcsrParams {
   int64_t ldc;                   // row stride of C in elements (= N)
   int32_t M, N;
   int32_t n_block_rows;
+  int32_t max_ctas;              // persistent grid size (one CTA per SM)
   uint32_t *status;              // device status word
   uint64_t wait_limit_ns;        // bound of every mbarrier wait
 };
@@ -55,10 +56,11 @@ struct WcsrParams {
   uint64_t wait_limit_ns;
 };
 
-// tmV covers the values array as [16 rows, P_total cols] with 64 x 16 boxes
-// and 128-byte swizzle.
-cudaError_t launch_wcsr(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
-                        cudaStream_t stream);
+// tmV covers the values array as [16 rows, P_total cols] with 64 x 16 boxes;
+// tmB covers B as [K rows, N cols] with 64 x 1 boxes (row gathers); both with
+// 128-byte swizzle.
+cudaError_t launch_wcsr(const CUtensorMap &tmV, const CUtensorMap &tmB, const WcsrParams &p, bool in_bf16,
+                        bool out_bf16, cudaStream_t stream);
 
 // Sum the partials of split windows into C in slot order.
 cudaError_t launch_wcsr_reduce(const WcsrSplit *splits, int32_t n_splits, const float *workspace,

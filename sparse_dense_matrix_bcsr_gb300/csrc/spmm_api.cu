@@ -260,6 +260,7 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
     p.M = static_cast<int32_t>(h->m);
     p.N = static_cast<int32_t>(N);
     p.n_block_rows = static_cast<int32_t>(h->n_groups);
+    p.max_ctas = std::max(h->num_sms, 1);
     p.status = h->d_status;
     p.wait_limit_ns = h->wait_limit_ns;
     cudaError_t e = spmm::launch_bcsr(h->tm_vals, h->tm_B, p, in_bf16, out_bf16, s);
@@ -277,6 +278,13 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
     CUDA_TRY(cudaMalloc(&h->d_ws, need), "cudaMalloc(split workspace)");
     h->ws_bytes = need;
   }
+  if (h->b_cached != B || h->n_cached != N) {
+    spmm_status st = encode_2d(&h->tm_B, B, in_bf16, static_cast<uint64_t>(std::max<int64_t>(h->k, 1)),
+                               static_cast<uint64_t>(N), static_cast<uint64_t>(N), 1, 64);
+    if (st != SPMM_OK) return st;
+    h->b_cached = B;
+    h->n_cached = N;
+  }
   spmm::WcsrParams p;
   p.tasks = h->d_tasks;
   p.window_col_idx = h->d_idx;
@@ -290,7 +298,7 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
   p.n_tasks = static_cast<int32_t>(h->tasks.size());
   p.status = h->d_status;
   p.wait_limit_ns = h->wait_limit_ns;
-  cudaError_t e = spmm::launch_wcsr(h->tm_vals, p, in_bf16, out_bf16, s);
+  cudaError_t e = spmm::launch_wcsr(h->tm_vals, h->tm_B, p, in_bf16, out_bf16, s);
   if (e != cudaSuccess) return cuda_fail(e, "WCSR kernel launch");
   e = spmm::launch_wcsr_reduce(h->d_splits, static_cast<int32_t>(h->splits.size()), h->d_ws, C, p.M, p.N, out_bf16, s);
   if (e != cudaSuccess) return cuda_fail(e, "WCSR reduce launch");

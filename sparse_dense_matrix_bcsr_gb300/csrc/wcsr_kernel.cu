@@ -1,24 +1,26 @@
 // wcsr_kernel.cu -- WCSR SpMM for sm_103a.
 //
 // Method: "AsyncSparse", Section III-B (the packed value tile of a window is
-// contiguous and loaded by TMA; the matching rows of B are gathered through
-// window_col_idx by all threads into shared memory with the 128-byte swizzle
-// applied by hand) and Section III-C (task-based decomposition: long windows
-// are split into fixed-size sub-tasks and the CTA index names a task).  The
-// paper adds split partial sums with atomicAdd; here a split task writes an
-// fp32 partial and a second kernel adds a window's partials in slot order, so
-// results are bitwise reproducible.
+// contiguous and loaded by TMA; the matching rows of B are fetched through
+// window_col_idx) and Section III-C (task-based decomposition: long windows
+// are split into fixed-size sub-tasks and the CTA index names a task).  On
+// Hopper the paper gathers B with all threads of a warpgroup because TMA
+// cannot gather; sm_103a's TMA can (tile::gather4, four rows per
+// instruction), so here one producer warp issues every load, as in the BCSR
+// kernel, and the MMA runs decoupled behind an mbarrier ring.  The paper adds
+// split partial sums with atomicAdd; here a split task writes an fp32 partial
+// and a second kernel adds a window's partials in slot order, so results are
+// bitwise reproducible.
 //
-// As in the BCSR kernel the product is computed transposed: the 128 columns of
-// an accumulator are the MMA's M (TMEM lanes) and the 16 rows of a window are
-// the MMA's N, so a 16-row window is a legal tcgen05 shape (M >= 64 would
-// otherwise waste 3/4 of the MMA).
+// The product is computed transposed: the 128 columns of an accumulator are
+// the MMA's M (TMEM lanes) and the 16 rows of a window are the MMA's N, so a
+// 16-row window is a legal tcgen05 shape.
 //
-// CTA = one task x one tile of BN = 128*NACC columns; 5 warps:
-//   warps 0..3  gather producers (cp.async, 16 B per copy), warp 0 lane 0
-//               also issues the TMA for the value tile; afterwards the same
-//               warps are the epilogue (warp w reads TMEM sub-partition w)
-//   warp 4      TMEM allocator and MMA issuer
+// CTA = one task x one tile of BN = 128*NACC columns; 6 warps:
+//   warp 0      producer: value tile (2-D TMA) and B rows (TMA gather4); the
+//               warp prefetches the column indices PF stages ahead
+//   warp 1      TMEM allocator and MMA issuer
+//   warps 2..5  epilogue (warp w reads TMEM sub-partition w % 4)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -32,9 +34,8 @@ constexpr int kH = 16;                       // window height
 constexpr int kKC = 64;                      // packed columns per stage
 constexpr int kValBytes = kH * kKC * 2;      // 2 KB value tile per stage
 constexpr int kChunkBytes = kKC * 64 * 2;    // 64 gathered rows x 64 columns
-constexpr int kProducerWarps = 4;
-constexpr int kThreads = 32 * (kProducerWarps + 1);
-constexpr int kLag = 2;                      // cp.async groups kept in flight per thread
+constexpr int kThreads = 192;
+constexpr int kPF = 4;                       // index prefetch distance (stages)
 
 template <int NACC, int Q>
 struct Cfg {
@@ -43,7 +44,6 @@ struct Cfg {
   static constexpr int kStageBytes = kValBytes + kChunks * kChunkBytes;
   static constexpr int kTmemCols = 32;  // NACC * 16 <= 32
   static constexpr int kSmemBytes = Q * kStageBytes + 1024 + 1024;
-  static_assert(kLag < Q, "the producer must not wait on a stage it has not released");
 };
 
 template <bool OUT_BF16>
@@ -56,7 +56,8 @@ __device__ __forceinline__ void store_out(void *C, int64_t off, float v) {
 
 template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    wcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmV, const WcsrParams p) {
+    wcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
+                     const WcsrParams p) {
   using C_ = Cfg<NACC, Q>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -70,6 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n0 = blockIdx.y * C_::kBN;
   const int nvalid = min(C_::kBN, p.N - n0);
   const int nacc = min(NACC, (nvalid + 127) / 128);
+  const int nch = min(C_::kChunks, (nvalid + 63) / 64);
   const int64_t ncols = task.p_end - task.p_begin;
   const int nstages = static_cast<int>((ncols + kKC - 1) / kKC);
 
@@ -80,7 +82,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < Q; ++q) {
-      mbar_init(full0 + 8 * q, kProducerWarps + 1);  // one arrive per gather warp + the TMA arrive
+      mbar_init(full0 + 8 * q, 1);
       mbar_init(empty0 + 8 * q, 1);
     }
     mbar_init(accum_bar, 1);
@@ -88,8 +90,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmB);
   }
-  if (warp == kProducerWarps) {
+  if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), C_::kTmemCols);
     tmem_relinquish();
   }
@@ -98,79 +101,71 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < kProducerWarps) {
-    // ------------------------------------------------------------ gather
-    // Copy layout: one 16-byte piece = 8 consecutive columns of one B row.
-    // A row of the tile has BN/8 pieces; 32/(BN/8/...) rows per warp step.
-    constexpr int kPiecesPerRow = C_::kBN / 8;             // 16 or 32
-    constexpr int kRowsPerStep = 32 / kPiecesPerRow;       // rows one warp copies per instruction
-    constexpr int kRowsPerWarp = kKC / kProducerWarps;     // 16
-    const int piece = lane % kPiecesPerRow;
-    const int sub = lane / kPiecesPerRow;
-    const int ncol = n0 + piece * 8;                       // first column of this lane's piece
-    const bool col_ok = ncol < p.N;
-    const uint16_t *Bp = reinterpret_cast<const uint16_t *>(p.B);
-    const int chunk = piece / 8;                           // 64-column chunk of the piece
-    const uint32_t unit = static_cast<uint32_t>(piece % 8);
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // Lane l gathers row group g = l % 16 (rows 4g..4g+3 of a stage) for the
+    // column chunks of its half-warp.
+    const int g = lane & 15;
+    constexpr int kChunksPerLane = C_::kChunks / 2;
+    const int c_first = (lane >> 4) * kChunksPerLane;
+    const int32_t oob_row = p.K;  // padding (-1) gathers an out-of-range row: TMA fills zeros
+    auto load_idx = [&](int s) -> int4 {
+      const int64_t pb = task.p_begin + static_cast<int64_t>(s) * kKC + 4 * g;
+      if (s < nstages && pb < task.p_end) return *reinterpret_cast<const int4 *>(p.window_col_idx + pb);
+      return make_int4(-2, -2, -2, -2);
+    };
+    int4 ring[kPF];
+#pragma unroll
+    for (int i = 0; i < kPF; ++i) ring[i] = load_idx(i);
 
     uint32_t stage = 0, phase = 0;
+    int64_t issued = 0;
     bool ok = true;
-    int s = 0;
-    for (; s < nstages; ++s) {
+    for (int s = 0; s < nstages; ++s) {
+      const int4 cur = ring[0];
+#pragma unroll
+      for (int i = 0; i + 1 < kPF; ++i) ring[i] = ring[i + 1];
+      ring[kPF - 1] = load_idx(s + kPF);
+
       if (lane == 0) ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns) && !*abort_flag;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const int64_t pbase = task.p_begin + static_cast<int64_t>(s) * kKC;
+      const int64_t left = task.p_end - pbase;
+      const int groups = left >= kKC ? kKC / 4 : static_cast<int>(left / 4);
       const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
-      if (warp == 0 && lane == 0) {
-        const uint32_t fb = full0 + 8 * stage;
-        mbar_arrive_expect_tx(fb, kValBytes);
+      const uint32_t fb = full0 + 8 * stage;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(fb, kValBytes + groups * 4 * 128 * nch);
         tma_load_2d(st, &tmV, fb, static_cast<int32_t>(pbase), 0);
       }
-      // Column indices of this warp's 16 rows of the stage.
-      const int64_t my_p = pbase + warp * kRowsPerWarp + (lane & 15);
-      const int32_t my_idx = (lane < 16 && my_p < task.p_end) ? p.window_col_idx[my_p] : -2;
-      const uint32_t gath = st + kValBytes + chunk * kChunkBytes;
+      __syncwarp();
+      if (g < groups) {
+        const int32_t r0 = cur.x < 0 ? oob_row : cur.x;
+        const int32_t r1 = cur.y < 0 ? oob_row : cur.y;
+        const int32_t r2 = cur.z < 0 ? oob_row : cur.z;
+        const int32_t r3 = cur.w < 0 ? oob_row : cur.w;
 #pragma unroll
-      for (int rr = 0; rr < kRowsPerWarp; rr += kRowsPerStep) {
-        const int rloc = rr + sub;                         // row within this warp's 16
-        const int32_t col = __shfl_sync(0xffffffffu, my_idx, rloc);
-        if (col != -2) {                                   // -2: past the task's end, not read by the MMA
-          const int k = warp * kRowsPerWarp + rloc;        // row within the stage
-          const uint32_t dst = gath + k * 128 + ((unit ^ static_cast<uint32_t>(k & 7)) << 4);
-          const bool live = col_ok && col >= 0;
-          const void *src = live ? static_cast<const void *>(Bp + static_cast<int64_t>(col) * p.N + ncol)
-                                 : static_cast<const void *>(Bp);
-          cp_async_16(dst, src, live ? 16u : 0u);
+        for (int j = 0; j < kChunksPerLane; ++j) {
+          const int c = c_first + j;
+          if (c < nch)
+            tma_gather4(st + kValBytes + c * kChunkBytes + g * 512, &tmB, fb, n0 + c * 64, r0, r1, r2, r3);
         }
       }
-      cp_async_commit();
-      if (s >= kLag) {
-        cp_async_wait<kLag>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full0 + 8 * ((stage + Q - kLag) % Q));
-      }
+      ++issued;
       if (++stage == Q) {
         stage = 0;
         phase ^= 1u;
       }
     }
-    // Release the stages still pending.
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    __syncwarp();
-    {
-      const int done = s;  // stages issued
-      const int first = done > kLag ? done - kLag : 0;
-      for (int t = first; t < done; ++t)
-        if (lane == 0) mbar_arrive(full0 + 8 * (t % Q));
-    }
     if (!ok && lane == 0) {
       atomicOr(p.status, kDevTimeout);
       *abort_flag = 1;
+      const int64_t first = issued > Q ? issued - Q : 0;
+      for (int64_t i = first; i < issued; ++i)
+        mbar_wait(full0 + 8 * (i % Q), static_cast<uint32_t>((i / Q) & 1), 1000000ull);
     }
-  } else {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && nstages > 0) {
       constexpr uint32_t idesc = idesc_f16(IN_BF16, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, kH);
@@ -213,11 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  }
-
-  if (warp < kProducerWarps) {
+  } else {
     // ------------------------------------------------------------ epilogue
-    const int sp = warp;  // warps 0..3 own TMEM sub-partitions 0..3
+    const int sp = warp & 3;  // TMEM sub-partition this warp may read
     const int row0 = task.window * kH;
     const bool to_ws = task.slot >= 0;
     float *ws = to_ws ? p.workspace + static_cast<int64_t>(task.slot) * kH * p.N : nullptr;
@@ -257,14 +250,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == kProducerWarps) {
+  if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, C_::kTmemCols);
   }
 }
 
 template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
-cudaError_t launch_variant(const CUtensorMap &tmV, const WcsrParams &p, cudaStream_t stream) {
+cudaError_t launch_variant(const CUtensorMap &tmV, const CUtensorMap &tmB, const WcsrParams &p,
+                           cudaStream_t stream) {
   using C_ = Cfg<NACC, Q>;
   auto kern = wcsr_spmm_kernel<NACC, Q, IN_BF16, OUT_BF16>;
   static bool attr_set = false;
@@ -274,16 +268,18 @@ cudaError_t launch_variant(const CUtensorMap &tmV, const WcsrParams &p, cudaStre
     attr_set = true;
   }
   dim3 grid(p.n_tasks, (p.N + C_::kBN - 1) / C_::kBN);
-  kern<<<grid, kThreads, C_::kSmemBytes, stream>>>(tmV, p);
+  kern<<<grid, kThreads, C_::kSmemBytes, stream>>>(tmV, tmB, p);
   return cudaGetLastError();
 }
 
 template <int NACC, int Q>
-cudaError_t launch_dtypes(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
-                          cudaStream_t s) {
+cudaError_t launch_dtypes(const CUtensorMap &tmV, const CUtensorMap &tmB, const WcsrParams &p, bool in_bf16,
+                          bool out_bf16, cudaStream_t s) {
   if (in_bf16)
-    return out_bf16 ? launch_variant<NACC, Q, true, true>(tmV, p, s) : launch_variant<NACC, Q, true, false>(tmV, p, s);
-  return out_bf16 ? launch_variant<NACC, Q, false, true>(tmV, p, s) : launch_variant<NACC, Q, false, false>(tmV, p, s);
+    return out_bf16 ? launch_variant<NACC, Q, true, true>(tmV, tmB, p, s)
+                    : launch_variant<NACC, Q, true, false>(tmV, tmB, p, s);
+  return out_bf16 ? launch_variant<NACC, Q, false, true>(tmV, tmB, p, s)
+                  : launch_variant<NACC, Q, false, false>(tmV, tmB, p, s);
 }
 
 // One thread per 4 consecutive columns of one row of one split window;
@@ -322,11 +318,11 @@ __global__ void __launch_bounds__(256) wcsr_reduce_kernel(const WcsrSplit *split
 
 }  // namespace
 
-cudaError_t launch_wcsr(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
-                        cudaStream_t stream) {
+cudaError_t launch_wcsr(const CUtensorMap &tmV, const CUtensorMap &tmB, const WcsrParams &p, bool in_bf16,
+                        bool out_bf16, cudaStream_t stream) {
   if (p.n_tasks == 0 || p.N == 0) return cudaSuccess;
-  if (p.N <= 128) return launch_dtypes<1, 6>(tmV, p, in_bf16, out_bf16, stream);
-  return launch_dtypes<2, 4>(tmV, p, in_bf16, out_bf16, stream);
+  if (p.N <= 128) return launch_dtypes<1, 10>(tmV, tmB, p, in_bf16, out_bf16, stream);
+  return launch_dtypes<2, 6>(tmV, tmB, p, in_bf16, out_bf16, stream);
 }
 
 cudaError_t launch_wcsr_reduce(const WcsrSplit *splits, int32_t n_splits, const float *workspace, void *C,
