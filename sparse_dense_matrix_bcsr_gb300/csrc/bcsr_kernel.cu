@@ -14,8 +14,7 @@
 //
 // Work unit ("tile") = one block row x one tile of BN = 128*NACC columns of
 // C.  The kernel is persistent: CTA c takes tiles c, c + G, c + 2G, ... (G =
-// grid size), consecutive tile ids share a column tile so that concurrently
-// running CTAs read the same slice of B from L2.  Two TMEM accumulators
+// grid size); see tile_coords for the order.  Two TMEM accumulators
 // alternate between tiles, so the epilogue of one tile overlaps the loads and
 // MMAs of the next (the paper's non-persistent grid cannot overlap them when
 // one CTA fills an SM).  6 warps:
@@ -35,11 +34,16 @@ namespace {
 constexpr int kBlk = 64;                      // block rows = block cols = K per block
 constexpr int kBlkBytes = kBlk * kBlk * 2;    // one 64x64 16-bit block
 constexpr int kChunkBytes = 64 * 64 * 2;      // 64 rows (k) x 64 columns (n) of B
-constexpr int kThreads = 192;
+constexpr int kLsuWarps = 4;                  // cp.async producer warps
+constexpr int kTmaWarp = kLsuWarps;           // TMA producer warp
+constexpr int kMmaWarp = kLsuWarps + 1;       // TMEM allocator and MMA issuer
 constexpr int kEpiWarps = 4;
+constexpr int kThreads = 32 * (kLsuWarps + 2 + kEpiWarps);
 
-template <int NACC, int Q>
+template <int NACC, int Q, int LSU_CH>
 struct Cfg {
+  static_assert(LSU_CH >= 0 && LSU_CH <= 2 * NACC, "LSU chunks are a subset of the tile's chunks");
+  static constexpr int kTmaChunks = 2 * NACC - LSU_CH;   // B chunks loaded by TMA (the first ones)
   static constexpr int kBN = 128 * NACC;
   static constexpr int kChunks = 2 * NACC;
   static constexpr int kStageBytes = kBlkBytes + kChunks * kChunkBytes;
@@ -47,6 +51,21 @@ struct Cfg {
   static constexpr int kTmemCols = NACC == 1 ? 128 : 256;  // two sets
   static constexpr int kSmemBytes = Q * kStageBytes + 1024 + 1024;  // + barriers + alignment slack
 };
+
+// Tile t -> (block row, column tile).  Consecutive tile ids walk kGroupN
+// column tiles of the same block row, so the CTAs running at one time touch
+// about kGroupN column slices of B at once (they stay in L2) instead of one
+// (whose rows, N elements apart, fall on few L2 slices when N is a large
+// power of two).
+constexpr int kGroupN = 8;
+__device__ __forceinline__ void tile_coords(int64_t t, int n_block_rows, int n_col_tiles, int &br, int &nt) {
+  const int64_t span = static_cast<int64_t>(n_block_rows) * kGroupN;
+  const int64_t g = t / span;
+  const int64_t r = t - g * span;
+  const int gsz = min(kGroupN, n_col_tiles - static_cast<int>(g) * kGroupN);
+  br = static_cast<int>(r / gsz);
+  nt = static_cast<int>(g) * kGroupN + static_cast<int>(r % gsz);
+}
 
 template <bool OUT_BF16>
 __device__ __forceinline__ void store_c(void *C, int64_t off, float v) {
@@ -56,11 +75,11 @@ __device__ __forceinline__ void store_c(void *C, int64_t off, float v) {
     reinterpret_cast<float *>(C)[off] = v;
 }
 
-template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
+template <int NACC, int Q, int LSU_CH, bool IN_BF16, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const BcsrParams p) {
-  using C_ = Cfg<NACC, Q>;
+  using C_ = Cfg<NACC, Q, LSU_CH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Q * C_::kStageBytes);
@@ -70,7 +89,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t n_tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + C_::kBN - 1) / C_::kBN);
+  const int n_col_tiles = (p.N + C_::kBN - 1) / C_::kBN;
+  const int64_t n_tiles = static_cast<int64_t>(p.n_block_rows) * n_col_tiles;
 
   const uint32_t full0 = smem_addr(&bars[0]);
   const uint32_t empty0 = smem_addr(&bars[Q]);
@@ -80,7 +100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < Q; ++q) {
-      mbar_init(full0 + 8 * q, 1);
+      // the TMA arrive (with its transaction bytes) + one arrive per cp.async lane
+      mbar_init(full0 + 8 * q, 1 + (LSU_CH > 0 ? 32 * kLsuWarps : 0));
       mbar_init(empty0 + 8 * q, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -93,7 +114,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), C_::kTmemCols);
     tmem_relinquish();
   }
@@ -102,15 +123,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp < kLsuWarps) {
+    // ------------------------------------------------------------ cp.async producers
+    // The last LSU_CH 64-column chunks of each B tile: 64 rows x LSU_CH*8
+    // 16-byte units, copied with the 128-byte swizzle written by hand.
+    if constexpr (LSU_CH > 0) {
+      constexpr int kUnitsRow = LSU_CH * 8;
+      constexpr int kCopies = 64 * kUnitsRow / (32 * kLsuWarps);
+      constexpr int kRowsPerPass = 32 * kLsuWarps / kUnitsRow;
+      const int pt = threadIdx.x;
+      const int v = pt % kUnitsRow;
+      const int k0 = pt / kUnitsRow;
+      const uint16_t *Bp = reinterpret_cast<const uint16_t *>(p.B);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        int br, nt;
+        tile_coords(t, p.n_block_rows, n_col_tiles, br, nt);
+        const int n = nt * C_::kBN + C_::kTmaChunks * 64 + v * 8;
+        const bool n_live = n < p.N;
+        const uint32_t u = static_cast<uint32_t>(v & 7);
+        const uint32_t dst_col = kBlkBytes + (C_::kTmaChunks + (v >> 3)) * kChunkBytes;
+        const int64_t jb = p.block_row_ptr[br];
+        const int64_t je = p.block_row_ptr[br + 1];
+        for (int64_t jbase = jb; jbase < je && ok; jbase += 32) {
+          const int64_t jl = jbase + lane;
+          const int32_t my_col = jl < je ? p.block_col_idx[jl] : 0;
+          const int cnt = (je - jbase) < 32 ? static_cast<int>(je - jbase) : 32;
+          for (int i = 0; i < cnt; ++i) {
+            const int32_t bcol = __shfl_sync(0xffffffffu, my_col, i);
+            if (lane == 0) ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns) && !*abort_flag;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
+            const int64_t krow0 = static_cast<int64_t>(bcol) * kBlk + k0;
+            const uint16_t *src0 = Bp + krow0 * p.N + n;
+#pragma unroll
+            for (int q = 0; q < kCopies; ++q) {
+              const int k = k0 + q * kRowsPerPass;
+              const bool live = n_live && (krow0 + q * kRowsPerPass) < p.K;
+              const uint32_t dst = st + dst_col + k * 128 + ((u ^ static_cast<uint32_t>(k & 7)) << 4);
+              cp_async_16(dst, live ? static_cast<const void *>(src0 + static_cast<int64_t>(q) * kRowsPerPass * p.N)
+                                    : static_cast<const void *>(Bp),
+                          live ? 16u : 0u);
+            }
+            cp_async_arrive_noinc(full0 + 8 * stage);
+            if (++stage == Q) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      cp_async_wait<0>();
+      if (!ok && lane == 0) {
+        atomicOr(p.status, kDevTimeout);
+        *abort_flag = 1;
+      }
+    }
+  } else if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ TMA producer
     uint32_t stage = 0, phase = 0;
     int64_t issued = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-      const int br = static_cast<int>(t % p.n_block_rows);
-      const int n0 = static_cast<int>(t / p.n_block_rows) * C_::kBN;
-      const int nch = min(C_::kChunks, (p.N - n0 + 63) / 64);
+      int br, nt;
+      tile_coords(t, p.n_block_rows, n_col_tiles, br, nt);
+      const int n0 = nt * C_::kBN;
+      const int nch = min(C_::kTmaChunks, max(0, (p.N - n0 + 63) / 64));
       const int64_t jb = p.block_row_ptr[br];
       const int64_t je = p.block_row_ptr[br + 1];
       for (int64_t jbase = jb; jbase < je && ok; jbase += 32) {
@@ -150,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t i = first; i < issued; ++i)
         mbar_wait(full0 + 8 * (i % Q), static_cast<uint32_t>((i / Q) & 1), 1000000ull);
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(IN_BF16, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, 64);
@@ -158,8 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t tcount = 0;  // non-empty tiles processed
       bool ok = true;
       for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-        const int br = static_cast<int>(t % p.n_block_rows);
-        const int n0 = static_cast<int>(t / p.n_block_rows) * C_::kBN;
+        int br, nt;
+        tile_coords(t, p.n_block_rows, n_col_tiles, br, nt);
+        const int n0 = nt * C_::kBN;
         const int nacc = min(NACC, (p.N - n0 + 127) / 128);
         const int nblk = static_cast<int>(p.block_row_ptr[br + 1] - p.block_row_ptr[br]);
         if (nblk == 0) continue;
@@ -178,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after_sync();
+          if constexpr (LSU_CH > 0) fence_proxy_async_smem();  // cp.async writes -> async-proxy MMA reads
           const uint32_t a_blk = smem_addr(smem + stage * C_::kStageBytes);  // A block: MMA operand B
           const uint32_t b_til = a_blk + kBlkBytes;                          // B tile:  MMA operand A
 #pragma unroll
@@ -218,8 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sp = warp & 3;  // TMEM sub-partition this warp may read
     uint32_t tcount = 0;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-      const int br = static_cast<int>(t % p.n_block_rows);
-      const int n0 = static_cast<int>(t / p.n_block_rows) * C_::kBN;
+      int br, nt;
+      tile_coords(t, p.n_block_rows, n_col_tiles, br, nt);
+      const int n0 = nt * C_::kBN;
       const int nacc = min(NACC, (p.N - n0 + 127) / 128);
       const int nblk = static_cast<int>(p.block_row_ptr[br + 1] - p.block_row_ptr[br]);
       const int row0 = br * kBlk;
@@ -269,17 +352,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, C_::kTmemCols);
   }
 }
 
-template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
+template <int NACC, int Q, int LSU_CH, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_variant(const CUtensorMap &tmA, const CUtensorMap &tmB, const BcsrParams &p,
                            cudaStream_t stream) {
-  using C_ = Cfg<NACC, Q>;
-  auto kern = bcsr_spmm_kernel<NACC, Q, IN_BF16, OUT_BF16>;
+  using C_ = Cfg<NACC, Q, LSU_CH>;
+  auto kern = bcsr_spmm_kernel<NACC, Q, LSU_CH, IN_BF16, OUT_BF16>;
   static bool attr_set = false;  // per instantiation; the attribute is per device function
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::kSmemBytes);
@@ -292,14 +375,14 @@ cudaError_t launch_variant(const CUtensorMap &tmA, const CUtensorMap &tmB, const
   return cudaGetLastError();
 }
 
-template <int NACC, int Q>
+template <int NACC, int Q, int LSU_CH>
 cudaError_t launch_dtypes(const CUtensorMap &tmA, const CUtensorMap &tmB, const BcsrParams &p, bool in_bf16,
                           bool out_bf16, cudaStream_t s) {
   if (in_bf16)
-    return out_bf16 ? launch_variant<NACC, Q, true, true>(tmA, tmB, p, s)
-                    : launch_variant<NACC, Q, true, false>(tmA, tmB, p, s);
-  return out_bf16 ? launch_variant<NACC, Q, false, true>(tmA, tmB, p, s)
-                  : launch_variant<NACC, Q, false, false>(tmA, tmB, p, s);
+    return out_bf16 ? launch_variant<NACC, Q, LSU_CH, true, true>(tmA, tmB, p, s)
+                    : launch_variant<NACC, Q, LSU_CH, true, false>(tmA, tmB, p, s);
+  return out_bf16 ? launch_variant<NACC, Q, LSU_CH, false, true>(tmA, tmB, p, s)
+                  : launch_variant<NACC, Q, LSU_CH, false, false>(tmA, tmB, p, s);
 }
 
 }  // namespace
@@ -309,8 +392,8 @@ cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const Bc
   if (p.n_block_rows == 0 || p.N == 0) return cudaSuccess;
   // Tile width: 128 columns when N is small, else 256 (two accumulators
   // sharing each loaded block).
-  if (p.N <= 128) return launch_dtypes<1, 6>(tmA, tmB, p, in_bf16, out_bf16, stream);
-  return launch_dtypes<2, 4>(tmA, tmB, p, in_bf16, out_bf16, stream);
+  if (p.N <= 128) return launch_dtypes<1, 6, 0>(tmA, tmB, p, in_bf16, out_bf16, stream);
+  return launch_dtypes<2, 4, 0>(tmA, tmB, p, in_bf16, out_bf16, stream);
 }
 
 }  // namespace spmm

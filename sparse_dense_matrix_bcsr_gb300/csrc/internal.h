@@ -11,9 +11,11 @@ namespace spmm {
 struct BcsrParams {
   const int64_t *block_row_ptr;  // device, n_block_rows + 1
   const int32_t *block_col_idx;  // device, n_blocks
+  const void *blocks;            // device, n_blocks x 64 x 64 row-major
+  const void *B;                 // device, K x N row-major
   void *C;                       // device, M x N row-major
   int64_t ldc;                   // row stride of C in elements (= N)
-  int32_t M, N;
+  int32_t M, N, K;
   int32_t n_block_rows;
   int32_t max_ctas;              // persistent grid size (one CTA per SM)
   uint32_t *status;              // device status word
@@ -21,10 +23,10 @@ struct BcsrParams {
 };
 
 // in_bf16: A/B are bf16 (else fp16); out_bf16: C is bf16 (else fp32).
-// tmA covers the blocks array as [n_blocks*64 rows, 64 cols]; tmB covers B as
+// tmA covers the blocks array as [n_blocks*64 rows, 64 cols], tmB covers B as
 // [K rows, N cols]; both with 64 x 64 boxes and 128-byte swizzle.
-cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const BcsrParams &p,
-                        bool in_bf16, bool out_bf16, cudaStream_t stream);
+cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const BcsrParams &p, bool in_bf16,
+                        bool out_bf16, cudaStream_t stream);
 
 // WCSR task: packed columns [p_begin, p_end) of one window.
 struct WcsrTask {

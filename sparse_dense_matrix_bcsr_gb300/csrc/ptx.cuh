@@ -41,29 +41,35 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One probe of the phase; the thread may be suspended for up to about
+// 20 us (the hint) while the phase is incomplete, and resumes as soon as it
+// completes, so waiting warps do not take issue slots from working ones.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(20000)
       : "memory");
   return done != 0;
 }
 
 // Wait until the phase with the given parity has completed, for at most
-// limit_ns nanoseconds (global timer).  Returns false when the limit ran out;
-// no wait in this library is unbounded.
+// limit_ns nanoseconds.  Returns false when the limit ran out; no wait in
+// this library is unbounded.  The bound is counted with the SM's own cycle
+// counter (cheap to read) at 2.1 GHz, so at lower clocks the wait lasts
+// proportionally longer but still ends.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long limit_cycles = static_cast<long long>(limit_ns) * 21 / 10;
+  const long long t0 = clock64();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 4; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > limit_ns) return false;
+    if (clock64() - t0 > limit_cycles) return false;
   }
 }
 
@@ -122,6 +128,12 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
+}
+
+// Arrive on `bar` (without incrementing its pending count) once every
+// cp.async this thread issued before has completed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }

@@ -255,10 +255,13 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
     spmm::BcsrParams p;
     p.block_row_ptr = h->d_ptr;
     p.block_col_idx = h->d_idx;
+    p.blocks = h->d_vals;
+    p.B = B;
     p.C = C;
     p.ldc = N;
     p.M = static_cast<int32_t>(h->m);
     p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(h->k);
     p.n_block_rows = static_cast<int32_t>(h->n_groups);
     p.max_ctas = std::max(h->num_sms, 1);
     p.status = h->d_status;

@@ -114,6 +114,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (s < nstages && pb < task.p_end) return *reinterpret_cast<const int4 *>(p.window_col_idx + pb);
       return make_int4(-2, -2, -2, -2);
     };
+    // Index prefetch ring: slot u holds the indices of stage s with s % kPF == u.
+    // The loop is unrolled by kPF so every slot stays in a fixed register and a
+    // load is only waited for when its stage is issued, kPF stages later.
     int4 ring[kPF];
 #pragma unroll
     for (int i = 0; i < kPF; ++i) ring[i] = load_idx(i);
@@ -121,41 +124,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t stage = 0, phase = 0;
     int64_t issued = 0;
     bool ok = true;
-    for (int s = 0; s < nstages; ++s) {
-      const int4 cur = ring[0];
+    for (int s0 = 0; s0 < nstages && ok; s0 += kPF) {
 #pragma unroll
-      for (int i = 0; i + 1 < kPF; ++i) ring[i] = ring[i + 1];
-      ring[kPF - 1] = load_idx(s + kPF);
+      for (int u = 0; u < kPF; ++u) {
+        const int s = s0 + u;
+        if (s >= nstages || !ok) break;
+        const int4 cur = ring[u];
+        ring[u] = load_idx(s + kPF);
 
-      if (lane == 0) ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns) && !*abort_flag;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      const int64_t pbase = task.p_begin + static_cast<int64_t>(s) * kKC;
-      const int64_t left = task.p_end - pbase;
-      const int groups = left >= kKC ? kKC / 4 : static_cast<int>(left / 4);
-      const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
-      const uint32_t fb = full0 + 8 * stage;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(fb, kValBytes + groups * 4 * 128 * nch);
-        tma_load_2d(st, &tmV, fb, static_cast<int32_t>(pbase), 0);
-      }
-      __syncwarp();
-      if (g < groups) {
-        const int32_t r0 = cur.x < 0 ? oob_row : cur.x;
-        const int32_t r1 = cur.y < 0 ? oob_row : cur.y;
-        const int32_t r2 = cur.z < 0 ? oob_row : cur.z;
-        const int32_t r3 = cur.w < 0 ? oob_row : cur.w;
-#pragma unroll
-        for (int j = 0; j < kChunksPerLane; ++j) {
-          const int c = c_first + j;
-          if (c < nch)
-            tma_gather4(st + kValBytes + c * kChunkBytes + g * 512, &tmB, fb, n0 + c * 64, r0, r1, r2, r3);
+        if (lane == 0) ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns) && !*abort_flag;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const int64_t pbase = task.p_begin + static_cast<int64_t>(s) * kKC;
+        const int64_t left = task.p_end - pbase;
+        const int groups = left >= kKC ? kKC / 4 : static_cast<int>(left / 4);
+        const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
+        const uint32_t fb = full0 + 8 * stage;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, kValBytes + groups * 4 * 128 * nch);
+          tma_load_2d(st, &tmV, fb, static_cast<int32_t>(pbase), 0);
         }
-      }
-      ++issued;
-      if (++stage == Q) {
-        stage = 0;
-        phase ^= 1u;
+        __syncwarp();
+        if (g < groups) {
+          const int32_t r0 = cur.x < 0 ? oob_row : cur.x;
+          const int32_t r1 = cur.y < 0 ? oob_row : cur.y;
+          const int32_t r2 = cur.z < 0 ? oob_row : cur.z;
+          const int32_t r3 = cur.w < 0 ? oob_row : cur.w;
+#pragma unroll
+          for (int j = 0; j < kChunksPerLane; ++j) {
+            const int c = c_first + j;
+            if (c < nch)
+              tma_gather4(st + kValBytes + c * kChunkBytes + g * 512, &tmB, fb, n0 + c * 64, r0, r1, r2, r3);
+          }
+        }
+        ++issued;
+        if (++stage == Q) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
     }
     if (!ok && lane == 0) {
