@@ -159,7 +159,7 @@ def run_ours(args, rank, world):
                          device=f"cuda:{dev}")
         eff, stored_fl, bytes_min = part_model(w, info)
         parts.append(dict(name=name, w=w, h=h, info=info, B=B, dB=dB, dC=dC, eff=eff, stored_flops=stored_fl,
-                          bytes_min=bytes_min, launches=1 + (1 if info.get("n_split_windows", 0) else 0),
+                          bytes_min=bytes_min, launches=2 if w.fmt == "wcsr" else 1,
                           kernel="bcsr_kernel.cu" if w.fmt == "bcsr" else "wcsr_kernel.cu"))
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=f"cuda:{dev}")
 

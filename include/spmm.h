@@ -65,9 +65,9 @@ typedef struct {
     int64_t padding;         /* stored - nnz: explicit zeros kept by the format */
     int64_t idx_bytes;       /* bytes of the index arrays on the device (ptr + idx) */
     int64_t val_bytes;       /* bytes of the value array on the device */
-    int64_t n_tasks;         /* WCSR: work items after window splitting; BCSR: n_groups */
-    int64_t n_split_windows; /* WCSR: windows split across several tasks; BCSR: 0 */
-    int64_t split_cols;      /* WCSR: maximum packed columns per task; BCSR: 0 */
+    int64_t n_tasks;         /* WCSR: stages (<= 64 packed columns of one window); BCSR: n_groups */
+    int64_t n_split_windows; /* WCSR: windows cut between CTAs at N <= 256; BCSR: 0 */
+    int64_t split_cols;      /* WCSR: packed columns per stage (64); BCSR: 0 */
 } spmm_info;
 
 /*
@@ -101,8 +101,8 @@ spmm_status spmm_bcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64
  * the window w owning position p, 0 where absent or padded.
  * Arguments as for spmm_bcsr_create; window_h and col_pad in 1..256.
  * spmm_run needs window_h == 16 and col_pad a multiple of 16.
- * Large windows are split into tasks of at most split_cols packed columns
- * (chosen from the device's SM count; see spmm_set_split_cols).
+ * Windows are cut into stages of at most 64 packed columns; each persistent
+ * CTA takes an equal number of stages (see spmm_set_max_ctas).
  */
 spmm_status spmm_wcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64_t *row_ptr,
                              const int32_t *col_idx, const void *vals, spmm_dtype in_t,
@@ -116,9 +116,9 @@ spmm_status spmm_wcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64
  *   C  device pointer, m x N row-major, out_t, 16-byte aligned; fully
  *      overwritten (rows of A without entries give 0).
  *   N  number of columns of B and C, N > 0 and N % 8 == 0 (TMA row stride).
- * A WCSR handle whose windows are split uses an fp32 workspace that grows
- * (cudaMalloc, outside any launch) on the first run with a larger N; results
- * are bitwise reproducible run to run (fixed reduction order).
+ * A WCSR handle adds the partial sums of windows cut between CTAs in a
+ * second kernel, in a fixed order, using a workspace allocated at create;
+ * results are bitwise reproducible run to run.
  * Errors: INVALID_ARG (null handle/pointers, N <= 0); UNSUPPORTED (N % 8,
  * alignment, format parameters the kernels do not take, device not sm_103);
  * OOM (workspace); CUDA (launch).  Asynchronous: see spmm_check.
@@ -185,12 +185,14 @@ spmm_status spmm_wcsr_convert(int64_t m, int64_t k, const int64_t *row_ptr, cons
 spmm_status spmm_check(spmm_handle h, void *stream);
 
 /*
- * spmm_set_split_cols -- WCSR only: rebuild the task list so that no task
- * holds more than `cols` packed columns (rounded up to a multiple of 64;
- * cols <= 0 restores the automatic choice).  Windows longer than that are
- * split; their partial sums are added in a fixed order by a second kernel.
+ * spmm_set_max_ctas -- cap the number of persistent CTAs a run launches
+ * (ctas = 0: one per SM, the default).  Both kernels give each CTA an equal
+ * share of the work (BCSR: whole block-row x column tiles; WCSR: equal
+ * numbers of 64-column stages), so the cap changes where WCSR windows are cut
+ * between CTAs (their partial sums are added by a second kernel in a fixed
+ * order) but not the result beyond fp32 rounding.
  */
-spmm_status spmm_set_split_cols(spmm_handle h, int64_t cols);
+spmm_status spmm_set_max_ctas(spmm_handle h, int32_t ctas);
 
 /*
  * spmm_selftest_wait_timeout -- failure-detection self test.  Launches one

@@ -9,7 +9,7 @@ kernels of ``libspmm_gb300.so``.  The functions keep the C names:
     spmm_destroy(h)
 
 plus ``spmm_format_info``, ``spmm_export_format``, ``spmm_check``,
-``spmm_set_split_cols``, ``spmm_run_host``, the host-only converters
+``spmm_set_max_ctas``, ``spmm_run_host``, the host-only converters
 ``spmm_bcsr_convert`` / ``spmm_wcsr_convert`` and
 ``spmm_selftest_wait_timeout``.  ``run_torch`` is a convenience that passes
 torch tensors and the current stream.
@@ -47,7 +47,7 @@ SPMM_FORMAT_WCSR = 1
 EXPORTS = (
     "spmm_bcsr_create", "spmm_wcsr_create", "spmm_run", "spmm_run_host", "spmm_destroy",
     "spmm_format_info", "spmm_export_format", "spmm_bcsr_convert", "spmm_wcsr_convert",
-    "spmm_check", "spmm_set_split_cols", "spmm_selftest_wait_timeout", "spmm_status_str",
+    "spmm_check", "spmm_set_max_ctas", "spmm_selftest_wait_timeout", "spmm_status_str",
     "spmm_last_error",
 )
 
@@ -94,7 +94,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "spmm_bcsr_convert": [I64, I64, P, P, P, I32, I32, ctypes.POINTER(I64), P, P, P],
         "spmm_wcsr_convert": [I64, I64, P, P, P, I32, I32, ctypes.POINTER(I64), P, P, P],
         "spmm_check": [P, P],
-        "spmm_set_split_cols": [P, I64],
+        "spmm_set_max_ctas": [P, ctypes.c_int32],
         "spmm_selftest_wait_timeout": [I64, P, ctypes.POINTER(ctypes.c_int32)],
     }
     for name, args in sig.items():
@@ -207,8 +207,8 @@ def spmm_check(h: int, stream: int = 0) -> int:
     return load_library().spmm_check(h, stream or None)
 
 
-def spmm_set_split_cols(h: int, cols: int) -> None:
-    _check(load_library().spmm_set_split_cols(h, cols), "spmm_set_split_cols")
+def spmm_set_max_ctas(h: int, ctas: int) -> None:
+    _check(load_library().spmm_set_max_ctas(h, ctas), "spmm_set_max_ctas")
 
 
 def spmm_selftest_wait_timeout(timeout_ns: int, stream: int = 0) -> int:

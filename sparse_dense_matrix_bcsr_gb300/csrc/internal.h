@@ -28,45 +28,51 @@ struct BcsrParams {
 cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const BcsrParams &p, bool in_bf16,
                         bool out_bf16, cudaStream_t stream);
 
-// WCSR task: packed columns [p_begin, p_end) of one window.
-struct WcsrTask {
+// WCSR work is a list of stages: at most 64 packed columns of one window.
+// Every window has at least one stage (ncols = 0 for a window without
+// columns), and stages are listed in window order.
+struct WcsrStage {
+  int32_t p_begin;   // first packed column
   int32_t window;
-  int32_t slot;      // -1: the task covers the whole window and writes C; else partial index
-  int64_t p_begin;
-  int64_t p_end;
+  int32_t ncols;     // 0..64, a multiple of 16
+  int32_t flags;     // kStageFirst | kStageLast
 };
+constexpr int32_t kStageFirst = 1;
+constexpr int32_t kStageLast = 2;
 
-// A window split across several tasks: its partials are slots
-// [slot_begin, slot_begin + n_slots), summed in that order.
-struct WcsrSplit {
-  int32_t window;
-  int32_t slot_begin;
-  int32_t n_slots;
+// A partial sum written to the workspace: the window / column tile it
+// belongs to and whether it holds the window's first and/or last stage.
+struct WcsrPartial {
+  int32_t window;    // -1: slot unused in this run
+  int32_t col_tile;
+  int32_t flags;     // kStageFirst | kStageLast
   int32_t pad_;
 };
 
 struct WcsrParams {
-  const WcsrTask *tasks;         // device, n_tasks
-  const int32_t *window_col_idx; // device, P_total
+  const WcsrStage *stages;       // device, n_stages
+  const int32_t *stage_idx;      // device, n_stages x 64: stage s's column indices, -2 past its ncols
+  const void *values;            // device, 16 x P_total row-major
   const void *B;                 // device, K x N row-major
   void *C;                       // device, M x N row-major
-  float *workspace;              // device, n_slots x 16 x N fp32 (split windows only)
+  float *workspace;              // device, 2 * grid x 16 x 256 fp32
+  WcsrPartial *partials;         // device, 2 * grid
+  int64_t n_stages;
   int64_t P_total;
   int32_t M, N, K;
-  int32_t n_tasks;
+  int32_t grid;                  // persistent CTAs; CTA c owns a contiguous range of (column tile, stage)
   uint32_t *status;
   uint64_t wait_limit_ns;
 };
 
-// tmV covers the values array as [16 rows, P_total cols] with 64 x 16 boxes;
-// tmB covers B as [K rows, N cols] with 64 x 1 boxes (row gathers); both with
-// 128-byte swizzle.
-cudaError_t launch_wcsr(const CUtensorMap &tmV, const CUtensorMap &tmB, const WcsrParams &p, bool in_bf16,
-                        bool out_bf16, cudaStream_t stream);
+// Workspace floats per partial slot (16 rows x 256 columns).
+constexpr int64_t kWcsrSlotFloats = 16 * 256;
 
-// Sum the partials of split windows into C in slot order.
-cudaError_t launch_wcsr_reduce(const WcsrSplit *splits, int32_t n_splits, const float *workspace,
-                               void *C, int32_t M, int32_t N, bool out_bf16, cudaStream_t stream);
+// tmV covers the values array as [16 rows, P_total cols] with 64 x 16 boxes
+// and 128-byte swizzle.  Runs the SpMM kernel, then the kernel that adds the
+// partials of windows cut between CTAs.
+cudaError_t launch_wcsr(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
+                        cudaStream_t stream);
 
 // Failure-detection self test: wait on an mbarrier nothing arrives at.
 cudaError_t launch_wait_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t stream);

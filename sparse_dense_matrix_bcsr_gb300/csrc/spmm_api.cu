@@ -102,16 +102,16 @@ struct spmm_handle_s {
   int64_t n_cached = -1;
   CUtensorMap tm_B;
 
-  // WCSR work decomposition
-  int64_t split_cols = 0;
-  bool split_auto = true;
-  std::vector<spmm::WcsrTask> tasks;
-  std::vector<spmm::WcsrSplit> splits;
-  int64_t n_slots = 0;
-  spmm::WcsrTask *d_tasks = nullptr;
-  spmm::WcsrSplit *d_splits = nullptr;
+  // WCSR work decomposition: stages of <= 64 packed columns, and the
+  // partial-sum workspace of windows cut between persistent CTAs
+  int32_t max_ctas = 0;  // 0: one CTA per SM
+  int64_t n_stages = 0;
+  spmm::WcsrStage *d_stages = nullptr;
+  int32_t *d_stage_idx = nullptr;
   float *d_ws = nullptr;
-  size_t ws_bytes = 0;
+  spmm::WcsrPartial *d_partials = nullptr;
+  int64_t ws_slots = 0;
+  std::vector<int32_t> stage_first;  // host copy of the stage list's first-stage flags (for statistics)
 
   uint32_t *d_status = nullptr;
   uint64_t wait_limit_ns = kDefaultWaitLimitNs;
@@ -147,8 +147,9 @@ void free_handle(spmm_handle h) {
   cudaFree(h->d_ptr);
   cudaFree(h->d_idx);
   cudaFree(h->d_vals);
-  cudaFree(h->d_tasks);
-  cudaFree(h->d_splits);
+  cudaFree(h->d_stages);
+  cudaFree(h->d_stage_idx);
+  cudaFree(h->d_partials);
   cudaFree(h->d_ws);
   cudaFree(h->d_status);
   cudaFree(h->d_bstage);
@@ -179,52 +180,51 @@ spmm_status upload_common(spmm_handle h, const HostFormat &f) {
   return SPMM_OK;
 }
 
-// Split windows longer than split_cols packed columns into tasks; order the
-// tasks longest first so the block scheduler starts the long ones early.
-spmm_status build_tasks(spmm_handle h, const std::vector<int64_t> &wptr) {
-  int64_t T = h->split_cols;
-  if (h->split_auto) {
-    const int64_t sms = std::max(h->num_sms, 1);
-    const int64_t target = (h->n_units + sms * 4 - 1) / (sms * 4);
-    T = std::max<int64_t>(512, (target + 63) / 64 * 64);
-  }
-  h->split_cols = T;
-  std::vector<spmm::WcsrTask> tasks;
-  std::vector<spmm::WcsrSplit> splits;
-  int32_t slot = 0;
+// The WCSR stage list: each window cut into stages of at most 64 packed
+// columns, in window order; a window without columns gets one empty stage.
+spmm_status build_stages(spmm_handle h, const std::vector<int64_t> &wptr, const std::vector<int32_t> &widx) {
+  std::vector<spmm::WcsrStage> st;
   const int64_t nw = h->n_groups;
   for (int64_t w = 0; w < nw; ++w) {
     const int64_t b = wptr[w], e = wptr[w + 1];
-    if (e - b <= T) {
-      tasks.push_back({static_cast<int32_t>(w), -1, b, e});
-    } else {
-      const int32_t ns = static_cast<int32_t>((e - b + T - 1) / T);
-      splits.push_back({static_cast<int32_t>(w), slot, ns, 0});
-      for (int32_t s = 0; s < ns; ++s)
-        tasks.push_back({static_cast<int32_t>(w), slot + s, b + s * T, std::min(e, b + (s + 1) * T)});
-      slot += ns;
+    if (e == b) {
+      st.push_back({static_cast<int32_t>(b), static_cast<int32_t>(w), 0, spmm::kStageFirst | spmm::kStageLast});
+      continue;
+    }
+    for (int64_t p = b; p < e; p += 64) {
+      int32_t flags = (p == b ? spmm::kStageFirst : 0) | (p + 64 >= e ? spmm::kStageLast : 0);
+      st.push_back({static_cast<int32_t>(p), static_cast<int32_t>(w), static_cast<int32_t>(std::min<int64_t>(64, e - p)),
+                    flags});
     }
   }
-  std::stable_sort(tasks.begin(), tasks.end(), [](const spmm::WcsrTask &x, const spmm::WcsrTask &y) {
-    return (x.p_end - x.p_begin) > (y.p_end - y.p_begin);
-  });
-  if (tasks.size() >= (1u << 31)) return fail(SPMM_ERR_UNSUPPORTED, "too many tasks");
-  cudaFree(h->d_tasks);
-  cudaFree(h->d_splits);
-  h->d_tasks = nullptr;
-  h->d_splits = nullptr;
-  CUDA_TRY(cudaMalloc(&h->d_tasks, std::max<size_t>(tasks.size(), 1) * sizeof(spmm::WcsrTask)), "cudaMalloc(tasks)");
-  if (!tasks.empty())
-    CUDA_TRY(cudaMemcpy(h->d_tasks, tasks.data(), tasks.size() * sizeof(spmm::WcsrTask), cudaMemcpyHostToDevice),
-             "upload tasks");
-  CUDA_TRY(cudaMalloc(&h->d_splits, std::max<size_t>(splits.size(), 1) * sizeof(spmm::WcsrSplit)), "cudaMalloc(splits)");
-  if (!splits.empty())
-    CUDA_TRY(cudaMemcpy(h->d_splits, splits.data(), splits.size() * sizeof(spmm::WcsrSplit), cudaMemcpyHostToDevice),
-             "upload splits");
-  h->tasks.swap(tasks);
-  h->splits.swap(splits);
-  h->n_slots = slot;
+  h->n_stages = static_cast<int64_t>(st.size());
+  // Column indices of each stage at a fixed place (64 per stage).
+  std::vector<int32_t> sidx(st.size() * 64, -2);
+  for (size_t i = 0; i < st.size(); ++i)
+    for (int r = 0; r < st[i].ncols; ++r) sidx[i * 64 + r] = widx[st[i].p_begin + r];
+  CUDA_TRY(cudaMalloc(&h->d_stage_idx, std::max<size_t>(sidx.size(), 64) * sizeof(int32_t)), "cudaMalloc(stage_idx)");
+  if (!sidx.empty())
+    CUDA_TRY(cudaMemcpy(h->d_stage_idx, sidx.data(), sidx.size() * sizeof(int32_t), cudaMemcpyHostToDevice),
+             "upload stage_idx");
+  h->stage_first.resize(st.size());
+  for (size_t i = 0; i < st.size(); ++i) h->stage_first[i] = st[i].flags & spmm::kStageFirst;
+  CUDA_TRY(cudaMalloc(&h->d_stages, std::max<size_t>(st.size(), 1) * sizeof(spmm::WcsrStage)), "cudaMalloc(stages)");
+  if (!st.empty())
+    CUDA_TRY(cudaMemcpy(h->d_stages, st.data(), st.size() * sizeof(spmm::WcsrStage), cudaMemcpyHostToDevice),
+             "upload stages");
+  // Two partial slots per CTA, sized for the largest grid.
+  h->ws_slots = 2 * static_cast<int64_t>(std::max(h->num_sms, 1));
+  CUDA_TRY(cudaMalloc(&h->d_ws, h->ws_slots * spmm::kWcsrSlotFloats * sizeof(float)), "cudaMalloc(workspace)");
+  CUDA_TRY(cudaMalloc(&h->d_partials, h->ws_slots * sizeof(spmm::WcsrPartial)), "cudaMalloc(partials)");
   return SPMM_OK;
+}
+
+// Persistent grid of the WCSR kernel for N columns.
+int32_t wcsr_grid(spmm_handle h, int64_t N) {
+  const int64_t bn = N <= 128 ? 128 : 256;
+  const int64_t items = h->n_stages * ((N + bn - 1) / bn);
+  int64_t g = h->max_ctas > 0 ? std::min<int64_t>(h->max_ctas, h->num_sms) : h->num_sms;
+  return static_cast<int32_t>(std::max<int64_t>(0, std::min(g, items)));
 }
 
 spmm_status check_run_args(spmm_handle h, const void *B, void *C, int64_t N) {
@@ -263,7 +263,7 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(h->k);
     p.n_block_rows = static_cast<int32_t>(h->n_groups);
-    p.max_ctas = std::max(h->num_sms, 1);
+    p.max_ctas = std::max(h->max_ctas > 0 ? std::min(h->max_ctas, h->num_sms) : h->num_sms, 1);
     p.status = h->d_status;
     p.wait_limit_ns = h->wait_limit_ns;
     cudaError_t e = spmm::launch_bcsr(h->tm_vals, h->tm_B, p, in_bf16, out_bf16, s);
@@ -273,38 +273,24 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
   // WCSR
   if (h->b_row != 16 || h->b_col % 16 != 0)
     return fail(SPMM_ERR_UNSUPPORTED, "the WCSR kernel takes window height 16 and column padding a multiple of 16");
-  const size_t need = static_cast<size_t>(h->n_slots) * 16 * static_cast<size_t>(N) * sizeof(float);
-  if (need > h->ws_bytes) {
-    cudaFree(h->d_ws);
-    h->d_ws = nullptr;
-    h->ws_bytes = 0;
-    CUDA_TRY(cudaMalloc(&h->d_ws, need), "cudaMalloc(split workspace)");
-    h->ws_bytes = need;
-  }
-  if (h->b_cached != B || h->n_cached != N) {
-    spmm_status st = encode_2d(&h->tm_B, B, in_bf16, static_cast<uint64_t>(std::max<int64_t>(h->k, 1)),
-                               static_cast<uint64_t>(N), static_cast<uint64_t>(N), 1, 64);
-    if (st != SPMM_OK) return st;
-    h->b_cached = B;
-    h->n_cached = N;
-  }
   spmm::WcsrParams p;
-  p.tasks = h->d_tasks;
-  p.window_col_idx = h->d_idx;
+  p.stages = h->d_stages;
+  p.stage_idx = h->d_stage_idx;
+  p.values = h->d_vals;
+  p.P_total = h->n_units;
   p.B = B;
   p.C = C;
   p.workspace = h->d_ws;
-  p.P_total = h->n_units;
+  p.partials = h->d_partials;
+  p.n_stages = h->n_stages;
   p.M = static_cast<int32_t>(h->m);
   p.N = static_cast<int32_t>(N);
   p.K = static_cast<int32_t>(h->k);
-  p.n_tasks = static_cast<int32_t>(h->tasks.size());
+  p.grid = wcsr_grid(h, N);
   p.status = h->d_status;
   p.wait_limit_ns = h->wait_limit_ns;
-  cudaError_t e = spmm::launch_wcsr(h->tm_vals, h->tm_B, p, in_bf16, out_bf16, s);
+  cudaError_t e = spmm::launch_wcsr(h->tm_vals, p, in_bf16, out_bf16, s);
   if (e != cudaSuccess) return cuda_fail(e, "WCSR kernel launch");
-  e = spmm::launch_wcsr_reduce(h->d_splits, static_cast<int32_t>(h->splits.size()), h->d_ws, C, p.M, p.N, out_bf16, s);
-  if (e != cudaSuccess) return cuda_fail(e, "WCSR reduce launch");
   return SPMM_OK;
 }
 
@@ -418,7 +404,7 @@ spmm_status spmm_wcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64
     st = encode_2d(&h->tm_vals, h->d_vals, in_t == SPMM_BF16, 16,
                    static_cast<uint64_t>(f.n_units > 0 ? f.n_units : 64),
                    static_cast<uint64_t>(f.n_units > 0 ? f.n_units : 64), 16, 64);
-  if (st == SPMM_OK) st = build_tasks(h, f.ptr);
+  if (st == SPMM_OK) st = build_stages(h, f.ptr, f.idx);
   if (st != SPMM_OK) {
     free_handle(h);
     return st;
@@ -427,20 +413,11 @@ spmm_status spmm_wcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64
   return SPMM_OK;
 }
 
-spmm_status spmm_set_split_cols(spmm_handle h, int64_t cols) {
+spmm_status spmm_set_max_ctas(spmm_handle h, int32_t ctas) {
   if (!h) return fail(SPMM_ERR_INVALID_ARG, "handle is NULL");
-  if (h->format != SPMM_FORMAT_WCSR) return fail(SPMM_ERR_INVALID_ARG, "split columns apply to WCSR handles only");
-  CUDA_TRY(cudaSetDevice(h->device), "cudaSetDevice");
-  std::vector<int64_t> wptr(static_cast<size_t>(h->n_groups + 1));
-  CUDA_TRY(cudaMemcpy(wptr.data(), h->d_ptr, wptr.size() * sizeof(int64_t), cudaMemcpyDeviceToHost), "download ptr");
-  CUDA_TRY(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
-  if (cols <= 0) {
-    h->split_auto = true;
-  } else {
-    h->split_auto = false;
-    h->split_cols = (cols + 63) / 64 * 64;
-  }
-  return build_tasks(h, wptr);
+  if (ctas < 0) return fail(SPMM_ERR_INVALID_ARG, "ctas must be >= 0");
+  h->max_ctas = ctas;
+  return SPMM_OK;
 }
 
 spmm_status spmm_run(spmm_handle h, const void *B, void *C, int64_t N, void *stream) {
@@ -520,9 +497,16 @@ spmm_status spmm_format_info(spmm_handle h, spmm_info *info) {
   info->idx_bytes = (h->n_groups + 1) * 8 + h->n_units * 4;
   info->val_bytes = h->stored * 2;
   if (h->format == SPMM_FORMAT_WCSR) {
-    info->n_tasks = static_cast<int64_t>(h->tasks.size());
-    info->n_split_windows = static_cast<int64_t>(h->splits.size());
-    info->split_cols = h->split_cols;
+    info->n_tasks = h->n_stages;
+    info->split_cols = 64;
+    // windows cut by a CTA boundary when the product has one column tile
+    const int64_t g = wcsr_grid(h, 8);
+    int64_t cut = 0;
+    for (int64_t c = 1; c < g; ++c) {
+      const int64_t f = h->n_stages * c / g;
+      if (!h->stage_first[f]) ++cut;
+    }
+    info->n_split_windows = cut;
   } else {
     info->n_tasks = h->n_groups;
   }

@@ -1,26 +1,47 @@
 // wcsr_kernel.cu -- WCSR SpMM for sm_103a.
 //
-// Method: "AsyncSparse", Section III-B (the packed value tile of a window is
-// contiguous and loaded by TMA; the matching rows of B are fetched through
-// window_col_idx) and Section III-C (task-based decomposition: long windows
-// are split into fixed-size sub-tasks and the CTA index names a task).  On
-// Hopper the paper gathers B with all threads of a warpgroup because TMA
-// cannot gather; sm_103a's TMA can (tile::gather4, four rows per
-// instruction), so here one producer warp issues every load, as in the BCSR
-// kernel, and the MMA runs decoupled behind an mbarrier ring.  The paper adds
-// split partial sums with atomicAdd; here a split task writes an fp32 partial
-// and a second kernel adds a window's partials in slot order, so results are
-// bitwise reproducible.
+// Method: "AsyncSparse", Section III-B (a window's packed value tile is
+// contiguous; the rows of B it multiplies are fetched
+// through window_col_idx by all threads, written to shared memory with the
+// 128-byte swizzle applied by hand) and Section III-C (task decomposition so
+// that long windows do not serialise on one CTA).
+//
+// Work list: every window is cut into stages of at most 64 packed columns,
+// listed in window order (a window without columns has one empty stage).  The
+// kernel is persistent: CTA c owns the contiguous range
+// [T*c/G, T*(c+1)/G) of the T = stages x column-tiles work items, so every
+// CTA gets the same number of stages whatever the window lengths, and the
+// column indices a CTA reads are contiguous.  A window whose stages are cut
+// by a range boundary is finished by a second kernel: each CTA writes the
+// fp32 partial sums of its first and last window to two workspace slots, and
+// the CTA that holds the window's first stage adds the slots of the following
+// CTAs in CTA order (the paper adds split partials with atomicAdd; the fixed
+// order here makes results bitwise reproducible).
 //
 // The product is computed transposed: the 128 columns of an accumulator are
-// the MMA's M (TMEM lanes) and the 16 rows of a window are the MMA's N, so a
-// 16-row window is a legal tcgen05 shape.
+// the MMA's M (TMEM lanes) and the 16 rows of a window are the MMA's N.
 //
-// CTA = one task x one tile of BN = 128*NACC columns; 6 warps:
-//   warp 0      producer: value tile (2-D TMA) and B rows (TMA gather4); the
-//               warp prefetches the column indices PF stages ahead
-//   warp 1      TMEM allocator and MMA issuer
-//   warps 2..5  epilogue (warp w reads TMEM sub-partition w % 4)
+// Only the producer warps read global memory.  Their loads of stage
+// descriptors and column indices queue behind the SM's outstanding gathers,
+// so they are independent of each other (the column indices of stage s sit
+// at a fixed place, stage_idx[64*s ...]) and issued two work items ahead.
+// The MMA thread learns a stage's shape from a record the producer writes to
+// shared memory, and the epilogue learns a window's identity from a record
+// the MMA thread writes, so neither waits on a global load.
+//
+// 9 warps:
+//   warps 0..3  producers; warp w loads the work items w, w+4, ... of the
+//               CTA's range: the 16 x 64 value tile and the 64 B rows with
+//               16-byte cp.async (one B row, 512 B, per warp instruction at
+//               BN = 256; a strided TMA box of the value tile stalled the
+//               issuing warp behind slow HBM rows); every lane ends the item with
+//               cp.async.mbarrier.arrive.noinc, so producers never block on
+//               their own copies and one warp's barrier handling overlaps
+//               another's copies
+//   warp 4      TMEM allocator and MMA issuer; fences the generic proxy
+//               against the async proxy before reading a stage
+//   warps 5..8  epilogue (warp w reads TMEM sub-partition w % 4), four
+//               accumulator buffers in TMEM rotate between windows
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -34,16 +55,21 @@ constexpr int kH = 16;                       // window height
 constexpr int kKC = 64;                      // packed columns per stage
 constexpr int kValBytes = kH * kKC * 2;      // 2 KB value tile per stage
 constexpr int kChunkBytes = kKC * 64 * 2;    // 64 gathered rows x 64 columns
-constexpr int kThreads = 192;
-constexpr int kPF = 4;                       // index prefetch distance (stages)
+constexpr int kProducerWarps = 4;
+constexpr int kMmaWarp = kProducerWarps;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = 32 * (kProducerWarps + 1 + kEpiWarps);
+constexpr int kAccBufs = 4;
 
 template <int NACC, int Q>
 struct Cfg {
   static constexpr int kBN = 128 * NACC;
   static constexpr int kChunks = 2 * NACC;
   static constexpr int kStageBytes = kValBytes + kChunks * kChunkBytes;
-  static constexpr int kTmemCols = 32;  // NACC * 16 <= 32
-  static constexpr int kSmemBytes = Q * kStageBytes + 1024 + 1024;
+  static constexpr int kAccCols = kH * NACC;                     // TMEM columns per accumulator buffer
+  static constexpr int kTmemCols = kAccBufs * kAccCols <= 32 ? 32 : (kAccBufs * kAccCols <= 64 ? 64 : 128);
+  static constexpr int kSmemBytes = Q * kStageBytes + 2048 + 1024;
+  static_assert(kAccBufs * kAccCols <= kTmemCols, "accumulator buffers exceed the TMEM allocation");
 };
 
 template <bool OUT_BF16>
@@ -54,45 +80,77 @@ __device__ __forceinline__ void store_out(void *C, int64_t off, float v) {
     reinterpret_cast<float *>(C)[off] = v;
 }
 
+__device__ __forceinline__ int4 shfl_int4(const int4 &v, int src) {
+  return make_int4(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src),
+                   __shfl_sync(0xffffffffu, v.z, src), __shfl_sync(0xffffffffu, v.w, src));
+}
+
+// Descriptor of work item f (stage f % n_stages of column tile f / n_stages),
+// or an empty item past the CTA's range.
+__device__ __forceinline__ int4 load_item(const int4 *stg, int64_t f, int64_t f1, int64_t n_stages) {
+  return f < f1 ? stg[f % n_stages] : make_int4(0, -1, 0, 0);
+}
+
+// Shared-memory records passed between roles.
+struct StageRec {   // producer -> MMA, one per ring stage
+  int32_t ncols;
+  int32_t flags;
+  int32_t window;
+  int32_t tile;
+};
+struct SegRec {     // MMA -> epilogue, one per accumulator buffer
+  int32_t window;   // -1: no more segments
+  int32_t tile;
+  int32_t flags;    // kStageFirst | kStageLast of the window, as covered by this CTA
+  int32_t zero;     // no MMA was issued (a window without columns)
+  int32_t slot;     // workspace slot for a partial segment
+  int32_t pad_[3];
+};
+
 template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    wcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
-                     const WcsrParams p) {
+    wcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmV, const WcsrParams p) {
   using C_ = Cfg<NACC, Q>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Q * C_::kStageBytes);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Q + 2);
+  // bars: full[Q], empty[Q], acc_full[kAccBufs], acc_empty[kAccBufs], drain
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Q + 2 * kAccBufs + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  StageRec *stage_rec = reinterpret_cast<StageRec *>(tmem_slot + 4);        // [Q]
+  volatile SegRec *seg_rec = reinterpret_cast<volatile SegRec *>(stage_rec + Q);  // [kAccBufs]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const WcsrTask task = p.tasks[blockIdx.x];
-  const int n0 = blockIdx.y * C_::kBN;
-  const int nvalid = min(C_::kBN, p.N - n0);
-  const int nacc = min(NACC, (nvalid + 127) / 128);
-  const int nch = min(C_::kChunks, (nvalid + 63) / 64);
-  const int64_t ncols = task.p_end - task.p_begin;
-  const int nstages = static_cast<int>((ncols + kKC - 1) / kKC);
+  const int n_col_tiles = (p.N + C_::kBN - 1) / C_::kBN;
+  const int64_t total = p.n_stages * n_col_tiles;
+  const int64_t f0 = total * blockIdx.x / gridDim.x;
+  const int64_t f1 = total * (blockIdx.x + 1) / gridDim.x;
+  const int4 *stg = reinterpret_cast<const int4 *>(p.stages);
 
   const uint32_t full0 = smem_addr(&bars[0]);
   const uint32_t empty0 = smem_addr(&bars[Q]);
-  const uint32_t accum_bar = smem_addr(&bars[2 * Q]);
-  const uint32_t drain_bar = smem_addr(&bars[2 * Q + 1]);
+  const uint32_t accf0 = smem_addr(&bars[2 * Q]);
+  const uint32_t acce0 = smem_addr(&bars[2 * Q + kAccBufs]);
+  const uint32_t drain_bar = smem_addr(&bars[2 * Q + 2 * kAccBufs]);
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < Q; ++q) {
-      mbar_init(full0 + 8 * q, 1);
+      mbar_init(full0 + 8 * q, 33);  // 32 cp.async lane arrivals + lane 0's arrive (stage record)
       mbar_init(empty0 + 8 * q, 1);
     }
-    mbar_init(accum_bar, 1);
+    for (int b = 0; b < kAccBufs; ++b) {
+      mbar_init(accf0 + 8 * b, 2);  // the MMA commit + the MMA thread's arrive (segment record)
+      mbar_init(acce0 + 8 * b, kEpiWarps);
+    }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
-    tma_prefetch_desc(&tmV);
-    tma_prefetch_desc(&tmB);
+    // partial-sum records of this CTA (overwritten below when used)
+    p.partials[2 * blockIdx.x] = WcsrPartial{-1, 0, 0, 0};
+    p.partials[2 * blockIdx.x + 1] = WcsrPartial{-1, 0, 0, 0};
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), C_::kTmemCols);
     tmem_relinquish();
   }
@@ -101,170 +159,289 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // Lane l gathers row group g = l % 16 (rows 4g..4g+3 of a stage) for the
-    // column chunks of its half-warp.
-    const int g = lane & 15;
-    constexpr int kChunksPerLane = C_::kChunks / 2;
-    const int c_first = (lane >> 4) * kChunksPerLane;
-    const int32_t oob_row = p.K;  // padding (-1) gathers an out-of-range row: TMA fills zeros
-    auto load_idx = [&](int s) -> int4 {
-      const int64_t pb = task.p_begin + static_cast<int64_t>(s) * kKC + 4 * g;
-      if (s < nstages && pb < task.p_end) return *reinterpret_cast<const int4 *>(p.window_col_idx + pb);
-      return make_int4(-2, -2, -2, -2);
+  if (warp < kProducerWarps) {
+    // ------------------------------------------------------------ producers
+    const uint16_t *Bp = reinterpret_cast<const uint16_t *>(p.B);
+    const uint16_t *Vp = reinterpret_cast<const uint16_t *>(p.values);
+    // Work items of this warp: f = f0 + warp + 4*i.  Item i's descriptor and
+    // column indices are loaded two items ahead into ring slot i % 2 (the
+    // loop is unrolled by 2, so slots are fixed registers).
+    int4 ring_d[2];
+    int32_t ring_lo[2], ring_hi[2];
+    auto prefetch = [&](int slot_, int64_t fi) {
+      const bool in = fi < f1;
+      const int64_t sidx = in ? fi % p.n_stages : 0;
+      ring_d[slot_] = in ? stg[sidx] : make_int4(0, -1, 0, 0);
+      ring_lo[slot_] = in ? p.stage_idx[sidx * kKC + lane] : -2;
+      ring_hi[slot_] = in ? p.stage_idx[sidx * kKC + 32 + lane] : -2;
     };
-    // Index prefetch ring: slot u holds the indices of stage s with s % kPF == u.
-    // The loop is unrolled by kPF so every slot stays in a fixed register and a
-    // load is only waited for when its stage is issued, kPF stages later.
-    int4 ring[kPF];
-#pragma unroll
-    for (int i = 0; i < kPF; ++i) ring[i] = load_idx(i);
-
-    uint32_t stage = 0, phase = 0;
-    int64_t issued = 0;
+    int64_t f = f0 + warp;
+    prefetch(0, f);
+    prefetch(1, f + kProducerWarps);
     bool ok = true;
-    for (int s0 = 0; s0 < nstages && ok; s0 += kPF) {
+    for (; f < f1 && ok; f += 2 * kProducerWarps) {
 #pragma unroll
-      for (int u = 0; u < kPF; ++u) {
-        const int s = s0 + u;
-        if (s >= nstages || !ok) break;
-        const int4 cur = ring[u];
-        ring[u] = load_idx(s + kPF);
+      for (int slot = 0; slot < 2; ++slot) {
+        const int64_t fi = f + slot * kProducerWarps;
+        if (fi >= f1) break;
+        const int4 d = ring_d[slot];
+        const int32_t lo = ring_lo[slot], hi = ring_hi[slot];
+        prefetch(slot, fi + 2 * kProducerWarps);
 
+        const int64_t it = fi - f0;
+        const uint32_t stage = static_cast<uint32_t>(it % Q);
+        const uint32_t phase = static_cast<uint32_t>((it / Q) & 1);
         if (lane == 0) ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns) && !*abort_flag;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        const int64_t pbase = task.p_begin + static_cast<int64_t>(s) * kKC;
-        const int64_t left = task.p_end - pbase;
-        const int groups = left >= kKC ? kKC / 4 : static_cast<int>(left / 4);
         const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
         const uint32_t fb = full0 + 8 * stage;
+        const int tile = static_cast<int>(fi / p.n_stages);
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, kValBytes + groups * 4 * 128 * nch);
-          tma_load_2d(st, &tmV, fb, static_cast<int32_t>(pbase), 0);
+          stage_rec[stage] = StageRec{d.z, d.w, d.y, tile};  // released by this arrive
+          mbar_arrive(fb);
         }
-        __syncwarp();
-        if (g < groups) {
-          const int32_t r0 = cur.x < 0 ? oob_row : cur.x;
-          const int32_t r1 = cur.y < 0 ? oob_row : cur.y;
-          const int32_t r2 = cur.z < 0 ? oob_row : cur.z;
-          const int32_t r3 = cur.w < 0 ? oob_row : cur.w;
+        // The 16 x 64 value tile (rows P_total apart), K-major with the
+        // 128-byte swizzle: lane copies unit lane % 8 of rows lane / 8 + 4q.
+        if (d.z > 0) {
+          const uint32_t u = static_cast<uint32_t>(lane & 7);
+          const int64_t pcol = static_cast<int64_t>(d.x) + u * 8;
+          const bool in = pcol < p.P_total;
 #pragma unroll
-          for (int j = 0; j < kChunksPerLane; ++j) {
-            const int c = c_first + j;
-            if (c < nch)
-              tma_gather4(st + kValBytes + c * kChunkBytes + g * 512, &tmB, fb, n0 + c * 64, r0, r1, r2, r3);
+          for (int q = 0; q < 4; ++q) {
+            const int r = (lane >> 3) + 4 * q;
+            cp_async_16(st + r * 128 + ((u ^ static_cast<uint32_t>(r & 7)) << 4),
+                        in ? static_cast<const void *>(Vp + r * p.P_total + pcol) : static_cast<const void *>(Vp),
+                        in ? 16u : 0u);
           }
         }
-        ++issued;
-        if (++stage == Q) {
-          stage = 0;
-          phase ^= 1u;
+        const int n0 = tile * C_::kBN;
+        if constexpr (NACC == 2) {
+          // one B row (32 units of 16 B) per warp instruction
+          const int n = n0 + lane * 8;
+          const bool n_live = n < p.N;
+          const uint32_t dst_col = kValBytes + (lane >> 3) * kChunkBytes;
+          const uint32_t u = static_cast<uint32_t>(lane & 7);
+          for (int r = 0; r < d.z; ++r) {
+            const int32_t col = __shfl_sync(0xffffffffu, r < 32 ? lo : hi, r & 31);
+            const bool live = n_live && col >= 0;
+            cp_async_16(st + dst_col + r * 128 + ((u ^ static_cast<uint32_t>(r & 7)) << 4),
+                        live ? static_cast<const void *>(Bp + static_cast<int64_t>(col) * p.N + n)
+                             : static_cast<const void *>(Bp),
+                        live ? 16u : 0u);
+          }
+        } else {
+          // two B rows (16 units each) per warp instruction
+          const int v = lane & 15;
+          const int half = lane >> 4;
+          const int n = n0 + v * 8;
+          const bool n_live = n < p.N;
+          const uint32_t dst_col = kValBytes + (v >> 3) * kChunkBytes;
+          const uint32_t u = static_cast<uint32_t>(v & 7);
+          for (int r2 = 0; r2 < d.z; r2 += 2) {
+            const int r = r2 + half;
+            const int32_t col = __shfl_sync(0xffffffffu, r2 < 32 ? lo : hi, r & 31);
+            const bool live = n_live && col >= 0;
+            cp_async_16(st + dst_col + r * 128 + ((u ^ static_cast<uint32_t>(r & 7)) << 4),
+                        live ? static_cast<const void *>(Bp + static_cast<int64_t>(col) * p.N + n)
+                             : static_cast<const void *>(Bp),
+                        live ? 16u : 0u);
+          }
         }
+        cp_async_arrive_noinc(fb);
       }
     }
+    cp_async_wait<0>();
     if (!ok && lane == 0) {
       atomicOr(p.status, kDevTimeout);
       *abort_flag = 1;
-      const int64_t first = issued > Q ? issued - Q : 0;
-      for (int64_t i = first; i < issued; ++i)
-        mbar_wait(full0 + 8 * (i % Q), static_cast<uint32_t>((i / Q) & 1), 1000000ull);
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nstages > 0) {
+    if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(IN_BF16, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, kH);
       uint32_t stage = 0, phase = 0;
+      uint32_t seg = 0;     // window segments started
+      uint32_t buf = 0;
+      int ksteps_done = 0;  // MMA k-steps issued into the current segment
+      int32_t s_flags = 0;
+      bool s_at_f0 = false;
       bool ok = true;
-      for (int s = 0; s < nstages; ++s) {
+      auto open_buffer = [&](uint32_t b, uint32_t use) -> bool {
+        const bool r = mbar_wait(acce0 + 8 * b, (use & 1u) ^ 1u, p.wait_limit_ns) && !*abort_flag;
+        tc_fence_after_sync();
+        return r;
+      };
+      for (int64_t f = f0; f < f1 && ok; ++f) {
         if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns) || *abort_flag) {
           ok = false;
           break;
         }
+        const StageRec rec = stage_rec[stage];
+        const bool seg_first = f == f0 || (rec.flags & kStageFirst);
+        const bool seg_last = f == f1 - 1 || (rec.flags & kStageLast);
+        if (seg_first) {
+          buf = seg % kAccBufs;
+          if (!open_buffer(buf, seg / kAccBufs)) {
+            ok = false;
+            break;
+          }
+          ksteps_done = 0;
+          s_flags = rec.flags & kStageFirst;
+          s_at_f0 = f == f0;
+        }
+        fence_proxy_async_smem();  // the stage's cp.async writes -> async-proxy MMA reads
         tc_fence_after_sync();
         const uint32_t vals = smem_addr(smem + stage * C_::kStageBytes);  // MMA operand B (K-major)
         const uint32_t gath = vals + kValBytes;                           // MMA operand A (MN-major)
-        const int64_t left = ncols - static_cast<int64_t>(s) * kKC;
-        const int ksteps = left >= kKC ? 4 : static_cast<int>(left / 16);
+        const int nacc = min(NACC, (p.N - rec.tile * C_::kBN + 127) / 128);
+        const int ksteps = rec.ncols / 16;
+        const uint32_t acc = tmem + buf * C_::kAccCols;
         for (int kk = 0; kk < ksteps; ++kk) {
           const uint64_t bdesc = smem_desc_sw128(vals + kk * 32, 16, 1024);
 #pragma unroll
           for (int a = 0; a < NACC; ++a) {
             if (a < nacc) {
               const uint64_t adesc = smem_desc_sw128(gath + a * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
-              umma_f16(tmem + a * kH, adesc, bdesc, idesc, (s > 0 || kk > 0) ? 1u : 0u);
+              umma_f16(acc + a * kH, adesc, bdesc, idesc, ksteps_done > 0 ? 1u : 0u);
             }
           }
+          ++ksteps_done;
         }
         umma_commit(empty0 + 8 * stage);
+        if (seg_last) {
+          s_flags |= rec.flags & kStageLast;
+          volatile SegRec &sr = seg_rec[buf];
+          sr.window = rec.window;
+          sr.tile = rec.tile;
+          sr.flags = s_flags;
+          sr.zero = ksteps_done == 0;
+          sr.slot = 2 * static_cast<int32_t>(blockIdx.x) + (s_at_f0 ? 0 : 1);
+          mbar_arrive(accf0 + 8 * buf);  // releases the record
+          umma_commit(accf0 + 8 * buf);  // arrives when the MMAs are done
+          ++seg;
+        }
         if (++stage == Q) {
           stage = 0;
           phase ^= 1u;
         }
       }
       if (ok) {
-        umma_commit(accum_bar);
-      } else {
+        // end marker for the epilogue
+        buf = seg % kAccBufs;
+        ok = open_buffer(buf, seg / kAccBufs);
+        if (ok) {
+          seg_rec[buf].window = -1;
+          mbar_arrive(accf0 + 8 * buf);
+          mbar_arrive(accf0 + 8 * buf);
+        }
+      }
+      if (!ok) {
         atomicOr(p.status, kDevTimeout);
         *abort_flag = 1;
         umma_commit(drain_bar);
         mbar_wait(drain_bar, 0, 1000000ull);
-        mbar_arrive(accum_bar);
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int sp = warp & 3;  // TMEM sub-partition this warp may read
-    const int row0 = task.window * kH;
-    const bool to_ws = task.slot >= 0;
-    float *ws = to_ws ? p.workspace + static_cast<int64_t>(task.slot) * kH * p.N : nullptr;
-    bool have = nstages > 0;
-    if (have) {
-      if (!mbar_wait(accum_bar, 0, p.wait_limit_ns)) {
-        atomicOr(p.status, kDevTimeout);
-        *abort_flag = 1;
-        have = false;
-      } else if (*abort_flag) {
-        have = false;
+    const int sp = warp & 3;
+    for (uint32_t seg = 0;; ++seg) {
+      const uint32_t buf = seg % kAccBufs;
+      const uint32_t use = seg / kAccBufs;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait(accf0 + 8 * buf, use & 1u, p.wait_limit_ns) && !*abort_flag;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      __syncwarp();  // orders the other lanes' record reads after lane 0's acquiring wait
+      if (!ok) {
+        if (lane == 0) {
+          atomicOr(p.status, kDevTimeout);
+          *abort_flag = 1;
+        }
+        break;
       }
+      const int32_t s_window = seg_rec[buf].window;
+      if (s_window < 0) break;
+      const int32_t s_tile = seg_rec[buf].tile;
+      const int32_t s_flags = seg_rec[buf].flags;
+      const bool s_zero = seg_rec[buf].zero != 0;
+      const int slot = seg_rec[buf].slot;
       tc_fence_after_sync();
-    }
-    for (int a = 0; a < nacc; ++a) {
-      const int n = n0 + a * 128 + sp * 32 + lane;
-      uint32_t v[16];
-      if (have) {
-        tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(sp * 32) << 16) + a * kH, v);
-        tmem_ld_wait();
-      } else {
+      const bool complete = s_flags == (kStageFirst | kStageLast);
+      const int n0 = s_tile * C_::kBN;
+      const int nacc = min(NACC, (p.N - n0 + 127) / 128);
+      float *ws = p.workspace + static_cast<int64_t>(slot) * kWcsrSlotFloats;
+      const int row0 = s_window * kH;
+      for (int a = 0; a < nacc; ++a) {
+        uint32_t v[16];
+        if (!s_zero) {
+          tmem_ld_32x32b_x16(tmem + (static_cast<uint32_t>(sp * 32) << 16) + buf * C_::kAccCols + a * kH, v);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0u;
-      }
-      if (n < p.N) {
+          for (int q = 0; q < 16; ++q) v[q] = 0u;
+        }
+        const int col = a * 128 + sp * 32 + lane;  // column within the tile
+        const int n = n0 + col;
+        if (n < p.N) {
+          if (complete) {
 #pragma unroll
-        for (int i = 0; i < kH; ++i) {
-          if (to_ws) {
-            ws[static_cast<int64_t>(i) * p.N + n] = __uint_as_float(v[i]);
-          } else if (row0 + i < p.M) {
-            store_out<OUT_BF16>(p.C, static_cast<int64_t>(row0 + i) * p.N + n, __uint_as_float(v[i]));
+            for (int q = 0; q < kH; ++q)
+              if (row0 + q < p.M)
+                store_out<OUT_BF16>(p.C, static_cast<int64_t>(row0 + q) * p.N + n, __uint_as_float(v[q]));
+          } else {
+#pragma unroll
+            for (int q = 0; q < kH; ++q) ws[q * 256 + col] = __uint_as_float(v[q]);
           }
         }
       }
+      if (!complete && threadIdx.x == 32 * (kMmaWarp + 1))
+        p.partials[slot] = WcsrPartial{s_window, s_tile, s_flags, 0};
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8 * buf);
     }
   }
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, C_::kTmemCols);
   }
 }
 
+// Second pass: slot s holds a window's first stage but not its last -> this
+// block adds that partial and the first-segment partials of the following
+// CTAs (in CTA order) until the one holding the window's last stage, and
+// writes the window's rows of C.
+template <bool OUT_BF16>
+__global__ void __launch_bounds__(256)
+    wcsr_reduce_kernel(const WcsrPartial *partials, const float *ws, void *C, int32_t M, int32_t N, int32_t grid,
+                       int32_t bn) {
+  const int slot = blockIdx.x;
+  const WcsrPartial rec = partials[slot];
+  if (rec.window < 0 || !(rec.flags & kStageFirst) || (rec.flags & kStageLast)) return;
+  const int n0 = rec.col_tile * bn;
+  const int width = min(bn, N - n0);
+  for (int e = threadIdx.x; e < kH * width; e += blockDim.x) {
+    const int q = e / width;
+    const int col = e - q * width;
+    const int row = rec.window * kH + q;
+    float acc = ws[static_cast<int64_t>(slot) * kWcsrSlotFloats + q * 256 + col];
+    for (int c = slot / 2 + 1; c < grid; ++c) {
+      const WcsrPartial r = partials[2 * c];
+      if (r.window != rec.window || r.col_tile != rec.col_tile) break;
+      acc += ws[static_cast<int64_t>(2 * c) * kWcsrSlotFloats + q * 256 + col];
+      if (r.flags & kStageLast) break;
+    }
+    if (row < M) store_out<OUT_BF16>(C, static_cast<int64_t>(row) * N + n0 + col, acc);
+  }
+}
+
 template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
-cudaError_t launch_variant(const CUtensorMap &tmV, const CUtensorMap &tmB, const WcsrParams &p,
-                           cudaStream_t stream) {
+cudaError_t launch_variant(const CUtensorMap &tmV, const WcsrParams &p, cudaStream_t stream) {
   using C_ = Cfg<NACC, Q>;
   auto kern = wcsr_spmm_kernel<NACC, Q, IN_BF16, OUT_BF16>;
   static bool attr_set = false;
@@ -273,75 +450,29 @@ cudaError_t launch_variant(const CUtensorMap &tmV, const CUtensorMap &tmB, const
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(p.n_tasks, (p.N + C_::kBN - 1) / C_::kBN);
-  kern<<<grid, kThreads, C_::kSmemBytes, stream>>>(tmV, tmB, p);
+  kern<<<p.grid, kThreads, C_::kSmemBytes, stream>>>(tmV, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, 0, stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
+                                                               C_::kBN);
   return cudaGetLastError();
 }
 
 template <int NACC, int Q>
-cudaError_t launch_dtypes(const CUtensorMap &tmV, const CUtensorMap &tmB, const WcsrParams &p, bool in_bf16,
-                          bool out_bf16, cudaStream_t s) {
+cudaError_t launch_dtypes(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
+                          cudaStream_t s) {
   if (in_bf16)
-    return out_bf16 ? launch_variant<NACC, Q, true, true>(tmV, tmB, p, s)
-                    : launch_variant<NACC, Q, true, false>(tmV, tmB, p, s);
-  return out_bf16 ? launch_variant<NACC, Q, false, true>(tmV, tmB, p, s)
-                  : launch_variant<NACC, Q, false, false>(tmV, tmB, p, s);
-}
-
-// One thread per 4 consecutive columns of one row of one split window;
-// blockIdx.x names the split window, threads stride over its 16 x N partials.
-template <bool OUT_BF16>
-__global__ void __launch_bounds__(256) wcsr_reduce_kernel(const WcsrSplit *splits, const float *ws, void *C,
-                                                          int32_t M, int32_t N) {
-  const WcsrSplit sp = splits[blockIdx.x];
-  const int64_t per = static_cast<int64_t>(kH) * N;
-  for (int64_t e = (static_cast<int64_t>(blockIdx.y) * blockDim.x + threadIdx.x) * 4; e < per;
-       e += static_cast<int64_t>(gridDim.y) * blockDim.x * 4) {
-    const int r = static_cast<int>(e / N);
-    const int row = sp.window * kH + r;
-    if (row >= M) break;  // rows only grow with e
-    const float *src = ws + static_cast<int64_t>(sp.slot_begin) * per + e;
-    float4 acc = *reinterpret_cast<const float4 *>(src);
-    for (int s = 1; s < sp.n_slots; ++s) {
-      const float4 v = *reinterpret_cast<const float4 *>(src + s * per);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    const int64_t off = static_cast<int64_t>(row) * N + (e - static_cast<int64_t>(r) * N);
-    if constexpr (OUT_BF16) {
-      __nv_bfloat16 *c = reinterpret_cast<__nv_bfloat16 *>(C) + off;
-      c[0] = __float2bfloat16_rn(acc.x);
-      c[1] = __float2bfloat16_rn(acc.y);
-      c[2] = __float2bfloat16_rn(acc.z);
-      c[3] = __float2bfloat16_rn(acc.w);
-    } else {
-      *reinterpret_cast<float4 *>(reinterpret_cast<float *>(C) + off) = acc;
-    }
-  }
+    return out_bf16 ? launch_variant<NACC, Q, true, true>(tmV, p, s) : launch_variant<NACC, Q, true, false>(tmV, p, s);
+  return out_bf16 ? launch_variant<NACC, Q, false, true>(tmV, p, s) : launch_variant<NACC, Q, false, false>(tmV, p, s);
 }
 
 }  // namespace
 
-cudaError_t launch_wcsr(const CUtensorMap &tmV, const CUtensorMap &tmB, const WcsrParams &p, bool in_bf16,
-                        bool out_bf16, cudaStream_t stream) {
-  if (p.n_tasks == 0 || p.N == 0) return cudaSuccess;
-  if (p.N <= 128) return launch_dtypes<1, 10>(tmV, tmB, p, in_bf16, out_bf16, stream);
-  return launch_dtypes<2, 6>(tmV, tmB, p, in_bf16, out_bf16, stream);
-}
-
-cudaError_t launch_wcsr_reduce(const WcsrSplit *splits, int32_t n_splits, const float *workspace, void *C,
-                               int32_t M, int32_t N, bool out_bf16, cudaStream_t stream) {
-  if (n_splits == 0 || N == 0) return cudaSuccess;
-  const int64_t per4 = (static_cast<int64_t>(kH) * N) / 4;  // N % 8 == 0
-  const int64_t blocks = (per4 + 255) / 256;
-  dim3 grid(n_splits, static_cast<unsigned>(blocks < 1024 ? blocks : 1024));
-  if (out_bf16)
-    wcsr_reduce_kernel<true><<<grid, 256, 0, stream>>>(splits, workspace, C, M, N);
-  else
-    wcsr_reduce_kernel<false><<<grid, 256, 0, stream>>>(splits, workspace, C, M, N);
-  return cudaGetLastError();
+cudaError_t launch_wcsr(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
+                        cudaStream_t stream) {
+  if (p.n_stages == 0 || p.N == 0 || p.grid == 0) return cudaSuccess;
+  if (p.N <= 128) return launch_dtypes<1, 10>(tmV, p, in_bf16, out_bf16, stream);
+  return launch_dtypes<2, 6>(tmV, p, in_bf16, out_bf16, stream);
 }
 
 }  // namespace spmm

@@ -18,8 +18,8 @@ def _lib():
     ensure_library()
 
 
-def full_check(m, k, n, rp, ci, vals, dt, out_dt, B, split_cols=None, runs=1):
-    outs, info = run_library("wcsr", m, k, rp, ci, vals, dt, out_dt, B, split_cols=split_cols, runs=runs)
+def full_check(m, k, n, rp, ci, vals, dt, out_dt, B, max_ctas=None, runs=1):
+    outs, info = run_library("wcsr", m, k, rp, ci, vals, dt, out_dt, B, max_ctas=max_ctas, runs=runs)
     C_ref, S_ref = oracle.spmm_csr(m, k, rp, ci, vals, ocode(dt), B)
     for C in outs:
         assert_parity(C, C_ref, S_ref, f"wcsr {m}x{k} N={n}")
@@ -40,18 +40,31 @@ def test_wcsr_parity_small(m, k, n, d, dt, out_dt):
     full_check(m, k, n, rp, ci, vals, dt, out_dt, B)
 
 
-@pytest.mark.parametrize("split,n", [(64, 256), (128, 128), (512, 72)])
-def test_wcsr_split_windows(split, n):
-    """Force long windows to be split; the two-pass sum must match and be
-    bitwise reproducible."""
-    rng = np.random.default_rng(split)
+@pytest.mark.parametrize("ctas,n", [(3, 256), (7, 128), (13, 72), (5, 520)])
+def test_wcsr_windows_cut_between_ctas(ctas, n):
+    """Few persistent CTAs: long windows are cut between CTAs and finished by
+    the second kernel; the result must match and be bitwise reproducible."""
+    rng = np.random.default_rng(ctas)
     m, k = 400, 5000
     rp, ci = W.powerlaw_pattern(rng, m, k, 1.3, 1, 1500, 300, 0.7)
     vals = W.draw_values(rng, len(ci), "u1", "bf16")
     B = W.dense_bits(rng, (k, n), "u1", "bf16")
-    outs, info = full_check(m, k, n, rp, ci, vals, "bf16", "f32", B, split_cols=split, runs=2)
+    outs, info = full_check(m, k, n, rp, ci, vals, "bf16", "f32", B, max_ctas=ctas, runs=2)
     assert info["n_split_windows"] > 0
     assert np.array_equal(outs[0], outs[1])
+
+
+def test_wcsr_window_spanning_many_ctas():
+    """One window much longer than a CTA's share: its partials span several CTAs."""
+    rng = np.random.default_rng(17)
+    m, k, n = 48, 6000, 136
+    rp = np.zeros(m + 1, np.int64)
+    cols = [np.sort(rng.choice(k, 3000 if i == 20 else 3, replace=False)) for i in range(m)]
+    rp[1:] = np.cumsum([len(c) for c in cols])
+    ci = np.concatenate(cols).astype(np.int32)
+    vals = W.draw_values(rng, len(ci), "u1", "bf16")
+    B = W.dense_bits(rng, (k, n), "u1", "bf16")
+    full_check(m, k, n, rp, ci, vals, "bf16", "bf16", B, max_ctas=9, runs=1)
 
 
 def test_wcsr_empty_windows_and_identity():
@@ -80,15 +93,15 @@ def test_wcsr_one_nonzero_per_row_exact():
     ci = rng.integers(0, k, m).astype(np.int32)
     vals = W.draw_values(rng, m, "u1", "f16")
     B = W.dense_bits(rng, (k, n), "u1", "f16")
-    outs, _ = run_library("wcsr", m, k, rp, ci, vals, "f16", "f32", B, split_cols=64)
+    outs, _ = run_library("wcsr", m, k, rp, ci, vals, "f16", "f32", B, max_ctas=5)
     ref = vals.view(np.float16).astype(np.float64)[:, None] * B.view(np.float16).astype(np.float64)[ci]
     assert np.array_equal(outs[0], ref)
 
 
-def sampled_check(w, nsamp=8000, seed=0, split_cols=None):
+def sampled_check(w, nsamp=8000, seed=0, max_ctas=None):
     import torch
     outs, info = run_library("wcsr", w.m, w.k, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.B(),
-                             keep_device=True, split_cols=split_cols)
+                             keep_device=True, max_ctas=max_ctas)
     C = outs[0]
     assert not torch.isnan(C).any().item(), "C not fully written"
     rng = np.random.default_rng(seed)
@@ -109,7 +122,7 @@ def test_wcsr_uniform_full_size():
 def test_wcsr_irregular_full_size_sampled():
     w = W.wcsr_irregular()
     info = sampled_check(w, nsamp=20000)
-    assert info["n_split_windows"] > 0  # the longest windows are split
+    assert info["n_split_windows"] > 0  # windows cut between CTAs
 
 
 @pytest.mark.parametrize("dens", W.WCSR_SWEEP_DENSITY)
