@@ -204,6 +204,39 @@ spmm_status spmm_set_max_ctas(spmm_handle h, int32_t ctas);
  */
 spmm_status spmm_selftest_wait_timeout(int64_t timeout_ns, void *stream, int32_t *dev_status);
 
+/*
+ * spmm_wcsr_run_noalloc -- C = A * B for A in WCSR, for callers that cannot
+ * allocate device memory when they run the product: code whose device memory
+ * all comes from its own pool or arena, or which must not call cudaMalloc /
+ * cudaFree at that point (they may synchronise the device).  The paper has
+ * no counterpart; it runs the same WCSR kernel as spmm_run.
+ * The caller passes device arrays of a WCSR format with window height 16 and
+ * a column padding that is a multiple of 16 (as spmm_wcsr_create /
+ * spmm_export_format produce them):
+ *   window_row_ptr  int64[ceil(m/16) + 1]
+ *   window_col_idx  int32[p_total]       (-1 = padding; other entries in [0, k))
+ *   values          16-bit [16][p_total] row-major, in_t, 16-byte aligned
+ * and B (k x N) and C (m x N) as for spmm_run; C is fully overwritten.
+ * Nothing is allocated: the work list and the partial sums of windows cut
+ * between CTAs live in one static device array of about 10 MB that every GPU
+ * which loads this library holds until the process exits.  Its limit:
+ * ceil(m/16) + p_total/64 <= 131072; larger problems are rejected with
+ * SPMM_ERR_UNSUPPORTED before anything is launched.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress), so make
+ * that first call before any stream capture on that device.
+ * Every call uses the same array, which keeps the previous call's contents
+ * (each call rebuilds what it reads): calls whose work overlaps on the GPU
+ * (other streams, other host threads) race and must be serialised by the
+ * caller.  Asynchronous on `stream`; a bounded wait that runs out is not
+ * reported here.
+ * Errors: INVALID_ARG (null pointers, sizes), UNSUPPORTED (N % 8,
+ * alignment, p_total % 16, the size limit, no sm_103 device), CUDA (launch).
+ */
+spmm_status spmm_wcsr_run_noalloc(const int64_t *window_row_ptr, const int32_t *window_col_idx,
+                                  const void *values, int64_t m, int64_t k, int64_t p_total,
+                                  spmm_dtype in_t, spmm_dtype out_t, const void *B, void *C,
+                                  int64_t N, void *stream);
+
 /* spmm_status_str -- static English name of a status. */
 const char *spmm_status_str(spmm_status s);
 

@@ -48,7 +48,7 @@ EXPORTS = (
     "spmm_bcsr_create", "spmm_wcsr_create", "spmm_run", "spmm_run_host", "spmm_destroy",
     "spmm_format_info", "spmm_export_format", "spmm_bcsr_convert", "spmm_wcsr_convert",
     "spmm_check", "spmm_set_max_ctas", "spmm_selftest_wait_timeout", "spmm_status_str",
-    "spmm_last_error",
+    "spmm_last_error", "spmm_wcsr_run_noalloc",
 )
 
 
@@ -96,6 +96,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "spmm_check": [P, P],
         "spmm_set_max_ctas": [P, ctypes.c_int32],
         "spmm_selftest_wait_timeout": [I64, P, ctypes.POINTER(ctypes.c_int32)],
+        "spmm_wcsr_run_noalloc": [P, P, P, I64, I64, I64, I32, I32, P, P, I64, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -216,6 +217,13 @@ def spmm_selftest_wait_timeout(timeout_ns: int, stream: int = 0) -> int:
     _check(load_library().spmm_selftest_wait_timeout(timeout_ns, stream or None, ctypes.byref(out)),
            "spmm_selftest_wait_timeout")
     return out.value
+
+
+def spmm_wcsr_run_noalloc(window_row_ptr: int, window_col_idx: int, values: int, m: int, k: int, p_total: int,
+                          in_t, out_t, B_ptr: int, C_ptr: int, N: int, stream: int = 0) -> None:
+    """WCSR product from caller-owned device arrays, allocating nothing (pointers are device addresses)."""
+    _check(load_library().spmm_wcsr_run_noalloc(window_row_ptr, window_col_idx, values, m, k, p_total, _dt(in_t),
+                                                _dt(out_t), B_ptr, C_ptr, N, stream or None), "spmm_wcsr_run_noalloc")
 
 
 def spmm_bcsr_convert(m, k, row_ptr, col_idx, vals, b_row=64, b_col=64):

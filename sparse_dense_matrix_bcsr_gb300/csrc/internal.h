@@ -53,6 +53,8 @@ struct WcsrParams {
   const WcsrStage *stages;       // device, n_stages
   const int32_t *stage_idx;      // device, n_stages x 64: stage s's column indices, -2 past its ncols
   const void *values;            // device, 16 x P_total row-major
+  const int32_t *window_col_idx; // device, P_total (read by the no-allocation variant only)
+  const int64_t *n_stages_dev;   // device stage count (no-allocation variant only)
   const void *B;                 // device, K x N row-major
   void *C;                       // device, M x N row-major
   float *workspace;              // device, 2 * grid x 16 x 256 fp32
@@ -67,6 +69,18 @@ struct WcsrParams {
 
 // Workspace floats per partial slot (16 rows x 256 columns).
 constexpr int64_t kWcsrSlotFloats = 16 * 256;
+
+// Limits of spmm_wcsr_run_noalloc's static scratch.
+constexpr int64_t kNoallocMaxStages = 131072;
+constexpr int kNoallocMaxCtas = 256;
+
+// spmm_wcsr_run_noalloc's launches: builds the stage list from the caller's
+// window_row_ptr into the static scratch, runs the WCSR kernel's no-allocation
+// variant and the partial-sum pass.  p carries the caller's arrays, B, C and
+// the sizes; the scratch pointers are filled in here.
+cudaError_t launch_wcsr_noalloc(WcsrParams p, const int64_t *window_row_ptr, int64_t n_windows, int num_sms,
+                                bool in_bf16, bool out_bf16, cudaStream_t stream);
+size_t wcsr_noalloc_scratch_bytes();
 
 // tmV covers the values array as [16 rows, P_total cols] with 64 x 16 boxes
 // and 128-byte swizzle.  Runs the SpMM kernel, then the kernel that adds the

@@ -277,6 +277,8 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
   p.stages = h->d_stages;
   p.stage_idx = h->d_stage_idx;
   p.values = h->d_vals;
+  p.window_col_idx = h->d_idx;
+  p.n_stages_dev = nullptr;
   p.P_total = h->n_units;
   p.B = B;
   p.C = C;
@@ -417,6 +419,52 @@ spmm_status spmm_set_max_ctas(spmm_handle h, int32_t ctas) {
   if (!h) return fail(SPMM_ERR_INVALID_ARG, "handle is NULL");
   if (ctas < 0) return fail(SPMM_ERR_INVALID_ARG, "ctas must be >= 0");
   h->max_ctas = ctas;
+  return SPMM_OK;
+}
+
+spmm_status spmm_wcsr_run_noalloc(const int64_t *window_row_ptr, const int32_t *window_col_idx, const void *values,
+                                  int64_t m, int64_t k, int64_t p_total, spmm_dtype in_t, spmm_dtype out_t,
+                                  const void *B, void *C, int64_t N, void *stream) {
+  if (!window_row_ptr || !B || !C || (p_total > 0 && (!window_col_idx || !values)))
+    return fail(SPMM_ERR_INVALID_ARG, "a device pointer is NULL");
+  if (m < 0 || k < 0 || m >= (1ll << 31) || k >= (1ll << 31) || p_total < 0 || p_total >= (1ll << 31))
+    return fail(SPMM_ERR_INVALID_ARG, "m, k, p_total must be in [0, 2^31)");
+  if (in_t != SPMM_F16 && in_t != SPMM_BF16) return fail(SPMM_ERR_INVALID_ARG, "in_t must be F16 or BF16");
+  if (out_t != SPMM_F32 && out_t != SPMM_BF16) return fail(SPMM_ERR_INVALID_ARG, "out_t must be F32 or BF16");
+  if (N <= 0 || N >= (1ll << 31)) return fail(SPMM_ERR_INVALID_ARG, "N must be in (0, 2^31)");
+  if (N % 8 != 0) return fail(SPMM_ERR_UNSUPPORTED, "N must be a multiple of 8 (16-byte rows of B)");
+  if (N > 65535ll * 128) return fail(SPMM_ERR_UNSUPPORTED, "N above 65535 * 128 exceeds the launch grid");
+  if (p_total % 16 != 0) return fail(SPMM_ERR_UNSUPPORTED, "p_total must be a multiple of 16 (column padding)");
+  if ((reinterpret_cast<uintptr_t>(B) | reinterpret_cast<uintptr_t>(C) | reinterpret_cast<uintptr_t>(values)) & 15)
+    return fail(SPMM_ERR_UNSUPPORTED, "B, C and values must be 16-byte aligned");
+  const int64_t n_windows = (m + 15) / 16;
+  const int64_t max_stages = n_windows + p_total / 64;  // each window: ceil(P_w/64) <= P_w/64 + 1 stages
+  if (max_stages > spmm::kNoallocMaxStages)
+    return fail(SPMM_ERR_UNSUPPORTED,
+                "problem needs up to %lld stages; the static scratch of spmm_wcsr_run_noalloc holds %lld "
+                "(ceil(m/16) + p_total/64 must not exceed it)",
+                static_cast<long long>(max_stages), static_cast<long long>(spmm::kNoallocMaxStages));
+  if (m == 0) return SPMM_OK;
+  int dev = 0, sms = 0, major = 0, minor = 0;
+  CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+  CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "device attribute");
+  CUDA_TRY(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev), "device attribute");
+  CUDA_TRY(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev), "device attribute");
+  if (major != 10 || minor != 3) return fail(SPMM_ERR_UNSUPPORTED, "the kernels need an sm_103 (GB300) device");
+  spmm::WcsrParams p;
+  std::memset(&p, 0, sizeof p);
+  p.values = values;
+  p.window_col_idx = window_col_idx;
+  p.B = B;
+  p.C = C;
+  p.P_total = p_total;
+  p.M = static_cast<int32_t>(m);
+  p.N = static_cast<int32_t>(N);
+  p.K = static_cast<int32_t>(k);
+  p.wait_limit_ns = kDefaultWaitLimitNs;
+  cudaError_t e = spmm::launch_wcsr_noalloc(p, window_row_ptr, n_windows, sms, in_t == SPMM_BF16,
+                                            out_t == SPMM_BF16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "no-allocation WCSR launch");
   return SPMM_OK;
 }
 

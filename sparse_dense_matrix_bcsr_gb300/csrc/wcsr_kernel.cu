@@ -45,6 +45,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstring>
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -107,7 +110,11 @@ struct SegRec {     // MMA -> epilogue, one per accumulator buffer
   int32_t pad_[3];
 };
 
-template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
+// NOALLOC: the variant behind spmm_wcsr_run_noalloc -- the stage count is
+// read from device memory (the stage list is built on the device), CTAs
+// beyond the number of work items leave at once, and column indices are read
+// from window_col_idx at each stage's first packed column.
+template <int NACC, int Q, bool IN_BF16, bool OUT_BF16, bool NOALLOC = false>
 __global__ void __launch_bounds__(kThreads, 1)
     wcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmV, const WcsrParams p) {
   using C_ = Cfg<NACC, Q>;
@@ -123,9 +130,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_col_tiles = (p.N + C_::kBN - 1) / C_::kBN;
-  const int64_t total = p.n_stages * n_col_tiles;
-  const int64_t f0 = total * blockIdx.x / gridDim.x;
-  const int64_t f1 = total * (blockIdx.x + 1) / gridDim.x;
+  const int64_t n_stages = NOALLOC ? *p.n_stages_dev : p.n_stages;
+  const int64_t total = n_stages * n_col_tiles;
+  const int64_t grid = NOALLOC ? (total < gridDim.x ? total : gridDim.x) : gridDim.x;
+  if (NOALLOC && blockIdx.x >= grid) {
+    if (threadIdx.x == 0) {
+      p.partials[2 * blockIdx.x] = WcsrPartial{-1, 0, 0, 0};
+      p.partials[2 * blockIdx.x + 1] = WcsrPartial{-1, 0, 0, 0};
+    }
+    return;
+  }
+  const int64_t f0 = total * blockIdx.x / grid;
+  const int64_t f1 = total * (blockIdx.x + 1) / grid;
   const int4 *stg = reinterpret_cast<const int4 *>(p.stages);
 
   const uint32_t full0 = smem_addr(&bars[0]);
@@ -170,10 +186,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t ring_lo[2], ring_hi[2];
     auto prefetch = [&](int slot_, int64_t fi) {
       const bool in = fi < f1;
-      const int64_t sidx = in ? fi % p.n_stages : 0;
+      const int64_t sidx = in ? fi % n_stages : 0;
       ring_d[slot_] = in ? stg[sidx] : make_int4(0, -1, 0, 0);
-      ring_lo[slot_] = in ? p.stage_idx[sidx * kKC + lane] : -2;
-      ring_hi[slot_] = in ? p.stage_idx[sidx * kKC + 32 + lane] : -2;
+      if constexpr (NOALLOC) {
+        const int4 d = ring_d[slot_];
+        ring_lo[slot_] = lane < d.z ? p.window_col_idx[static_cast<int64_t>(d.x) + lane] : -2;
+        ring_hi[slot_] = lane + 32 < d.z ? p.window_col_idx[static_cast<int64_t>(d.x) + 32 + lane] : -2;
+      } else {
+        ring_lo[slot_] = in ? p.stage_idx[sidx * kKC + lane] : -2;
+        ring_hi[slot_] = in ? p.stage_idx[sidx * kKC + 32 + lane] : -2;
+      }
     };
     int64_t f = f0 + warp;
     prefetch(0, f);
@@ -196,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
         const uint32_t fb = full0 + 8 * stage;
-        const int tile = static_cast<int>(fi / p.n_stages);
+        const int tile = static_cast<int>(fi / n_stages);
         if (lane == 0) {
           stage_rec[stage] = StageRec{d.z, d.w, d.y, tile};  // released by this arrive
           mbar_arrive(fb);
@@ -224,7 +246,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t u = static_cast<uint32_t>(lane & 7);
           for (int r = 0; r < d.z; ++r) {
             const int32_t col = __shfl_sync(0xffffffffu, r < 32 ? lo : hi, r & 31);
-            const bool live = n_live && col >= 0;
+            // caller-supplied indices (no-allocation variant) are clamped to B's rows
+            const bool live = n_live && col >= 0 && (!NOALLOC || col < p.K);
             cp_async_16(st + dst_col + r * 128 + ((u ^ static_cast<uint32_t>(r & 7)) << 4),
                         live ? static_cast<const void *>(Bp + static_cast<int64_t>(col) * p.N + n)
                              : static_cast<const void *>(Bp),
@@ -241,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r2 = 0; r2 < d.z; r2 += 2) {
             const int r = r2 + half;
             const int32_t col = __shfl_sync(0xffffffffu, r2 < 32 ? lo : hi, r & 31);
-            const bool live = n_live && col >= 0;
+            const bool live = n_live && col >= 0 && (!NOALLOC || col < p.K);
             cp_async_16(st + dst_col + r * 128 + ((u ^ static_cast<uint32_t>(r & 7)) << 4),
                         live ? static_cast<const void *>(Bp + static_cast<int64_t>(col) * p.N + n)
                              : static_cast<const void *>(Bp),
@@ -466,7 +489,126 @@ cudaError_t launch_dtypes(const CUtensorMap &tmV, const WcsrParams &p, bool in_b
   return out_bf16 ? launch_variant<NACC, Q, false, true>(tmV, p, s) : launch_variant<NACC, Q, false, false>(tmV, p, s);
 }
 
+// ------------------------------------------------------------ no-allocation variant
+// Builds the stage list of spmm_wcsr_run_noalloc on the device: one block,
+// each thread walks a contiguous run of windows, counts their stages
+// (ceil(P_w / 64), at least 1), a block-wide exclusive scan places the runs,
+// and the threads write their stages.  The total goes to *n_stages.
+__global__ void __launch_bounds__(1024)
+    wcsr_noalloc_stages_kernel(const int64_t *window_row_ptr, int64_t n_windows, WcsrStage *stages,
+                               int64_t *n_stages, uint32_t *status) {
+  __shared__ int64_t part[1024];
+  const int t = threadIdx.x;
+  if (t == 0) *status = 0;  // the scratch keeps the previous call's contents
+  const int64_t per = (n_windows + blockDim.x - 1) / blockDim.x;
+  const int64_t w0 = t * per < n_windows ? t * per : n_windows;
+  const int64_t w1 = w0 + per < n_windows ? w0 + per : n_windows;
+  int64_t cnt = 0;
+  for (int64_t w = w0; w < w1; ++w) {
+    const int64_t pw = window_row_ptr[w + 1] - window_row_ptr[w];
+    cnt += pw > 0 ? (pw + kKC - 1) / kKC : 1;
+  }
+  part[t] = cnt;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive scan (Hillis-Steele)
+    const int64_t v = t >= off ? part[t - off] : 0;
+    __syncthreads();
+    part[t] += v;
+    __syncthreads();
+  }
+  int64_t pos = part[t] - cnt;
+  for (int64_t w = w0; w < w1; ++w) {
+    const int64_t b = window_row_ptr[w], e = window_row_ptr[w + 1];
+    if (e == b) {
+      stages[pos++] = WcsrStage{static_cast<int32_t>(b), static_cast<int32_t>(w), 0, kStageFirst | kStageLast};
+      continue;
+    }
+    for (int64_t q = b; q < e; q += kKC) {
+      const int32_t flags = (q == b ? kStageFirst : 0) | (q + kKC >= e ? kStageLast : 0);
+      stages[pos++] = WcsrStage{static_cast<int32_t>(q), static_cast<int32_t>(w),
+                                static_cast<int32_t>(e - q < kKC ? e - q : kKC), flags};
+    }
+  }
+  if (t == 1023) *n_stages = part[1023];
+}
+
+template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
+cudaError_t launch_noalloc_variant(const WcsrParams &p, cudaStream_t stream) {
+  using C_ = Cfg<NACC, Q>;
+  auto kern = wcsr_spmm_kernel<NACC, Q, IN_BF16, OUT_BF16, true>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap unused;  // the kernel loads values with cp.async; the map is not read
+  memset(&unused, 0, sizeof unused);
+  kern<<<p.grid, kThreads, C_::kSmemBytes, stream>>>(unused, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, 0, stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
+                                                               C_::kBN);
+  return cudaGetLastError();
+}
+
+// Scratch of spmm_wcsr_run_noalloc: stage list, partial-sum slots (two per
+// CTA), partial records and the stage count.  Held by every GPU that loads
+// the library, for the life of the process.
+constexpr size_t kNoallocStageBytes = static_cast<size_t>(kNoallocMaxStages) * sizeof(WcsrStage);
+constexpr size_t kNoallocWsBytes = static_cast<size_t>(2 * kNoallocMaxCtas) * kWcsrSlotFloats * sizeof(float);
+constexpr size_t kNoallocRecBytes = static_cast<size_t>(2 * kNoallocMaxCtas) * sizeof(WcsrPartial);
+constexpr size_t kNoallocScratchBytes = kNoallocStageBytes + kNoallocWsBytes + kNoallocRecBytes + 256;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
+
 }  // namespace
+
+size_t wcsr_noalloc_scratch_bytes() { return kNoallocScratchBytes; }
+
+cudaError_t launch_wcsr_noalloc(WcsrParams p, const int64_t *window_row_ptr, int64_t n_windows, int num_sms,
+                                bool in_bf16, bool out_bf16, cudaStream_t stream) {
+  // Device address of the scratch array, looked up once per device with
+  // that device current (in host code the array's name is only a stand-in).
+  static std::mutex mu;
+  static uint8_t *addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  uint8_t *base;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+      void *ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      if (e != cudaSuccess) return e;
+      addr[dev] = static_cast<uint8_t *>(ptr);
+    }
+    base = addr[dev];
+  }
+  WcsrStage *stages = reinterpret_cast<WcsrStage *>(base);
+  p.stages = stages;
+  p.workspace = reinterpret_cast<float *>(base + kNoallocStageBytes);
+  p.partials = reinterpret_cast<WcsrPartial *>(base + kNoallocStageBytes + kNoallocWsBytes);
+  uint8_t *tail = base + kNoallocStageBytes + kNoallocWsBytes + kNoallocRecBytes;  // 256 spare bytes
+  p.n_stages_dev = reinterpret_cast<int64_t *>(tail);
+  p.status = reinterpret_cast<uint32_t *>(tail + 8);  // bounded-wait timeouts (not reported by this entry point)
+  p.grid = num_sms < kNoallocMaxCtas ? num_sms : kNoallocMaxCtas;
+  wcsr_noalloc_stages_kernel<<<1, 1024, 0, stream>>>(window_row_ptr, n_windows, stages,
+                                                      reinterpret_cast<int64_t *>(tail), p.status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.N <= 128) {
+    if (in_bf16) return out_bf16 ? launch_noalloc_variant<1, 10, true, true>(p, stream)
+                                 : launch_noalloc_variant<1, 10, true, false>(p, stream);
+    return out_bf16 ? launch_noalloc_variant<1, 10, false, true>(p, stream)
+                    : launch_noalloc_variant<1, 10, false, false>(p, stream);
+  }
+  if (in_bf16) return out_bf16 ? launch_noalloc_variant<2, 6, true, true>(p, stream)
+                               : launch_noalloc_variant<2, 6, true, false>(p, stream);
+  return out_bf16 ? launch_noalloc_variant<2, 6, false, true>(p, stream)
+                  : launch_noalloc_variant<2, 6, false, false>(p, stream);
+}
 
 cudaError_t launch_wcsr(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
                         cudaStream_t stream) {
