@@ -45,7 +45,10 @@ L2_FLUSH_BYTES = 256 << 20
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
 # valid only for the kernel source it was taken on (sha256 of the file).
-MEASURED_TRAFFIC = {}
+MEASURED_TRAFFIC = {
+    # bcsr_weight: 370 MB at N = 8192 (profiles/bcsr_kernel_bcsr_weight_N8192.md), B and C scale with N
+    "bcsr_kernel.cu": {"src_sha": "c34275d6ac6f4738", "bytes_per_launch": 2.96e9},
+}
 
 
 def load_peaks():
