@@ -200,21 +200,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cnt = (je - jbase) < 32 ? static_cast<int>(je - jbase) : 32;
         for (int i = 0; i < cnt; ++i) {
           const int32_t bcol = __shfl_sync(0xffffffffu, my_col, i);
-          if (lane == 0) {
-            if (!mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns) || *abort_flag) {
-              ok = false;
-            } else {
-              const uint32_t fb = full0 + 8 * stage;
-              const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
-              mbar_arrive_expect_tx(fb, kBlkBytes + nch * kChunkBytes);
-              tma_load_2d(st, &tmA, fb, 0, static_cast<int32_t>((jbase + i) * kBlk));
-              for (int c = 0; c < nch; ++c)
-                tma_load_2d(st + kBlkBytes + c * kChunkBytes, &tmB, fb, n0 + c * 64, bcol * kBlk);
-              ++issued;
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
+          // the whole warp takes the wait (see mbar_wait_warp); lane 0 issues
+          ok = mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns);
+          ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
           if (!ok) break;
+          if (lane == 0) {
+            const uint32_t fb = full0 + 8 * stage;
+            const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
+            mbar_arrive_expect_tx(fb, kBlkBytes + nch * kChunkBytes);
+            tma_load_2d(st, &tmA, fb, 0, static_cast<int32_t>((jbase + i) * kBlk));
+            for (int c = 0; c < nch; ++c)
+              tma_load_2d(st + kBlkBytes + c * kChunkBytes, &tmB, fb, n0 + c * 64, bcol * kBlk);
+          }
+          ++issued;
           if (++stage == Q) {
             stage = 0;
             phase ^= 1u;
@@ -232,8 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp takes the waits (see mbar_wait_warp); lane 0 issues.
+    {
       constexpr uint32_t idesc = idesc_f16(IN_BF16, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, 64);
+      const bool leader = lane == 0;
       uint32_t stage = 0, phase = 0;
       uint32_t tcount = 0;  // non-empty tiles processed
       bool ok = true;
@@ -247,51 +247,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t buf = tcount & 1u;
         const uint32_t use = tcount >> 1;
         // Wait until the epilogue has drained this accumulator set.
-        if (!mbar_wait(acce0 + 8 * buf, (use & 1u) ^ 1u, p.wait_limit_ns) || *abort_flag) {
-          ok = false;
-          break;
-        }
+        ok = mbar_wait_warp(acce0 + 8 * buf, (use & 1u) ^ 1u, p.wait_limit_ns);
+        ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
+        if (!ok) break;
         tc_fence_after_sync();
         const uint32_t acc = tmem + buf * C_::kAccCols;
         for (int j = 0; j < nblk; ++j) {
-          if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns) || *abort_flag) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          if constexpr (LSU_CH > 0) fence_proxy_async_smem();  // cp.async writes -> async-proxy MMA reads
-          const uint32_t a_blk = smem_addr(smem + stage * C_::kStageBytes);  // A block: MMA operand B
-          const uint32_t b_til = a_blk + kBlkBytes;                          // B tile:  MMA operand A
+          ok = mbar_wait_warp(full0 + 8 * stage, phase, p.wait_limit_ns);
+          ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
+          if (!ok) break;
+          if (leader) {
+            tc_fence_after_sync();
+            if constexpr (LSU_CH > 0) fence_proxy_async_smem();  // cp.async writes -> async-proxy MMA reads
+            const uint32_t a_blk = smem_addr(smem + stage * C_::kStageBytes);  // A block: MMA operand B
+            const uint32_t b_til = a_blk + kBlkBytes;                          // B tile:  MMA operand A
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(a_blk + kk * 32, 16, 1024);
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t bdesc = smem_desc_sw128(a_blk + kk * 32, 16, 1024);
 #pragma unroll
-            for (int a = 0; a < NACC; ++a) {
-              if (a < nacc) {
-                const uint64_t adesc =
-                    smem_desc_sw128(b_til + a * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
-                umma_f16(acc + a * 64, adesc, bdesc, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+              for (int a = 0; a < NACC; ++a) {
+                if (a < nacc) {
+                  const uint64_t adesc =
+                      smem_desc_sw128(b_til + a * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
+                  umma_f16(acc + a * 64, adesc, bdesc, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                }
               }
             }
+            umma_commit(empty0 + 8 * stage);  // frees the stage once these MMAs have read it
           }
-          umma_commit(empty0 + 8 * stage);  // frees the stage once these MMAs have read it
+          __syncwarp();
           if (++stage == Q) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(accf0 + 8 * buf);  // accumulator set ready for the epilogue
+        if (leader) umma_commit(accf0 + 8 * buf);  // accumulator set ready for the epilogue
         ++tcount;
       }
       if (!ok) {
-        atomicOr(p.status, kDevTimeout);
-        *abort_flag = 1;
-        umma_commit(drain_bar);
-        mbar_wait(drain_bar, 0, 1000000ull);
-        // release the epilogue of the tile that will not complete
-        mbar_arrive(accf0);
-        mbar_arrive(accf0 + 8);
+        if (leader) {
+          atomicOr(p.status, kDevTimeout);
+          *abort_flag = 1;
+          umma_commit(drain_bar);
+        }
+        mbar_wait_warp(drain_bar, 0, 1000000ull);
+        if (leader) {
+          // release the epilogue of the tile that will not complete
+          mbar_arrive(accf0);
+          mbar_arrive(accf0 + 8);
+        }
       }
     }
     __syncwarp();
@@ -317,9 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t buf = tcount & 1u;
       const uint32_t use = tcount >> 1;
-      if (!mbar_wait(accf0 + 8 * buf, use & 1u, p.wait_limit_ns)) {
-        atomicOr(p.status, kDevTimeout);
-        *abort_flag = 1;
+      if (!mbar_wait_warp(accf0 + 8 * buf, use & 1u, p.wait_limit_ns)) {
+        if (lane == 0) {
+          atomicOr(p.status, kDevTimeout);
+          *abort_flag = 1;
+        }
         break;
       }
       if (*abort_flag) break;

@@ -52,7 +52,9 @@ struct WcsrPartial {
 struct WcsrParams {
   const WcsrStage *stages;       // device, n_stages
   const int32_t *stage_idx;      // device, n_stages x 64: stage s's column indices, -2 past its ncols
-  const void *values;            // device, 16 x P_total row-major
+  const void *values;            // device, 16 x P_total row-major (read by the no-allocation variant)
+  const void *stage_vals;        // device, n_stages x 2 KB: stage s's 16 x 64 value tile in the MMA's
+                                 // swizzled K-major layout (zero past its ncols)
   const int32_t *window_col_idx; // device, P_total (read by the no-allocation variant only)
   const int64_t *n_stages_dev;   // device stage count (no-allocation variant only)
   const void *B;                 // device, K x N row-major

@@ -41,35 +41,56 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// One probe of the phase; the thread may be suspended for up to about
-// 20 us (the hint) while the phase is incomplete, and resumes as soon as it
-// completes, so waiting warps do not take issue slots from working ones.
+// One probe of the phase: true once the phase with this parity has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(bar), "r"(parity), "r"(20000)
+      : "r"(bar), "r"(parity)
       : "memory");
   return done != 0;
 }
 
 // Wait until the phase with the given parity has completed, for at most
 // limit_ns nanoseconds.  Returns false when the limit ran out; no wait in
-// this library is unbounded.  The bound is counted with the SM's own cycle
-// counter (cheap to read) at 2.1 GHz, so at lower clocks the wait lasts
-// proportionally longer but still ends.
+// this library is unbounded.  After two quick probes the thread sleeps
+// between probes (32 ns doubling to 256 ns): on GB300 a warp polling an
+// mbarrier in a tight loop occupies the shared-memory pipe that the copying
+// warps' cp.async needs (four polling warps cut a gather pipeline's rate to a
+// third).  The bound is counted with the SM's cycle counter at 2.1 GHz, so at
+// lower clocks the wait lasts proportionally longer but still ends.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity) || mbar_try_wait(bar, parity)) return true;
   const long long limit_cycles = static_cast<long long>(limit_ns) * 21 / 10;
   const long long t0 = clock64();
+  uint32_t sleep_ns = 32;
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 4; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    __nanosleep(sleep_ns);
+    if (sleep_ns < 256) sleep_ns <<= 1;
+    if (mbar_try_wait(bar, parity)) return true;
     if (clock64() - t0 > limit_cycles) return false;
+  }
+}
+
+// The same wait taken by a whole converged warp: every lane probes, lane 0's
+// result decides for all.  Measured on GB300: a gather pipeline whose warps
+// waited with lane 0 alone (the other lanes parked at a warp barrier) ran at a
+// third of the rate it reached when all 32 lanes took the wait together, so
+// every role in this library that has whole warps waits this way.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (__shfl_sync(0xffffffffu, mbar_try_wait(bar, parity) ? 1 : 0, 0)) return true;
+  const long long limit_cycles = static_cast<long long>(limit_ns) * 21 / 10;
+  const long long t0 = clock64();
+  uint32_t sleep_ns = 32;
+  while (true) {
+    __nanosleep(sleep_ns);
+    if (sleep_ns < 128) sleep_ns <<= 1;
+    int state = mbar_try_wait(bar, parity) ? 1 : (clock64() - t0 > limit_cycles ? 2 : 0);
+    state = __shfl_sync(0xffffffffu, state, 0);
+    if (state != 0) return state == 1;
   }
 }
 
@@ -96,6 +117,17 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// Contiguous bulk copy global -> shared (size a multiple of 16 bytes, both
+// addresses 16-byte aligned); completion is reported to `bar` as transaction
+// bytes.  Runs on the TMA engine, outside the issuing thread's cp.async
+// tracking.
+__device__ __forceinline__ void tma_bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 

@@ -108,6 +108,7 @@ struct spmm_handle_s {
   int64_t n_stages = 0;
   spmm::WcsrStage *d_stages = nullptr;
   int32_t *d_stage_idx = nullptr;
+  uint16_t *d_stage_vals = nullptr;
   float *d_ws = nullptr;
   spmm::WcsrPartial *d_partials = nullptr;
   int64_t ws_slots = 0;
@@ -149,6 +150,7 @@ void free_handle(spmm_handle h) {
   cudaFree(h->d_vals);
   cudaFree(h->d_stages);
   cudaFree(h->d_stage_idx);
+  cudaFree(h->d_stage_vals);
   cudaFree(h->d_partials);
   cudaFree(h->d_ws);
   cudaFree(h->d_status);
@@ -182,36 +184,67 @@ spmm_status upload_common(spmm_handle h, const HostFormat &f) {
 
 // The WCSR stage list: each window cut into stages of at most 64 packed
 // columns, in window order; a window without columns gets one empty stage.
-spmm_status build_stages(spmm_handle h, const std::vector<int64_t> &wptr, const std::vector<int32_t> &widx) {
+// The kernel reads each stage's column indices and 16 x 64 value tile from
+// per-stage copies (stage_idx, stage_vals).  In those copies a window of
+// ns >= 2 stages deals its padded column list round-robin over its stages
+// (stage j takes positions j, j + ns, j + 2 ns, ...; positions past P_w are
+// padding), so each stage's rows of B span the whole window: packed columns
+// are sorted, and windows processed at the same time by different CTAs would
+// otherwise all gather from the same band of B rows and the same L2 slices.
+// The product is the same sum in another order.
+spmm_status build_stages(spmm_handle h, const std::vector<int64_t> &wptr, const std::vector<int32_t> &widx,
+                         const std::vector<uint16_t> &wvals) {
   std::vector<spmm::WcsrStage> st;
+  std::vector<int32_t> sidx;
+  std::vector<uint16_t> svals;
   const int64_t nw = h->n_groups;
+  const int64_t P = h->n_units;
+  auto put_val = [&](size_t stage, int r, int c, uint16_t v) {
+    // row r at r * 128 bytes, 16-byte unit u stored at unit u ^ (r % 8)
+    svals[stage * 1024 + r * 64 + (((c >> 3) ^ (r & 7)) << 3) + (c & 7)] = v;
+  };
   for (int64_t w = 0; w < nw; ++w) {
-    const int64_t b = wptr[w], e = wptr[w + 1];
-    if (e == b) {
+    const int64_t b = wptr[w], e = wptr[w + 1], pw = e - b;
+    if (pw == 0) {
       st.push_back({static_cast<int32_t>(b), static_cast<int32_t>(w), 0, spmm::kStageFirst | spmm::kStageLast});
+      sidx.resize(sidx.size() + 64, -2);
+      svals.resize(svals.size() + 1024, 0);
       continue;
     }
-    for (int64_t p = b; p < e; p += 64) {
-      int32_t flags = (p == b ? spmm::kStageFirst : 0) | (p + 64 >= e ? spmm::kStageLast : 0);
-      st.push_back({static_cast<int32_t>(p), static_cast<int32_t>(w), static_cast<int32_t>(std::min<int64_t>(64, e - p)),
-                    flags});
+    const int64_t ns = (pw + 63) / 64;
+    for (int64_t j = 0; j < ns; ++j) {
+      const size_t s = st.size();
+      const int32_t flags = (j == 0 ? spmm::kStageFirst : 0) | (j == ns - 1 ? spmm::kStageLast : 0);
+      const int32_t ncols = ns == 1 ? static_cast<int32_t>(pw) : 64;
+      st.push_back({static_cast<int32_t>(b + 64 * j), static_cast<int32_t>(w), ncols, flags});
+      sidx.resize(sidx.size() + 64, -2);
+      svals.resize(svals.size() + 1024, 0);
+      for (int c = 0; c < ncols; ++c) {
+        const int64_t q = ns == 1 ? c : j + ns * c;  // position within the window
+        if (q >= pw) {
+          sidx[s * 64 + c] = -1;  // padding: zero values, no B row
+          continue;
+        }
+        sidx[s * 64 + c] = widx[b + q];
+        for (int r = 0; r < 16; ++r) put_val(s, r, c, wvals[r * P + b + q]);
+      }
     }
   }
   h->n_stages = static_cast<int64_t>(st.size());
-  // Column indices of each stage at a fixed place (64 per stage).
-  std::vector<int32_t> sidx(st.size() * 64, -2);
-  for (size_t i = 0; i < st.size(); ++i)
-    for (int r = 0; r < st[i].ncols; ++r) sidx[i * 64 + r] = widx[st[i].p_begin + r];
-  CUDA_TRY(cudaMalloc(&h->d_stage_idx, std::max<size_t>(sidx.size(), 64) * sizeof(int32_t)), "cudaMalloc(stage_idx)");
-  if (!sidx.empty())
-    CUDA_TRY(cudaMemcpy(h->d_stage_idx, sidx.data(), sidx.size() * sizeof(int32_t), cudaMemcpyHostToDevice),
-             "upload stage_idx");
   h->stage_first.resize(st.size());
   for (size_t i = 0; i < st.size(); ++i) h->stage_first[i] = st[i].flags & spmm::kStageFirst;
   CUDA_TRY(cudaMalloc(&h->d_stages, std::max<size_t>(st.size(), 1) * sizeof(spmm::WcsrStage)), "cudaMalloc(stages)");
   if (!st.empty())
     CUDA_TRY(cudaMemcpy(h->d_stages, st.data(), st.size() * sizeof(spmm::WcsrStage), cudaMemcpyHostToDevice),
              "upload stages");
+  CUDA_TRY(cudaMalloc(&h->d_stage_vals, std::max<size_t>(svals.size(), 1024) * sizeof(uint16_t)), "cudaMalloc(stage_vals)");
+  if (!svals.empty())
+    CUDA_TRY(cudaMemcpy(h->d_stage_vals, svals.data(), svals.size() * sizeof(uint16_t), cudaMemcpyHostToDevice),
+             "upload stage_vals");
+  CUDA_TRY(cudaMalloc(&h->d_stage_idx, std::max<size_t>(sidx.size(), 64) * sizeof(int32_t)), "cudaMalloc(stage_idx)");
+  if (!sidx.empty())
+    CUDA_TRY(cudaMemcpy(h->d_stage_idx, sidx.data(), sidx.size() * sizeof(int32_t), cudaMemcpyHostToDevice),
+             "upload stage_idx");
   // Two partial slots per CTA, sized for the largest grid.
   h->ws_slots = 2 * static_cast<int64_t>(std::max(h->num_sms, 1));
   CUDA_TRY(cudaMalloc(&h->d_ws, h->ws_slots * spmm::kWcsrSlotFloats * sizeof(float)), "cudaMalloc(workspace)");
@@ -276,6 +309,7 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
   spmm::WcsrParams p;
   p.stages = h->d_stages;
   p.stage_idx = h->d_stage_idx;
+  p.stage_vals = h->d_stage_vals;
   p.values = h->d_vals;
   p.window_col_idx = h->d_idx;
   p.n_stages_dev = nullptr;
@@ -406,7 +440,7 @@ spmm_status spmm_wcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64
     st = encode_2d(&h->tm_vals, h->d_vals, in_t == SPMM_BF16, 16,
                    static_cast<uint64_t>(f.n_units > 0 ? f.n_units : 64),
                    static_cast<uint64_t>(f.n_units > 0 ? f.n_units : 64), 16, 64);
-  if (st == SPMM_OK) st = build_stages(h, f.ptr, f.idx);
+  if (st == SPMM_OK) st = build_stages(h, f.ptr, f.idx, f.vals);
   if (st != SPMM_OK) {
     free_handle(h);
     return st;

@@ -31,10 +31,10 @@
 //
 // 9 warps:
 //   warps 0..3  producers; warp w loads the work items w, w+4, ... of the
-//               CTA's range: the 16 x 64 value tile and the 64 B rows with
-//               16-byte cp.async (one B row, 512 B, per warp instruction at
-//               BN = 256; a strided TMA box of the value tile stalled the
-//               issuing warp behind slow HBM rows); every lane ends the item with
+//               CTA's range: the 64 B rows with 16-byte cp.async (one B row,
+//               512 B, per warp instruction at BN = 256) and, two of its items
+//               ahead, the item's 2 KB value tile with one TMA bulk copy into
+//               a separate ring; every lane ends the item with
 //               cp.async.mbarrier.arrive.noinc, so producers never block on
 //               their own copies and one warp's barrier handling overlaps
 //               another's copies
@@ -64,14 +64,20 @@ constexpr int kEpiWarps = 4;
 constexpr int kThreads = 32 * (kProducerWarps + 1 + kEpiWarps);
 constexpr int kAccBufs = 4;
 
+constexpr int kVQ = 16;        // value-tile ring slots
+constexpr int kVLead = 2;      // a producer loads value tiles this many of its own items ahead
+
 template <int NACC, int Q>
 struct Cfg {
   static constexpr int kBN = 128 * NACC;
   static constexpr int kChunks = 2 * NACC;
-  static constexpr int kStageBytes = kValBytes + kChunks * kChunkBytes;
+  static constexpr int kStageBytes = kChunks * kChunkBytes;  // gathered B rows only
   static constexpr int kAccCols = kH * NACC;                     // TMEM columns per accumulator buffer
   static constexpr int kTmemCols = kAccBufs * kAccCols <= 32 ? 32 : (kAccBufs * kAccCols <= 64 ? 64 : 128);
-  static constexpr int kSmemBytes = Q * kStageBytes + 2048 + 1024;
+  static constexpr int kSmemBytes = Q * kStageBytes + kVQ * kValBytes + 2048 + 1024;
+  // a value slot is reused by the item kVQ later; the producer fills it kVLead
+  // of its items (kVLead * 4 work items) ahead, so it only waits on older items
+  static_assert(kVQ > kVLead * kProducerWarps, "value slots must outlast the lead");
   static_assert(kAccBufs * kAccCols <= kTmemCols, "accumulator buffers exceed the TMEM allocation");
 };
 
@@ -120,9 +126,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C_ = Cfg<NACC, Q>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Q * C_::kStageBytes);
-  // bars: full[Q], empty[Q], acc_full[kAccBufs], acc_empty[kAccBufs], drain
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Q + 2 * kAccBufs + 1);
+  uint8_t *vring = smem + Q * C_::kStageBytes;  // kVQ value tiles, 2 KB each
+  uint64_t *bars = reinterpret_cast<uint64_t *>(vring + kVQ * kValBytes);
+  // bars: full[Q], empty[Q], acc_full[kAccBufs], acc_empty[kAccBufs], drain, vfull[kVQ], vempty[kVQ]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Q + 2 * kAccBufs + 1 + 2 * kVQ);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   StageRec *stage_rec = reinterpret_cast<StageRec *>(tmem_slot + 4);        // [Q]
   volatile SegRec *seg_rec = reinterpret_cast<volatile SegRec *>(stage_rec + Q);  // [kAccBufs]
@@ -149,6 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t accf0 = smem_addr(&bars[2 * Q]);
   const uint32_t acce0 = smem_addr(&bars[2 * Q + kAccBufs]);
   const uint32_t drain_bar = smem_addr(&bars[2 * Q + 2 * kAccBufs]);
+  const uint32_t vfull0 = smem_addr(&bars[2 * Q + 2 * kAccBufs + 1]);
+  const uint32_t vempty0 = vfull0 + 8 * kVQ;
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < Q; ++q) {
@@ -160,6 +169,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(acce0 + 8 * b, kEpiWarps);
     }
     mbar_init(drain_bar, 1);
+    for (int v = 0; v < kVQ; ++v) {
+      // TMA bulk copy (lane 0's expect_tx arrive), or cp.async arrivals of the
+      // loading warp's 32 lanes in the no-allocation variant
+      mbar_init(vfull0 + 8 * v, NOALLOC ? 32 : 1);
+      mbar_init(vempty0 + 8 * v, 1);  // the MMA commit
+    }
     *abort_flag = 0;
     fence_barrier_init();
     // partial-sum records of this CTA (overwritten below when used)
@@ -178,43 +193,97 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kProducerWarps) {
     // ------------------------------------------------------------ producers
     const uint16_t *Bp = reinterpret_cast<const uint16_t *>(p.B);
-    const uint16_t *Vp = reinterpret_cast<const uint16_t *>(p.values);
-    // Work items of this warp: f = f0 + warp + 4*i.  Item i's descriptor and
-    // column indices are loaded two items ahead into ring slot i % 2 (the
-    // loop is unrolled by 2, so slots are fixed registers).
-    int4 ring_d[2];
+    // Work items of this warp: f = f0 + warp + 4*i.  Descriptors are loaded
+    // four of the warp's items ahead and column indices two items ahead, into
+    // ring slots chosen by the (unrolled) item position, so a register is
+    // only read long after its load was issued.  The item's 2 KB value tile
+    // (stored per stage, already in the swizzled layout the MMA reads) is
+    // loaded kVLead items ahead into its own ring, so HBM latency of the
+    // values does not gate the gather pipeline.
+    const uint16_t *Vs = reinterpret_cast<const uint16_t *>(p.stage_vals);
+    constexpr int kStep = kProducerWarps;
+    int4 ring_d[4];
     int32_t ring_lo[2], ring_hi[2];
-    auto prefetch = [&](int slot_, int64_t fi) {
+    auto load_d = [&](int64_t fi) -> int4 { return fi < f1 ? stg[fi % n_stages] : make_int4(0, -1, 0, 0); };
+    auto load_idx = [&](int k, int64_t fi, const int4 &dd) {
       const bool in = fi < f1;
-      const int64_t sidx = in ? fi % n_stages : 0;
-      ring_d[slot_] = in ? stg[sidx] : make_int4(0, -1, 0, 0);
       if constexpr (NOALLOC) {
-        const int4 d = ring_d[slot_];
-        ring_lo[slot_] = lane < d.z ? p.window_col_idx[static_cast<int64_t>(d.x) + lane] : -2;
-        ring_hi[slot_] = lane + 32 < d.z ? p.window_col_idx[static_cast<int64_t>(d.x) + 32 + lane] : -2;
+        ring_lo[k] = lane < dd.z ? p.window_col_idx[static_cast<int64_t>(dd.x) + lane] : -2;
+        ring_hi[k] = lane + 32 < dd.z ? p.window_col_idx[static_cast<int64_t>(dd.x) + 32 + lane] : -2;
       } else {
-        ring_lo[slot_] = in ? p.stage_idx[sidx * kKC + lane] : -2;
-        ring_hi[slot_] = in ? p.stage_idx[sidx * kKC + 32 + lane] : -2;
+        const int64_t sidx = in ? fi % n_stages : 0;
+        ring_lo[k] = in ? p.stage_idx[sidx * kKC + lane] : -2;
+        ring_hi[k] = in ? p.stage_idx[sidx * kKC + 32 + lane] : -2;
       }
     };
-    int64_t f = f0 + warp;
-    prefetch(0, f);
-    prefetch(1, f + kProducerWarps);
-    bool ok = true;
-    for (; f < f1 && ok; f += 2 * kProducerWarps) {
+    // Value tile of item fi (relative index it) into slot it % kVQ.
+    auto load_vals = [&](int64_t fi, const int4 &dd) -> bool {
+      if (fi >= f1) return true;
+      const int64_t it = fi - f0;
+      const uint32_t slot = static_cast<uint32_t>(it % kVQ);
+      if (!mbar_wait_warp(vempty0 + 8 * slot, static_cast<uint32_t>(((it / kVQ) & 1) ^ 1), p.wait_limit_ns))
+        return false;
+      const uint32_t vdst = smem_addr(vring + slot * kValBytes);
+      if constexpr (!NOALLOC) {
+        // One 2 KB bulk copy on the TMA engine: the tile is already stored in
+        // the swizzled layout.  (Copied with cp.async it would delay every
+        // later cp.async arrive of the issuing lanes by its HBM latency.)
+        if (lane == 0) {
+          if (dd.z > 0) {
+            mbar_arrive_expect_tx(vfull0 + 8 * slot, kValBytes);
+            tma_bulk_load(vdst, Vs + (fi % n_stages) * (kValBytes / 2), kValBytes, vfull0 + 8 * slot);
+          } else {
+            mbar_arrive(vfull0 + 8 * slot);
+          }
+        }
+        return true;
+      }
+      if (dd.z > 0) {
+        if constexpr (NOALLOC) {
+          // from the row-major [16][P_total] values, swizzling here
+          const uint16_t *Vp = reinterpret_cast<const uint16_t *>(p.values);
+          const uint32_t u = static_cast<uint32_t>(lane & 7);
+          const int64_t pcol = static_cast<int64_t>(dd.x) + u * 8;
+          const bool in = pcol < p.P_total;
 #pragma unroll
-      for (int slot = 0; slot < 2; ++slot) {
-        const int64_t fi = f + slot * kProducerWarps;
-        if (fi >= f1) break;
-        const int4 d = ring_d[slot];
-        const int32_t lo = ring_lo[slot], hi = ring_hi[slot];
-        prefetch(slot, fi + 2 * kProducerWarps);
+          for (int q = 0; q < 4; ++q) {
+            const int r = (lane >> 3) + 4 * q;
+            cp_async_16(vdst + r * 128 + ((u ^ static_cast<uint32_t>(r & 7)) << 4),
+                        in ? static_cast<const void *>(Vp + r * p.P_total + pcol) : static_cast<const void *>(Vp),
+                        in ? 16u : 0u);
+          }
+        }
+      }
+      cp_async_arrive_noinc(vfull0 + 8 * slot);
+      return true;
+    };
+    int64_t f = f0 + warp;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ring_d[u] = load_d(f + u * kStep);
+    load_idx(0, f, ring_d[0]);
+    load_idx(1, f + kStep, ring_d[1]);
+    bool ok = true;
+    // value tiles of the first kVLead items of this warp
+#pragma unroll
+    for (int u = 0; u < kVLead; ++u) ok = ok && load_vals(f + u * kStep, ring_d[u]);
+    for (; f < f1 && ok; f += 4 * kStep) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t fi = f + u * kStep;
+        if (fi >= f1 || !ok) break;
+        const int4 d = ring_d[u];
+        const int32_t lo = ring_lo[u & 1], hi = ring_hi[u & 1];
+        // value tile kVLead items ahead (its descriptor was loaded 2 items ago)
+        ok = load_vals(fi + kVLead * kStep, ring_d[(u + kVLead) & 3]);
+        if (!ok) break;
+        load_idx(u & 1, fi + 2 * kStep, ring_d[(u + 2) & 3]);
+        ring_d[u] = load_d(fi + 4 * kStep);
 
         const int64_t it = fi - f0;
         const uint32_t stage = static_cast<uint32_t>(it % Q);
         const uint32_t phase = static_cast<uint32_t>((it / Q) & 1);
-        if (lane == 0) ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns) && !*abort_flag;
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+        ok = mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns);
+        ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
         if (!ok) break;
         const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
         const uint32_t fb = full0 + 8 * stage;
@@ -223,35 +292,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           stage_rec[stage] = StageRec{d.z, d.w, d.y, tile};  // released by this arrive
           mbar_arrive(fb);
         }
-        // The 16 x 64 value tile (rows P_total apart), K-major with the
-        // 128-byte swizzle: lane copies unit lane % 8 of rows lane / 8 + 4q.
-        if (d.z > 0) {
-          const uint32_t u = static_cast<uint32_t>(lane & 7);
-          const int64_t pcol = static_cast<int64_t>(d.x) + u * 8;
-          const bool in = pcol < p.P_total;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int r = (lane >> 3) + 4 * q;
-            cp_async_16(st + r * 128 + ((u ^ static_cast<uint32_t>(r & 7)) << 4),
-                        in ? static_cast<const void *>(Vp + r * p.P_total + pcol) : static_cast<const void *>(Vp),
-                        in ? 16u : 0u);
-          }
-        }
         const int n0 = tile * C_::kBN;
         if constexpr (NACC == 2) {
           // one B row (32 units of 16 B) per warp instruction
           const int n = n0 + lane * 8;
           const bool n_live = n < p.N;
-          const uint32_t dst_col = kValBytes + (lane >> 3) * kChunkBytes;
-          const uint32_t u = static_cast<uint32_t>(lane & 7);
-          for (int r = 0; r < d.z; ++r) {
-            const int32_t col = __shfl_sync(0xffffffffu, r < 32 ? lo : hi, r & 31);
-            // caller-supplied indices (no-allocation variant) are clamped to B's rows
-            const bool live = n_live && col >= 0 && (!NOALLOC || col < p.K);
-            cp_async_16(st + dst_col + r * 128 + ((u ^ static_cast<uint32_t>(r & 7)) << 4),
-                        live ? static_cast<const void *>(Bp + static_cast<int64_t>(col) * p.N + n)
-                             : static_cast<const void *>(Bp),
-                        live ? 16u : 0u);
+          const uint32_t dst_col = (lane >> 3) * kChunkBytes;
+          const uint32_t uu = static_cast<uint32_t>(lane & 7);
+          // 16 rows at a time (ncols is a multiple of 16): the shuffles of a
+          // group issue back to back instead of each waiting for the last
+          for (int r0 = 0; r0 < d.z; r0 += 16) {
+            const int32_t src = r0 < 32 ? lo : hi;
+            int32_t col[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) col[j] = __shfl_sync(0xffffffffu, src, (r0 + j) & 31);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int r = r0 + j;
+              // caller-supplied indices (no-allocation variant) are clamped to B's rows
+              const bool live = n_live && col[j] >= 0 && (!NOALLOC || col[j] < p.K);
+              cp_async_16(st + dst_col + r * 128 + ((uu ^ static_cast<uint32_t>(r & 7)) << 4),
+                          live ? static_cast<const void *>(Bp + static_cast<int64_t>(col[j]) * p.N + n)
+                               : static_cast<const void *>(Bp),
+                          live ? 16u : 0u);
+            }
           }
         } else {
           // two B rows (16 units each) per warp instruction
@@ -259,16 +323,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int half = lane >> 4;
           const int n = n0 + v * 8;
           const bool n_live = n < p.N;
-          const uint32_t dst_col = kValBytes + (v >> 3) * kChunkBytes;
-          const uint32_t u = static_cast<uint32_t>(v & 7);
-          for (int r2 = 0; r2 < d.z; r2 += 2) {
-            const int r = r2 + half;
-            const int32_t col = __shfl_sync(0xffffffffu, r2 < 32 ? lo : hi, r & 31);
-            const bool live = n_live && col >= 0 && (!NOALLOC || col < p.K);
-            cp_async_16(st + dst_col + r * 128 + ((u ^ static_cast<uint32_t>(r & 7)) << 4),
-                        live ? static_cast<const void *>(Bp + static_cast<int64_t>(col) * p.N + n)
-                             : static_cast<const void *>(Bp),
-                        live ? 16u : 0u);
+          const uint32_t dst_col = (v >> 3) * kChunkBytes;
+          const uint32_t uu = static_cast<uint32_t>(v & 7);
+          for (int r0 = 0; r0 < d.z; r0 += 16) {
+            const int32_t src = r0 < 32 ? lo : hi;
+            int32_t col[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) col[j] = __shfl_sync(0xffffffffu, src, (r0 + 2 * j + half) & 31);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int r = r0 + 2 * j + half;
+              const bool live = n_live && col[j] >= 0 && (!NOALLOC || col[j] < p.K);
+              cp_async_16(st + dst_col + r * 128 + ((uu ^ static_cast<uint32_t>(r & 7)) << 4),
+                          live ? static_cast<const void *>(Bp + static_cast<int64_t>(col[j]) * p.N + n)
+                               : static_cast<const void *>(Bp),
+                          live ? 16u : 0u);
+            }
           }
         }
         cp_async_arrive_noinc(fb);
@@ -281,8 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp takes the waits (see mbar_wait_warp); lane 0 issues.
+    {
       constexpr uint32_t idesc = idesc_f16(IN_BF16, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, kH);
+      const bool leader = lane == 0;
       uint32_t stage = 0, phase = 0;
       uint32_t seg = 0;     // window segments started
       uint32_t buf = 0;
@@ -291,15 +363,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool s_at_f0 = false;
       bool ok = true;
       auto open_buffer = [&](uint32_t b, uint32_t use) -> bool {
-        const bool r = mbar_wait(acce0 + 8 * b, (use & 1u) ^ 1u, p.wait_limit_ns) && !*abort_flag;
+        const bool r = mbar_wait_warp(acce0 + 8 * b, (use & 1u) ^ 1u, p.wait_limit_ns);
         tc_fence_after_sync();
-        return r;
+        return __shfl_sync(0xffffffffu, r && !*abort_flag, 0);
       };
       for (int64_t f = f0; f < f1 && ok; ++f) {
-        if (!mbar_wait(full0 + 8 * stage, phase, p.wait_limit_ns) || *abort_flag) {
-          ok = false;
-          break;
-        }
+        const uint32_t vslot = static_cast<uint32_t>((f - f0) % kVQ);
+        ok = mbar_wait_warp(full0 + 8 * stage, phase, p.wait_limit_ns) &&
+             mbar_wait_warp(vfull0 + 8 * vslot, static_cast<uint32_t>(((f - f0) / kVQ) & 1), p.wait_limit_ns);
+        ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
+        if (!ok) break;
         const StageRec rec = stage_rec[stage];
         const bool seg_first = f == f0 || (rec.flags & kStageFirst);
         const bool seg_last = f == f1 - 1 || (rec.flags & kStageLast);
@@ -313,37 +386,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           s_flags = rec.flags & kStageFirst;
           s_at_f0 = f == f0;
         }
-        fence_proxy_async_smem();  // the stage's cp.async writes -> async-proxy MMA reads
-        tc_fence_after_sync();
-        const uint32_t vals = smem_addr(smem + stage * C_::kStageBytes);  // MMA operand B (K-major)
-        const uint32_t gath = vals + kValBytes;                           // MMA operand A (MN-major)
-        const int nacc = min(NACC, (p.N - rec.tile * C_::kBN + 127) / 128);
         const int ksteps = rec.ncols / 16;
-        const uint32_t acc = tmem + buf * C_::kAccCols;
-        for (int kk = 0; kk < ksteps; ++kk) {
-          const uint64_t bdesc = smem_desc_sw128(vals + kk * 32, 16, 1024);
+        if (leader) {
+          fence_proxy_async_smem();  // the stage's cp.async writes -> async-proxy MMA reads
+          tc_fence_after_sync();
+          const uint32_t vals = smem_addr(vring + vslot * kValBytes);        // MMA operand B (K-major)
+          const uint32_t gath = smem_addr(smem + stage * C_::kStageBytes);  // MMA operand A (MN-major)
+          const int nacc = min(NACC, (p.N - rec.tile * C_::kBN + 127) / 128);
+          const uint32_t acc = tmem + buf * C_::kAccCols;
+          for (int kk = 0; kk < ksteps; ++kk) {
+            const uint64_t bdesc = smem_desc_sw128(vals + kk * 32, 16, 1024);
 #pragma unroll
-          for (int a = 0; a < NACC; ++a) {
-            if (a < nacc) {
-              const uint64_t adesc = smem_desc_sw128(gath + a * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
-              umma_f16(acc + a * kH, adesc, bdesc, idesc, ksteps_done > 0 ? 1u : 0u);
+            for (int a = 0; a < NACC; ++a) {
+              if (a < nacc) {
+                const uint64_t adesc = smem_desc_sw128(gath + a * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
+                umma_f16(acc + a * kH, adesc, bdesc, idesc, (ksteps_done + kk) > 0 ? 1u : 0u);
+              }
             }
           }
-          ++ksteps_done;
+          umma_commit(empty0 + 8 * stage);
+          umma_commit(vempty0 + 8 * vslot);
         }
-        umma_commit(empty0 + 8 * stage);
+        ksteps_done += ksteps;
         if (seg_last) {
           s_flags |= rec.flags & kStageLast;
-          volatile SegRec &sr = seg_rec[buf];
-          sr.window = rec.window;
-          sr.tile = rec.tile;
-          sr.flags = s_flags;
-          sr.zero = ksteps_done == 0;
-          sr.slot = 2 * static_cast<int32_t>(blockIdx.x) + (s_at_f0 ? 0 : 1);
-          mbar_arrive(accf0 + 8 * buf);  // releases the record
-          umma_commit(accf0 + 8 * buf);  // arrives when the MMAs are done
+          if (leader) {
+            volatile SegRec &sr = seg_rec[buf];
+            sr.window = rec.window;
+            sr.tile = rec.tile;
+            sr.flags = s_flags;
+            sr.zero = ksteps_done == 0;
+            sr.slot = 2 * static_cast<int32_t>(blockIdx.x) + (s_at_f0 ? 0 : 1);
+            mbar_arrive(accf0 + 8 * buf);  // releases the record
+            umma_commit(accf0 + 8 * buf);  // arrives when the MMAs are done
+          }
           ++seg;
         }
+        __syncwarp();
         if (++stage == Q) {
           stage = 0;
           phase ^= 1u;
@@ -353,17 +432,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // end marker for the epilogue
         buf = seg % kAccBufs;
         ok = open_buffer(buf, seg / kAccBufs);
-        if (ok) {
+        if (ok && leader) {
           seg_rec[buf].window = -1;
           mbar_arrive(accf0 + 8 * buf);
           mbar_arrive(accf0 + 8 * buf);
         }
       }
       if (!ok) {
-        atomicOr(p.status, kDevTimeout);
-        *abort_flag = 1;
-        umma_commit(drain_bar);
-        mbar_wait(drain_bar, 0, 1000000ull);
+        if (leader) {
+          atomicOr(p.status, kDevTimeout);
+          *abort_flag = 1;
+          umma_commit(drain_bar);
+        }
+        mbar_wait_warp(drain_bar, 0, 1000000ull);
       }
     }
     __syncwarp();
@@ -374,9 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t buf = seg % kAccBufs;
       const uint32_t use = seg / kAccBufs;
       bool ok = true;
-      if (lane == 0) ok = mbar_wait(accf0 + 8 * buf, use & 1u, p.wait_limit_ns) && !*abort_flag;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      __syncwarp();  // orders the other lanes' record reads after lane 0's acquiring wait
+      ok = mbar_wait_warp(accf0 + 8 * buf, use & 1u, p.wait_limit_ns);
+      ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
       if (!ok) {
         if (lane == 0) {
           atomicOr(p.status, kDevTimeout);
@@ -604,17 +684,17 @@ cudaError_t launch_wcsr_noalloc(WcsrParams p, const int64_t *window_row_ptr, int
     return out_bf16 ? launch_noalloc_variant<1, 10, false, true>(p, stream)
                     : launch_noalloc_variant<1, 10, false, false>(p, stream);
   }
-  if (in_bf16) return out_bf16 ? launch_noalloc_variant<2, 6, true, true>(p, stream)
-                               : launch_noalloc_variant<2, 6, true, false>(p, stream);
-  return out_bf16 ? launch_noalloc_variant<2, 6, false, true>(p, stream)
-                  : launch_noalloc_variant<2, 6, false, false>(p, stream);
+  if (in_bf16) return out_bf16 ? launch_noalloc_variant<2, 5, true, true>(p, stream)
+                               : launch_noalloc_variant<2, 5, true, false>(p, stream);
+  return out_bf16 ? launch_noalloc_variant<2, 5, false, true>(p, stream)
+                  : launch_noalloc_variant<2, 5, false, false>(p, stream);
 }
 
 cudaError_t launch_wcsr(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
                         cudaStream_t stream) {
   if (p.n_stages == 0 || p.N == 0 || p.grid == 0) return cudaSuccess;
   if (p.N <= 128) return launch_dtypes<1, 10>(tmV, p, in_bf16, out_bf16, stream);
-  return launch_dtypes<2, 6>(tmV, p, in_bf16, out_bf16, stream);
+  return launch_dtypes<2, 5>(tmV, p, in_bf16, out_bf16, stream);
 }
 
 }  // namespace spmm
