@@ -80,6 +80,23 @@ spmm_status encode_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t ro
   return SPMM_OK;
 }
 
+// C as the destination of TMA stores: `rows` x `cols` row-major elements of
+// bf16 or fp32, boxes of 64 rows x 32 columns, no swizzle.
+spmm_status encode_c(CUtensorMap *map, void *base, bool bf16, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(SPMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const uint64_t esz = bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * esz};
+  cuuint32_t box[2] = {32, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPMM_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", static_cast<int>(r));
+  return SPMM_OK;
+}
+
 }  // namespace
 
 struct spmm_handle_s {
@@ -101,6 +118,9 @@ struct spmm_handle_s {
   const void *b_cached = nullptr;
   int64_t n_cached = -1;
   CUtensorMap tm_B;
+  void *c_cached = nullptr;
+  int64_t nc_cached = -1;
+  CUtensorMap tm_C;
 
   // WCSR work decomposition: stages of <= 64 packed columns, and the
   // partial-sum workspace of windows cut between persistent CTAs
@@ -285,6 +305,12 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
       h->b_cached = B;
       h->n_cached = N;
     }
+    if (h->c_cached != C || h->nc_cached != N) {
+      spmm_status st = encode_c(&h->tm_C, C, out_bf16, static_cast<uint64_t>(h->m), static_cast<uint64_t>(N));
+      if (st != SPMM_OK) return st;
+      h->c_cached = C;
+      h->nc_cached = N;
+    }
     spmm::BcsrParams p;
     p.block_row_ptr = h->d_ptr;
     p.block_col_idx = h->d_idx;
@@ -299,7 +325,7 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
     p.max_ctas = std::max(h->max_ctas > 0 ? std::min(h->max_ctas, h->num_sms) : h->num_sms, 1);
     p.status = h->d_status;
     p.wait_limit_ns = h->wait_limit_ns;
-    cudaError_t e = spmm::launch_bcsr(h->tm_vals, h->tm_B, p, in_bf16, out_bf16, s);
+    cudaError_t e = spmm::launch_bcsr(h->tm_vals, h->tm_B, h->tm_C, p, in_bf16, out_bf16, s);
     if (e != cudaSuccess) return cuda_fail(e, "BCSR kernel launch");
     return SPMM_OK;
   }
