@@ -7,18 +7,23 @@
 // and empty[Q] barriers with phase bits, the first MMA overwriting the
 // accumulator), Section III-B (each 64x64 block and its 64 rows of B are
 // 2-D TMA loads).  On sm_103a the consumer is a single thread issuing
-// tcgen05.mma into TMEM, and the product is computed transposed:
-//   C^T[n, r] = sum_k B[k, n] * blk[r, k]
-// so the dense dimension N (128 columns per accumulator) is the MMA's M and
-// runs over the 128 TMEM lanes, and the 64 rows of a block row are the MMA's
-// N.  B tiles are MN-major MMA operands, blocks K-major ones.
+// tcgen05.mma into TMEM:
+//   C[r, n] += sum_k blk[r, k] * B[k, n]
+// with the block as the M = 64 operand (K-major) and the B tile as the
+// N <= 256 operand (MN-major).  On GB300 an M=128 x N=64 MMA costs as long
+// as an M=64 x N=128 one (about 97 cycles), while M=64 x N=256 takes 128
+// cycles for twice the work, so the block rows are the MMA's M and the dense
+// columns its N.  An M=64 accumulator occupies TMEM lanes 0-15 of each
+// 32-lane sub-partition (rows 16s..16s+15 in lanes 32s..32s+15), one column
+// per output column.
 //
-// Work unit ("tile") = one block row x one tile of BN = 128*NACC columns of
-// C.  The kernel is persistent: CTA c takes tiles c, c + G, c + 2G, ... (G =
-// grid size); see tile_coords for the order.  Two TMEM accumulators
-// alternate between tiles, so the epilogue of one tile overlaps the loads and
-// MMAs of the next (the paper's non-persistent grid cannot overlap them when
-// one CTA fills an SM).  6 warps:
+// Work unit ("tile") = one block row x BN columns of C.  The kernel is
+// persistent: CTA c takes tiles c, c + G, c + 2G, ... (G = grid size); see
+// tile_coords for the order.  Two TMEM accumulators alternate between tiles,
+// so the epilogue of one tile overlaps the loads and MMAs of the next (with a
+// single accumulator of 512 columns the tensor pipe drains at every tile
+// boundary and the kernel measured 13% slower on GB300 than with two of 256).
+// 6 warps:
 //   warp 0      producer: reads the block-row pointers and block-column
 //               indices, waits for a free stage, writes the stage's tile
 //               record to shared memory and issues its TMA loads (lane 0)
@@ -27,8 +32,9 @@
 //               global load, and hands each finished accumulator to the
 //               epilogue with a record of its own
 //   warps 2..5  epilogue: TMEM -> registers -> a per-warp staging area in
-//               shared memory -> one TMA store per 32-column box (warp w reads
-//               the TMEM lanes of sub-partition w % 4, i.e. 32 columns of C)
+//               shared memory -> TMA stores of 16-row boxes (warp w reads the
+//               TMEM lanes of sub-partition w % 4, i.e. rows 16(w%4) ..
+//               16(w%4)+15 of the block row)
 // A block row without stored blocks still passes through the pipeline as
 // one stage without loads, so its rows of C are written (zeros) by the same
 // TMA stores.
@@ -49,7 +55,8 @@ constexpr int kMmaWarp = 1;
 constexpr int kEpiWarp0 = 2;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int kBoxCols = 32;                  // C columns of one TMA store box (one epilogue warp)
+constexpr int kBoxRows = 16;                  // C rows of one TMA store box (one epilogue warp)
+constexpr int kBoxBytes = kBoxRows * 128;     // 16 rows of 128 bytes, 128-byte swizzle
 
 // Stage record flags (producer -> MMA) and accumulator record flags (MMA -> epilogue).
 constexpr int32_t kRecFirst = 1;  // first stored block of its tile
@@ -64,21 +71,31 @@ struct TileRec {
   int32_t pad_;
 };
 
-template <int NACC, int Q, bool OUT_BF16>
+template <int BN, int Q, bool OUT_BF16>
 struct Cfg {
-  static constexpr int kBN = 128 * NACC;
-  static constexpr int kChunks = 2 * NACC;
+  static constexpr int kBN = BN;
+  static constexpr int kNmma = BN < 256 ? BN : 256;           // N of one MMA
+  static constexpr int kMmas = BN / kNmma;                    // MMAs per 16-deep k step
+  static constexpr int kChunks = BN / 64;                     // 64-column chunks of the B tile
   static constexpr int kStageBytes = kBlkBytes + kChunks * kChunkBytes;
-  static constexpr int kAccCols = 64 * NACC;               // TMEM columns of one accumulator set
-  static constexpr int kTmemCols = NACC == 1 ? 128 : 256;  // two sets
+  static constexpr int kTmemCols = 2 * BN;                    // two accumulators of BN columns
   static constexpr int kOutBytes = OUT_BF16 ? 2 : 4;
-  static constexpr int kBoxBytes = kBoxCols * kBlk * kOutBytes;   // 64 rows x 32 columns of C
-  static constexpr int kWarpStaging = NACC * kBoxBytes;           // one box per accumulator
+  static constexpr int kBoxCols = 128 / kOutBytes;            // C columns of one store box
+  // The epilogue writes a tile out in two parts through two staging buffers,
+  // so the TMA stores of one part overlap the TMEM reads of the next.
+  static constexpr int kPartCols = BN / 2;
+  static constexpr int kPartGroups = kPartCols / 16;          // 16-column TMEM loads per part
+  static constexpr int kBatches = kPartGroups / 4;            // batches of four loads per part
+  static constexpr int kPartBoxes = kPartCols / kBoxCols;     // store boxes per part
+  static constexpr int kPartBytes = kPartBoxes * kBoxBytes;
+  static constexpr int kWarpStaging = 2 * kPartBytes;
   static constexpr int kStagingBytes = kEpiWarps * kWarpStaging;
-  static constexpr int kMiscBytes = 1024;                         // barriers, records, TMEM address
+  static constexpr int kMiscBytes = 1024;                     // barriers, records, TMEM address
   static constexpr int kSmemBytes = Q * kStageBytes + kStagingBytes + kMiscBytes + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert((2 * Q + 6) * 8 + (Q + 2) * 16 + 16 <= kMiscBytes, "barrier area");
+  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
+  static_assert(BN % 128 == 0 && kNmma % 16 == 0 && kPartBoxes >= 1, "tile shape");
 };
 
 // Tile t -> (block row, column tile).  Consecutive tile ids walk kGroupN
@@ -94,11 +111,11 @@ __device__ __forceinline__ void tile_coords(int64_t t, int n_block_rows, int n_c
   nt = static_cast<int>(g) * kGroupN + static_cast<int>(r % gsz);
 }
 
-template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
+template <int BN, int Q, bool IN_BF16, bool OUT_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const BcsrParams p) {
-  using C_ = Cfg<NACC, Q, OUT_BF16>;
+  using C_ = Cfg<BN, Q, OUT_BF16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *staging = smem + Q * C_::kStageBytes;
@@ -238,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp takes the waits (see mbar_wait_warp); lane 0 issues.
-    constexpr uint32_t idesc = idesc_f16(IN_BF16, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, 64);
+    constexpr uint32_t idesc = idesc_f16(IN_BF16, /*a_mn_major=*/false, /*b_mn_major=*/true, 64, C_::kNmma);
     const bool leader = lane == 0;
     uint32_t stage = 0, phase = 0;
     uint32_t tcount = 0;  // tiles finished
@@ -250,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const TileRec rec = tile_rec[stage];
       if (rec.flags & (kRecFirst | kRecEnd)) {
-        // Wait until the epilogue has drained this accumulator set.
+        // Wait until the epilogue has drained this accumulator.
         buf = tcount & 1u;
         const bool r = mbar_wait_warp(acce0 + 8 * buf, ((tcount >> 1) & 1u) ^ 1u, p.wait_limit_ns);
         ok = __shfl_sync(0xffffffffu, r && !*abort_flag, 0);
@@ -268,19 +285,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (leader) {
         if (!(rec.flags & kRecEmpty)) {
           tc_fence_after_sync();
-          const int nacc = min(NACC, (p.N - rec.nt * C_::kBN + 127) / 128);
-          const uint32_t a_blk = smem_addr(smem + stage * C_::kStageBytes);  // A block: MMA operand B
-          const uint32_t b_til = a_blk + kBlkBytes;                          // B tile:  MMA operand A
-          const uint32_t acc = tmem + buf * C_::kAccCols;
+          const int nmma = min(C_::kMmas, (p.N - rec.nt * BN + C_::kNmma - 1) / C_::kNmma);
+          const uint32_t a_blk = smem_addr(smem + stage * C_::kStageBytes);  // block: MMA operand A (K-major)
+          const uint32_t b_til = a_blk + kBlkBytes;                          // B tile: MMA operand B (MN-major)
+          const uint32_t acc = tmem + buf * BN;
           const bool first = (rec.flags & kRecFirst) != 0;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(a_blk + kk * 32, 16, 1024);
+            const uint64_t adesc = smem_desc_sw128(a_blk + kk * 32, 16, 1024);
 #pragma unroll
-            for (int a = 0; a < NACC; ++a) {
-              if (a < nacc) {
-                const uint64_t adesc = smem_desc_sw128(b_til + a * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
-                umma_f16(acc + a * 64, adesc, bdesc, idesc, (first && kk == 0) ? 0u : 1u);
+            for (int m = 0; m < C_::kMmas; ++m) {
+              if (m < nmma) {
+                const uint64_t bdesc = smem_desc_sw128(b_til + m * (C_::kNmma / 64) * kChunkBytes + kk * 2048,
+                                                       kChunkBytes, 1024);
+                umma_f16(acc + m * C_::kNmma, adesc, bdesc, idesc, (first && kk == 0) ? 0u : 1u);
               }
             }
           }
@@ -318,9 +336,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int sp = warp & 3;  // TMEM sub-partition this warp may read: C columns sp*32 .. sp*32+31 of each 128
+    // Lane t < 16 of warp w holds row 16*(w%4) + t of the block row.  Its
+    // 16-column pieces go to the warp's staging area as 16-row x 128-byte
+    // boxes in the 128-byte swizzled layout the TMA store reads.  Each batch
+    // of four TMEM loads is issued before the previous batch is written to
+    // shared memory, so the load latency overlaps that work.
+    const int sp = warp & 3;
     uint8_t *stg = staging + (warp - kEpiWarp0) * C_::kWarpStaging;
     const uint32_t stg_addr = smem_addr(stg);
+    const uint32_t row_sw = static_cast<uint32_t>(lane & 7);
     uint32_t tcount = 0;
     while (true) {
       const uint32_t buf = tcount & 1u;
@@ -334,51 +358,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int32_t flags = acc_rec[buf].flags;
       if (flags & kRecEnd) break;
-      const int br = acc_rec[buf].br;
-      const int n0 = acc_rec[buf].nt * C_::kBN;
-      const int nacc = min(NACC, (p.N - n0 + 127) / 128);
+      const bool zero = (flags & kRecEmpty) != 0;
+      const int row0 = acc_rec[buf].br * kBlk + sp * kBoxRows;
+      const int n0 = acc_rec[buf].nt * BN;
+      const int ncg = min(BN / 16, (p.N - n0 + 15) / 16);  // 16-column groups holding columns of C
       tc_fence_after_sync();
-      // the staging area is free once this warp's previous stores have read it
-      if (lane == 0) bulk_wait_group_read0();
-      __syncwarp();
-      const uint32_t acc = tmem + buf * C_::kAccCols + (static_cast<uint32_t>(sp * 32) << 16);
-      for (int a = 0; a < nacc; ++a) {
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(sp * 32) << 16) + buf * BN;
+      // four 16-column groups starting at group g0 -> registers
+      auto load_batch = [&](int g0, uint32_t (&v)[4][16]) {
 #pragma unroll
-        for (int cb = 0; cb < kBlk / 16; ++cb) {
-          uint32_t v[16];
-          if (!(flags & kRecEmpty)) {
-            tmem_ld_32x32b_x16(acc + a * 64 + cb * 16, v);
-            tmem_ld_wait();
+        for (int g = 0; g < 4; ++g) {
+          if (g0 + g < ncg && !zero) {
+            tmem_ld_32x32b_x16(tbase + (g0 + g) * 16, v[g]);
           } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0u;
+            for (int i = 0; i < 16; ++i) v[g][i] = 0u;
           }
-          // row r of this warp's box: 32 consecutive columns, one per lane
+        }
+      };
+      // registers -> staging part `pst` (gl0: first group of the part)
+      auto store_batch = [&](uint8_t *pst, int g0, int gl0, const uint32_t (&v)[4][16]) {
+        if (lane < kBoxRows) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int r = cb * 16 + i;
-            if constexpr (OUT_BF16)
-              reinterpret_cast<__nv_bfloat16 *>(stg + a * C_::kBoxBytes)[r * kBoxCols + lane] =
-                  __float2bfloat16_rn(__uint_as_float(v[i]));
-            else
-              reinterpret_cast<float *>(stg + a * C_::kBoxBytes)[r * kBoxCols + lane] = __uint_as_float(v[i]);
+          for (int g = 0; g < 4; ++g) {
+            const int col = (g0 + g - gl0) * 16;  // column within the part
+            uint8_t *row_base = pst + (col / C_::kBoxCols) * kBoxBytes + lane * 128;
+            const uint32_t u0 = static_cast<uint32_t>((col % C_::kBoxCols) * C_::kOutBytes / 16);
+            if constexpr (OUT_BF16) {
+              uint32_t w[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const __nv_bfloat162 h =
+                    __floats2bfloat162_rn(__uint_as_float(v[g][2 * i]), __uint_as_float(v[g][2 * i + 1]));
+                w[i] = *reinterpret_cast<const uint32_t *>(&h);
+              }
+              *reinterpret_cast<uint4 *>(row_base + (((u0 + 0) ^ row_sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+              *reinterpret_cast<uint4 *>(row_base + (((u0 + 1) ^ row_sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4 *>(row_base + (((u0 + q) ^ row_sw) << 4)) =
+                    make_uint4(v[g][4 * q], v[g][4 * q + 1], v[g][4 * q + 2], v[g][4 * q + 3]);
+            }
           }
         }
-      }
-      // This warp's reads of the accumulator set are complete.
-      tc_fence_before_sync();
-      fence_proxy_async_smem();  // the staging writes -> the TMA engine's reads
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(acce0 + 8 * buf);
-        for (int a = 0; a < nacc; ++a) {
-          const int x = n0 + a * 128 + sp * 32;
-          if (x < p.N) tma_store_2d(&tmC, stg_addr + a * C_::kBoxBytes, x, br * kBlk);
+      };
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        const int gl0 = part * C_::kPartGroups;
+        uint8_t *pst = stg + part * C_::kPartBytes;
+        // this part's staging buffer is free once at most one store group
+        // (the other part's) is still reading shared memory
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        uint32_t va[4][16], vb[4][16];
+        load_batch(gl0, va);
+#pragma unroll
+        for (int b = 0; b < C_::kBatches; b += 2) {
+          tmem_ld_wait();
+          if (b + 1 < C_::kBatches) load_batch(gl0 + (b + 1) * 4, vb);
+          store_batch(pst, gl0 + b * 4, gl0, va);
+          if (b + 1 < C_::kBatches) {
+            tmem_ld_wait();
+            if (b + 2 < C_::kBatches) load_batch(gl0 + (b + 2) * 4, va);
+            store_batch(pst, gl0 + (b + 1) * 4, gl0, vb);
+          }
         }
-        bulk_commit_group();
+        if (part == 1) tc_fence_before_sync();  // this warp's reads of the accumulator are complete
+        fence_proxy_async_smem();               // the staging writes -> the TMA engine's reads
+        __syncwarp();
+        if (lane == 0) {
+          if (part == 1) mbar_arrive(acce0 + 8 * buf);
+          if (row0 < p.M) {
+            for (int b = 0; b < C_::kPartBoxes; ++b) {
+              const int x = n0 + part * C_::kPartCols + b * C_::kBoxCols;
+              if (x < p.N) tma_store_2d(&tmC, smem_addr(pst) + b * kBoxBytes, x, row0);
+            }
+          }
+          bulk_commit_group();
+        }
       }
       ++tcount;
     }
+    (void)stg_addr;
     if (lane == 0) bulk_wait_group0();
   }
 
@@ -390,31 +452,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
+template <int BN, int Q, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_variant(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                            const BcsrParams &p, cudaStream_t stream) {
-  using C_ = Cfg<NACC, Q, OUT_BF16>;
-  auto kern = bcsr_spmm_kernel<NACC, Q, IN_BF16, OUT_BF16>;
+  using C_ = Cfg<BN, Q, OUT_BF16>;
+  auto kern = bcsr_spmm_kernel<BN, Q, IN_BF16, OUT_BF16>;
   static bool attr_set = false;  // per instantiation; the attribute is per device function
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int64_t tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + C_::kBN - 1) / C_::kBN);
+  const int64_t tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + BN - 1) / BN);
   const int64_t grid = tiles < p.max_ctas ? tiles : p.max_ctas;
   kern<<<static_cast<unsigned>(grid), kThreads, C_::kSmemBytes, stream>>>(tmA, tmB, tmC, p);
   return cudaGetLastError();
 }
 
-template <int NACC, int Q>
+template <int BN, int Q>
 cudaError_t launch_dtypes(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                           const BcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t s) {
   if (in_bf16)
-    return out_bf16 ? launch_variant<NACC, Q, true, true>(tmA, tmB, tmC, p, s)
-                    : launch_variant<NACC, Q, true, false>(tmA, tmB, tmC, p, s);
-  return out_bf16 ? launch_variant<NACC, Q, false, true>(tmA, tmB, tmC, p, s)
-                  : launch_variant<NACC, Q, false, false>(tmA, tmB, tmC, p, s);
+    return out_bf16 ? launch_variant<BN, Q, true, true>(tmA, tmB, tmC, p, s)
+                    : launch_variant<BN, Q, true, false>(tmA, tmB, tmC, p, s);
+  return out_bf16 ? launch_variant<BN, Q, false, true>(tmA, tmB, tmC, p, s)
+                  : launch_variant<BN, Q, false, false>(tmA, tmB, tmC, p, s);
 }
 
 }  // namespace
@@ -422,10 +484,10 @@ cudaError_t launch_dtypes(const CUtensorMap &tmA, const CUtensorMap &tmB, const 
 cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const BcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream) {
   if (p.n_block_rows == 0 || p.N == 0) return cudaSuccess;
-  // Tile width: 128 columns when N is small, else 256 (two accumulators
-  // sharing each loaded block).
-  if (p.N <= 128) return launch_dtypes<1, 6>(tmA, tmB, tmC, p, in_bf16, out_bf16, stream);
-  return launch_dtypes<2, 4>(tmA, tmB, tmC, p, in_bf16, out_bf16, stream);
+  // Tile width: 128 columns (one MMA of N = 128 per k step) when N is small,
+  // else 256 (one MMA of N = 256).
+  if (p.N <= 128) return launch_dtypes<128, 6>(tmA, tmB, tmC, p, in_bf16, out_bf16, stream);
+  return launch_dtypes<256, 4>(tmA, tmB, tmC, p, in_bf16, out_bf16, stream);
 }
 
 }  // namespace spmm

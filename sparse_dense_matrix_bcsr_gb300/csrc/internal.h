@@ -25,7 +25,7 @@ struct BcsrParams {
 // in_bf16: A/B are bf16 (else fp16); out_bf16: C is bf16 (else fp32).
 // tmA covers the blocks array as [n_blocks*64 rows, 64 cols], tmB covers B as
 // [K rows, N cols]; both with 64 x 64 boxes and 128-byte swizzle.  tmC covers
-// C as [M rows, N cols] with boxes of 64 rows x 32 columns, no swizzle.
+// C as [M rows, N cols] with boxes of 16 rows x 128 bytes and 128-byte swizzle.
 cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const BcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream);
 

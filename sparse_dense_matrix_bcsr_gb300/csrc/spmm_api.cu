@@ -81,17 +81,18 @@ spmm_status encode_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t ro
 }
 
 // C as the destination of TMA stores: `rows` x `cols` row-major elements of
-// bf16 or fp32, boxes of 64 rows x 32 columns, no swizzle.
+// bf16 or fp32, boxes of 16 rows x 128 bytes (64 bf16 or 32 fp32 columns)
+// with the 128-byte swizzle.
 spmm_status encode_c(CUtensorMap *map, void *base, bool bf16, uint64_t rows, uint64_t cols) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(SPMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const uint64_t esz = bf16 ? 2 : 4;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * esz};
-  cuuint32_t box[2] = {32, 64};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), 16};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SPMM_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", static_cast<int>(r));
   return SPMM_OK;
