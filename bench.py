@@ -18,7 +18,8 @@ collective on the data path); the reported time is the max over ranks.
 
 --impl reference times the CPU oracle (fp64, OpenMP) on the host cores on a
 bounded sample of the same workload per step.
---sweep prints one line per benchmark configuration (not the driver line).
+--sweep prints one line per benchmark configuration (not the driver line);
+--sweep bcsr_weight:8192 runs one configuration at another dense width N.
 """
 from __future__ import annotations
 
@@ -399,15 +400,22 @@ def run_sweep(args):
     sptr = stream.cuda_stream
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
     cfgs = []
-    sel = args.sweep.split(",") if args.sweep not in ("all", "") else None
-    builders = [("bcsr_tiny", lambda: [W.bcsr_tiny()]), ("wcsr_uniform", lambda: [W.wcsr_uniform()]),
-                ("wcsr_irregular", lambda: [W.wcsr_irregular()]), ("bcsr_weight", lambda: [W.bcsr_weight()]),
-                ("bcsr_sweep", lambda: [W.bcsr_sweep(s, n) for s in W.BCSR_SWEEP_SPARSITY for n in W.SWEEP_N]),
-                ("wcsr_sweep", lambda: [W.wcsr_sweep(d, n) for d in W.WCSR_SWEEP_DENSITY for n in W.SWEEP_N])]
+    # entries: a configuration name, optionally ":N" to change the dense width
+    # of a single-workload configuration (e.g. a smaller case for a profiler)
+    sel = {}
+    for e in (args.sweep.split(",") if args.sweep not in ("all", "") else []):
+        name, _, n = e.partition(":")
+        sel[name] = int(n) if n else None
+    builders = [("bcsr_tiny", lambda n: [W.bcsr_tiny()]),
+                ("wcsr_uniform", lambda n: [W.wcsr_uniform(n=n) if n else W.wcsr_uniform()]),
+                ("wcsr_irregular", lambda n: [W.wcsr_irregular(n=n) if n else W.wcsr_irregular()]),
+                ("bcsr_weight", lambda n: [W.bcsr_weight(n=n) if n else W.bcsr_weight()]),
+                ("bcsr_sweep", lambda n: [W.bcsr_sweep(s, k) for s in W.BCSR_SWEEP_SPARSITY for k in W.SWEEP_N]),
+                ("wcsr_sweep", lambda n: [W.wcsr_sweep(d, k) for d in W.WCSR_SWEEP_DENSITY for k in W.SWEEP_N])]
     for name, b in builders:
         if sel and name not in sel:
             continue
-        cfgs.append((name, b))
+        cfgs.append((name, lambda b=b, n=sel.get(name): b(n)))
     for name, b in cfgs:
         cache = {}
         for w in b():

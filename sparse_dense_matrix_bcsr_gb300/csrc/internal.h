@@ -50,12 +50,19 @@ struct WcsrPartial {
   int32_t pad_;
 };
 
+// One stage as a record of kWcsrPackBytes in device memory, fetched by one
+// TMA bulk copy: the 16 x 64 value tile in the MMA's swizzled K-major layout
+// (zero past ncols), the 64 column indices (-1 for a padding position, -2
+// past ncols) and the descriptor {ncols, flags, window, 0}.
+constexpr int kWcsrPackValOff = 0;
+constexpr int kWcsrPackIdxOff = 2048;
+constexpr int kWcsrPackDescOff = 2048 + 256;
+constexpr int kWcsrPackBytes = 2048 + 256 + 16;
+
 struct WcsrParams {
-  const WcsrStage *stages;       // device, n_stages
-  const int32_t *stage_idx;      // device, n_stages x 64: stage s's column indices, -2 past its ncols
+  const WcsrStage *stages;       // device, n_stages (the no-allocation variant's stage list)
+  const void *stage_pack;        // device, n_stages x kWcsrPackBytes (the allocating entry points)
   const void *values;            // device, 16 x P_total row-major (read by the no-allocation variant)
-  const void *stage_vals;        // device, n_stages x 2 KB: stage s's 16 x 64 value tile in the MMA's
-                                 // swizzled K-major layout (zero past its ncols)
   const int32_t *window_col_idx; // device, P_total (read by the no-allocation variant only)
   const int64_t *n_stages_dev;   // device stage count (no-allocation variant only)
   const void *B;                 // device, K x N row-major

@@ -127,9 +127,7 @@ struct spmm_handle_s {
   // partial-sum workspace of windows cut between persistent CTAs
   int32_t max_ctas = 0;  // 0: one CTA per SM
   int64_t n_stages = 0;
-  spmm::WcsrStage *d_stages = nullptr;
-  int32_t *d_stage_idx = nullptr;
-  uint16_t *d_stage_vals = nullptr;
+  uint8_t *d_stage_pack = nullptr;
   float *d_ws = nullptr;
   spmm::WcsrPartial *d_partials = nullptr;
   int64_t ws_slots = 0;
@@ -169,9 +167,7 @@ void free_handle(spmm_handle h) {
   cudaFree(h->d_ptr);
   cudaFree(h->d_idx);
   cudaFree(h->d_vals);
-  cudaFree(h->d_stages);
-  cudaFree(h->d_stage_idx);
-  cudaFree(h->d_stage_vals);
+  cudaFree(h->d_stage_pack);
   cudaFree(h->d_partials);
   cudaFree(h->d_ws);
   cudaFree(h->d_status);
@@ -205,8 +201,8 @@ spmm_status upload_common(spmm_handle h, const HostFormat &f) {
 
 // The WCSR stage list: each window cut into stages of at most 64 packed
 // columns, in window order; a window without columns gets one empty stage.
-// The kernel reads each stage's column indices and 16 x 64 value tile from
-// per-stage copies (stage_idx, stage_vals).  In those copies a window of
+// The kernel reads each stage as one record (its 16 x 64 value tile, column
+// indices and descriptor; see kWcsrPackBytes).  In those records a window of
 // ns >= 2 stages deals its padded column list round-robin over its stages
 // (stage j takes positions j, j + ns, j + 2 ns, ...; positions past P_w are
 // padding), so each stage's rows of B span the whole window: packed columns
@@ -216,37 +212,46 @@ spmm_status upload_common(spmm_handle h, const HostFormat &f) {
 spmm_status build_stages(spmm_handle h, const std::vector<int64_t> &wptr, const std::vector<int32_t> &widx,
                          const std::vector<uint16_t> &wvals) {
   std::vector<spmm::WcsrStage> st;
-  std::vector<int32_t> sidx;
-  std::vector<uint16_t> svals;
+  std::vector<uint8_t> pack;
   const int64_t nw = h->n_groups;
   const int64_t P = h->n_units;
-  auto put_val = [&](size_t stage, int r, int c, uint16_t v) {
+  // stage s's record at s * kWcsrPackBytes
+  auto new_stage = [&](int32_t p_begin, int32_t window, int32_t ncols, int32_t flags) -> size_t {
+    const size_t s = st.size();
+    st.push_back({p_begin, window, ncols, flags});
+    pack.resize(pack.size() + spmm::kWcsrPackBytes, 0);
+    int32_t *idx = reinterpret_cast<int32_t *>(&pack[s * spmm::kWcsrPackBytes + spmm::kWcsrPackIdxOff]);
+    for (int c = 0; c < 64; ++c) idx[c] = -2;
+    const int32_t desc[4] = {ncols, flags, window, 0};
+    std::memcpy(&pack[s * spmm::kWcsrPackBytes + spmm::kWcsrPackDescOff], desc, sizeof desc);
+    return s;
+  };
+  auto put_val = [&](size_t s, int r, int c, uint16_t v) {
     // row r at r * 128 bytes, 16-byte unit u stored at unit u ^ (r % 8)
-    svals[stage * 1024 + r * 64 + (((c >> 3) ^ (r & 7)) << 3) + (c & 7)] = v;
+    uint16_t *tile = reinterpret_cast<uint16_t *>(&pack[s * spmm::kWcsrPackBytes + spmm::kWcsrPackValOff]);
+    tile[r * 64 + (((c >> 3) ^ (r & 7)) << 3) + (c & 7)] = v;
+  };
+  auto put_idx = [&](size_t s, int c, int32_t col) {
+    std::memcpy(&pack[s * spmm::kWcsrPackBytes + spmm::kWcsrPackIdxOff + 4 * c], &col, 4);
   };
   for (int64_t w = 0; w < nw; ++w) {
     const int64_t b = wptr[w], e = wptr[w + 1], pw = e - b;
     if (pw == 0) {
-      st.push_back({static_cast<int32_t>(b), static_cast<int32_t>(w), 0, spmm::kStageFirst | spmm::kStageLast});
-      sidx.resize(sidx.size() + 64, -2);
-      svals.resize(svals.size() + 1024, 0);
+      new_stage(static_cast<int32_t>(b), static_cast<int32_t>(w), 0, spmm::kStageFirst | spmm::kStageLast);
       continue;
     }
     const int64_t ns = (pw + 63) / 64;
     for (int64_t j = 0; j < ns; ++j) {
-      const size_t s = st.size();
       const int32_t flags = (j == 0 ? spmm::kStageFirst : 0) | (j == ns - 1 ? spmm::kStageLast : 0);
       const int32_t ncols = ns == 1 ? static_cast<int32_t>(pw) : 64;
-      st.push_back({static_cast<int32_t>(b + 64 * j), static_cast<int32_t>(w), ncols, flags});
-      sidx.resize(sidx.size() + 64, -2);
-      svals.resize(svals.size() + 1024, 0);
+      const size_t s = new_stage(static_cast<int32_t>(b + 64 * j), static_cast<int32_t>(w), ncols, flags);
       for (int c = 0; c < ncols; ++c) {
         const int64_t q = ns == 1 ? c : j + ns * c;  // position within the window
         if (q >= pw) {
-          sidx[s * 64 + c] = -1;  // padding: zero values, no B row
+          put_idx(s, c, -1);  // padding: zero values, no B row
           continue;
         }
-        sidx[s * 64 + c] = widx[b + q];
+        put_idx(s, c, widx[b + q]);
         for (int r = 0; r < 16; ++r) put_val(s, r, c, wvals[r * P + b + q]);
       }
     }
@@ -254,18 +259,9 @@ spmm_status build_stages(spmm_handle h, const std::vector<int64_t> &wptr, const 
   h->n_stages = static_cast<int64_t>(st.size());
   h->stage_first.resize(st.size());
   for (size_t i = 0; i < st.size(); ++i) h->stage_first[i] = st[i].flags & spmm::kStageFirst;
-  CUDA_TRY(cudaMalloc(&h->d_stages, std::max<size_t>(st.size(), 1) * sizeof(spmm::WcsrStage)), "cudaMalloc(stages)");
-  if (!st.empty())
-    CUDA_TRY(cudaMemcpy(h->d_stages, st.data(), st.size() * sizeof(spmm::WcsrStage), cudaMemcpyHostToDevice),
-             "upload stages");
-  CUDA_TRY(cudaMalloc(&h->d_stage_vals, std::max<size_t>(svals.size(), 1024) * sizeof(uint16_t)), "cudaMalloc(stage_vals)");
-  if (!svals.empty())
-    CUDA_TRY(cudaMemcpy(h->d_stage_vals, svals.data(), svals.size() * sizeof(uint16_t), cudaMemcpyHostToDevice),
-             "upload stage_vals");
-  CUDA_TRY(cudaMalloc(&h->d_stage_idx, std::max<size_t>(sidx.size(), 64) * sizeof(int32_t)), "cudaMalloc(stage_idx)");
-  if (!sidx.empty())
-    CUDA_TRY(cudaMemcpy(h->d_stage_idx, sidx.data(), sidx.size() * sizeof(int32_t), cudaMemcpyHostToDevice),
-             "upload stage_idx");
+  CUDA_TRY(cudaMalloc(&h->d_stage_pack, std::max<size_t>(pack.size(), spmm::kWcsrPackBytes)), "cudaMalloc(stage records)");
+  if (!pack.empty())
+    CUDA_TRY(cudaMemcpy(h->d_stage_pack, pack.data(), pack.size(), cudaMemcpyHostToDevice), "upload stage records");
   // Two partial slots per CTA, sized for the largest grid.
   h->ws_slots = 2 * static_cast<int64_t>(std::max(h->num_sms, 1));
   CUDA_TRY(cudaMalloc(&h->d_ws, h->ws_slots * spmm::kWcsrSlotFloats * sizeof(float)), "cudaMalloc(workspace)");
@@ -334,9 +330,8 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
   if (h->b_row != 16 || h->b_col % 16 != 0)
     return fail(SPMM_ERR_UNSUPPORTED, "the WCSR kernel takes window height 16 and column padding a multiple of 16");
   spmm::WcsrParams p;
-  p.stages = h->d_stages;
-  p.stage_idx = h->d_stage_idx;
-  p.stage_vals = h->d_stage_vals;
+  p.stages = nullptr;
+  p.stage_pack = h->d_stage_pack;
   p.values = h->d_vals;
   p.window_col_idx = h->d_idx;
   p.n_stages_dev = nullptr;

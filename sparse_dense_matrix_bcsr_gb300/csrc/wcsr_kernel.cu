@@ -57,6 +57,7 @@ namespace {
 constexpr int kH = 16;                       // window height
 constexpr int kKC = 64;                      // packed columns per stage
 constexpr int kValBytes = kH * kKC * 2;      // 2 KB value tile per stage
+constexpr int kMetaBytes = kWcsrPackBytes - kWcsrPackIdxOff;  // a stage record's indices + descriptor
 constexpr int kChunkBytes = kKC * 64 * 2;    // 64 gathered rows x 64 columns
 constexpr int kProducerWarps = 4;
 constexpr int kMmaWarp = kProducerWarps;
@@ -64,8 +65,8 @@ constexpr int kEpiWarps = 4;
 constexpr int kThreads = 32 * (kProducerWarps + 1 + kEpiWarps);
 constexpr int kAccBufs = 4;
 
-constexpr int kVQ = 16;        // value-tile ring slots
-constexpr int kVLead = 2;      // a producer loads value tiles this many of its own items ahead
+constexpr int kVLead = 2;      // a producer fetches stage records (value tiles) this many of its own items ahead
+constexpr int kLead = kVLead * kProducerWarps;  // = this many work items ahead
 
 template <int NACC, int Q>
 struct Cfg {
@@ -74,9 +75,15 @@ struct Cfg {
   static constexpr int kStageBytes = kChunks * kChunkBytes;  // gathered B rows only
   static constexpr int kAccCols = kH * NACC;                     // TMEM columns per accumulator buffer
   static constexpr int kTmemCols = kAccBufs * kAccCols <= 32 ? 32 : (kAccBufs * kAccCols <= 64 ? 64 : 128);
-  static constexpr int kSmemBytes = Q * kStageBytes + kVQ * kValBytes + 2048 + 1024;
-  // a value slot is reused by the item kVQ later; the producer fills it kVLead
-  // of its items (kVLead * 4 work items) ahead, so it only waits on older items
+  // Record ring slots.  The record of item i + kLead is fetched by the warp
+  // that has just seen the MMAs of item i - Q complete, into the slot that
+  // item i + kLead - kVQ = i - Q last used, so no other release is needed.
+  static constexpr int kVQ = Q + kLead;
+  static constexpr int kMetaRing = (kVQ * kMetaBytes + 1023) / 1024 * 1024;
+  static constexpr int kSmemBytes = Q * kStageBytes + kVQ * kValBytes + kMetaRing + 2048 + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  // no-allocation variant: a value slot is reused by the item kVQ later and a
+  // producer fills it kVLead of its items (kVLead * 4 work items) ahead
   static_assert(kVQ > kVLead * kProducerWarps, "value slots must outlast the lead");
   static_assert(kAccBufs * kAccCols <= kTmemCols, "accumulator buffers exceed the TMEM allocation");
 };
@@ -92,12 +99,6 @@ __device__ __forceinline__ void store_out(void *C, int64_t off, float v) {
 __device__ __forceinline__ int4 shfl_int4(const int4 &v, int src) {
   return make_int4(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src),
                    __shfl_sync(0xffffffffu, v.z, src), __shfl_sync(0xffffffffu, v.w, src));
-}
-
-// Descriptor of work item f (stage f % n_stages of column tile f / n_stages),
-// or an empty item past the CTA's range.
-__device__ __forceinline__ int4 load_item(const int4 *stg, int64_t f, int64_t f1, int64_t n_stages) {
-  return f < f1 ? stg[f % n_stages] : make_int4(0, -1, 0, 0);
 }
 
 // Shared-memory records passed between roles.
@@ -126,8 +127,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C_ = Cfg<NACC, Q>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *vring = smem + Q * C_::kStageBytes;  // kVQ value tiles, 2 KB each
-  uint64_t *bars = reinterpret_cast<uint64_t *>(vring + kVQ * kValBytes);
+  constexpr int kVQ = C_::kVQ;
+  uint8_t *vring = smem + Q * C_::kStageBytes;  // kVQ value tiles of 2 KB
+  uint8_t *mring = vring + kVQ * kValBytes;     // kVQ index + descriptor records of kMetaBytes
+  uint64_t *bars = reinterpret_cast<uint64_t *>(mring + C_::kMetaRing);
   // bars: full[Q], empty[Q], acc_full[kAccBufs], acc_empty[kAccBufs], drain, vfull[kVQ], vempty[kVQ]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Q + 2 * kAccBufs + 1 + 2 * kVQ);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -149,7 +152,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int64_t f0 = total * blockIdx.x / grid;
   const int64_t f1 = total * (blockIdx.x + 1) / grid;
-  const int4 *stg = reinterpret_cast<const int4 *>(p.stages);
 
   const uint32_t full0 = smem_addr(&bars[0]);
   const uint32_t empty0 = smem_addr(&bars[Q]);
@@ -193,54 +195,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kProducerWarps) {
     // ------------------------------------------------------------ producers
     const uint16_t *Bp = reinterpret_cast<const uint16_t *>(p.B);
-    // Work items of this warp: f = f0 + warp + 4*i.  Descriptors are loaded
-    // four of the warp's items ahead and column indices two items ahead, into
-    // ring slots chosen by the (unrolled) item position, so a register is
-    // only read long after its load was issued.  The item's 2 KB value tile
-    // (stored per stage, already in the swizzled layout the MMA reads) is
-    // loaded kVLead items ahead into its own ring, so HBM latency of the
-    // values does not gate the gather pipeline.
-    const uint16_t *Vs = reinterpret_cast<const uint16_t *>(p.stage_vals);
     constexpr int kStep = kProducerWarps;
-    int4 ring_d[4];
-    int32_t ring_lo[2], ring_hi[2];
-    auto load_d = [&](int64_t fi) -> int4 { return fi < f1 ? stg[fi % n_stages] : make_int4(0, -1, 0, 0); };
-    auto load_idx = [&](int k, int64_t fi, const int4 &dd) {
-      const bool in = fi < f1;
-      if constexpr (NOALLOC) {
-        ring_lo[k] = lane < dd.z ? p.window_col_idx[static_cast<int64_t>(dd.x) + lane] : -2;
-        ring_hi[k] = lane + 32 < dd.z ? p.window_col_idx[static_cast<int64_t>(dd.x) + 32 + lane] : -2;
-      } else {
-        const int64_t sidx = in ? fi % n_stages : 0;
-        ring_lo[k] = in ? p.stage_idx[sidx * kKC + lane] : -2;
-        ring_hi[k] = in ? p.stage_idx[sidx * kKC + 32 + lane] : -2;
-      }
-    };
-    // Value tile of item fi (relative index it) into slot it % kVQ.
-    auto load_vals = [&](int64_t fi, const int4 &dd) -> bool {
-      if (fi >= f1) return true;
-      const int64_t it = fi - f0;
-      const uint32_t slot = static_cast<uint32_t>(it % kVQ);
-      if (!mbar_wait_warp(vempty0 + 8 * slot, static_cast<uint32_t>(((it / kVQ) & 1) ^ 1), p.wait_limit_ns))
-        return false;
-      const uint32_t vdst = smem_addr(vring + slot * kValBytes);
-      if constexpr (!NOALLOC) {
-        // One 2 KB bulk copy on the TMA engine: the tile is already stored in
-        // the swizzled layout.  (Copied with cp.async it would delay every
-        // later cp.async arrive of the issuing lanes by its HBM latency.)
-        if (lane == 0) {
-          if (dd.z > 0) {
-            mbar_arrive_expect_tx(vfull0 + 8 * slot, kValBytes);
-            tma_bulk_load(vdst, Vs + (fi % n_stages) * (kValBytes / 2), kValBytes, vfull0 + 8 * slot);
-          } else {
-            mbar_arrive(vfull0 + 8 * slot);
+    // The B rows of one work item -> stage `st` with 16-byte cp.async
+    // (zero-fill for padding positions and columns past N); lo / hi hold the
+    // item's column indices for positions lane and 32 + lane.
+    auto gather = [&](uint32_t st, int n0, int ncols, int32_t lo, int32_t hi) {
+      if constexpr (NACC == 2) {
+        // one B row (32 units of 16 B) per warp instruction
+        const int n = n0 + lane * 8;
+        const bool n_live = n < p.N;
+        const uint32_t dst_col = (lane >> 3) * kChunkBytes;
+        const uint32_t uu = static_cast<uint32_t>(lane & 7);
+        // 16 rows at a time (ncols is a multiple of 16): the shuffles of a
+        // group issue back to back instead of each waiting for the last
+        for (int r0 = 0; r0 < ncols; r0 += 16) {
+          const int32_t src = r0 < 32 ? lo : hi;
+          int32_t col[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) col[j] = __shfl_sync(0xffffffffu, src, (r0 + j) & 31);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int r = r0 + j;
+            // caller-supplied indices (no-allocation variant) are clamped to B's rows
+            const bool live = n_live && col[j] >= 0 && (!NOALLOC || col[j] < p.K);
+            cp_async_16(st + dst_col + r * 128 + ((uu ^ static_cast<uint32_t>(r & 7)) << 4),
+                        live ? static_cast<const void *>(Bp + static_cast<int64_t>(col[j]) * p.N + n)
+                             : static_cast<const void *>(Bp),
+                        live ? 16u : 0u);
           }
         }
-        return true;
+      } else {
+        // two B rows (16 units each) per warp instruction
+        const int v = lane & 15;
+        const int half = lane >> 4;
+        const int n = n0 + v * 8;
+        const bool n_live = n < p.N;
+        const uint32_t dst_col = (v >> 3) * kChunkBytes;
+        const uint32_t uu = static_cast<uint32_t>(v & 7);
+        for (int r0 = 0; r0 < ncols; r0 += 16) {
+          const int32_t src = r0 < 32 ? lo : hi;
+          int32_t col[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) col[j] = __shfl_sync(0xffffffffu, src, (r0 + 2 * j + half) & 31);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int r = r0 + 2 * j + half;
+            const bool live = n_live && col[j] >= 0 && (!NOALLOC || col[j] < p.K);
+            cp_async_16(st + dst_col + r * 128 + ((uu ^ static_cast<uint32_t>(r & 7)) << 4),
+                        live ? static_cast<const void *>(Bp + static_cast<int64_t>(col[j]) * p.N + n)
+                             : static_cast<const void *>(Bp),
+                        live ? 16u : 0u);
+          }
+        }
       }
-      if (dd.z > 0) {
-        if constexpr (NOALLOC) {
-          // from the row-major [16][P_total] values, swizzling here
+    };
+    if constexpr (NOALLOC) {
+      // Caller-owned arrays: the stage list built on the device, the column
+      // indices read at each stage's first packed column, and the values
+      // copied from the row-major [16][P_total] array (swizzled here).
+      // Work items of this warp: f = f0 + warp + 4*i.  Descriptors are
+      // loaded four of the warp's items ahead and column indices two items
+      // ahead, into ring slots chosen by the (unrolled) item position, so a
+      // register is only read long after its load was issued.
+      const int4 *stg = reinterpret_cast<const int4 *>(p.stages);
+      int4 ring_d[4];
+      int32_t ring_lo[2], ring_hi[2];
+      auto load_d = [&](int64_t fi) -> int4 { return fi < f1 ? stg[fi % n_stages] : make_int4(0, -1, 0, 0); };
+      auto load_idx = [&](int k, const int4 &dd) {
+        ring_lo[k] = lane < dd.z ? p.window_col_idx[static_cast<int64_t>(dd.x) + lane] : -2;
+        ring_hi[k] = lane + 32 < dd.z ? p.window_col_idx[static_cast<int64_t>(dd.x) + 32 + lane] : -2;
+      };
+      // value tile of item fi into slot (fi - f0) % kVQ, with the cp.async
+      // arrivals of this warp's 32 lanes
+      auto load_vals = [&](int64_t fi, const int4 &dd) -> bool {
+        if (fi >= f1) return true;
+        const int64_t it = fi - f0;
+        const uint32_t slot = static_cast<uint32_t>(it % kVQ);
+        if (!mbar_wait_warp(vempty0 + 8 * slot, static_cast<uint32_t>(((it / kVQ) & 1) ^ 1), p.wait_limit_ns))
+          return false;
+        const uint32_t vdst = smem_addr(vring + slot * kValBytes);
+        if (dd.z > 0) {
           const uint16_t *Vp = reinterpret_cast<const uint16_t *>(p.values);
           const uint32_t u = static_cast<uint32_t>(lane & 7);
           const int64_t pcol = static_cast<int64_t>(dd.x) + u * 8;
@@ -253,101 +287,119 @@ __global__ void __launch_bounds__(kThreads, 1)
                         in ? 16u : 0u);
           }
         }
+        cp_async_arrive_noinc(vfull0 + 8 * slot);
+        return true;
+      };
+      int64_t f = f0 + warp;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) ring_d[u] = load_d(f + u * kStep);
+      load_idx(0, ring_d[0]);
+      load_idx(1, ring_d[1]);
+      bool ok = true;
+#pragma unroll
+      for (int u = 0; u < kVLead; ++u) ok = ok && load_vals(f + u * kStep, ring_d[u]);
+      for (; f < f1 && ok; f += 4 * kStep) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t fi = f + u * kStep;
+          if (fi >= f1 || !ok) break;
+          const int4 d = ring_d[u];
+          const int32_t lo = ring_lo[u & 1], hi = ring_hi[u & 1];
+          ok = load_vals(fi + kVLead * kStep, ring_d[(u + kVLead) & 3]);
+          if (!ok) break;
+          load_idx(u & 1, ring_d[(u + 2) & 3]);
+          ring_d[u] = load_d(fi + 4 * kStep);
+          const int64_t it = fi - f0;
+          const uint32_t stage = static_cast<uint32_t>(it % Q);
+          const uint32_t phase = static_cast<uint32_t>((it / Q) & 1);
+          ok = mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns);
+          ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
+          if (!ok) break;
+          const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
+          const uint32_t fb = full0 + 8 * stage;
+          const int tile = static_cast<int>(fi / n_stages);
+          if (lane == 0) {
+            stage_rec[stage] = StageRec{d.z, d.w, d.y, tile};  // released by this arrive
+            mbar_arrive(fb);
+          }
+          gather(st, tile * C_::kBN, d.z, lo, hi);
+          cp_async_arrive_noinc(fb);
+        }
       }
-      cp_async_arrive_noinc(vfull0 + 8 * slot);
-      return true;
-    };
-    int64_t f = f0 + warp;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) ring_d[u] = load_d(f + u * kStep);
-    load_idx(0, f, ring_d[0]);
-    load_idx(1, f + kStep, ring_d[1]);
-    bool ok = true;
-    // value tiles of the first kVLead items of this warp
-#pragma unroll
-    for (int u = 0; u < kVLead; ++u) ok = ok && load_vals(f + u * kStep, ring_d[u]);
-    for (; f < f1 && ok; f += 4 * kStep) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int64_t fi = f + u * kStep;
-        if (fi >= f1 || !ok) break;
-        const int4 d = ring_d[u];
-        const int32_t lo = ring_lo[u & 1], hi = ring_hi[u & 1];
-        // value tile kVLead items ahead (its descriptor was loaded 2 items ago)
-        ok = load_vals(fi + kVLead * kStep, ring_d[(u + kVLead) & 3]);
-        if (!ok) break;
-        load_idx(u & 1, fi + 2 * kStep, ring_d[(u + 2) & 3]);
-        ring_d[u] = load_d(fi + 4 * kStep);
-
-        const int64_t it = fi - f0;
+      cp_async_wait<0>();
+      if (!ok && lane == 0) {
+        atomicOr(p.status, kDevTimeout);
+        *abort_flag = 1;
+      }
+    } else {
+      // Every stage is one record in global memory (its value tile, its 64
+      // column indices and its descriptor).  Warp w owns the work items
+      // f0 + w, f0 + w + 4, ...: it fetches an item's record with two TMA
+      // bulk copies (value ring, index ring) kVLead of its items ahead, then
+      // reads the indices and the descriptor from shared memory, so no
+      // global load stalls its issue behind the SM's outstanding gathers,
+      // and copies the item's B rows.  Four warps keep four items' barrier
+      // handling and copy issue in flight at once.
+      const uint8_t *pack = reinterpret_cast<const uint8_t *>(p.stage_pack);
+      int64_t f = f0 + warp;
+      // stage-list position of the item whose record this warp fetches next
+      int64_t fl = f;
+      int64_t s_lead = f % n_stages;
+      auto advance_pos = [&](int64_t &s) {
+        s += kStep;
+        while (s >= n_stages) s -= n_stages;
+      };
+      auto load_pack = [&]() {
+        if (fl < f1 && lane == 0) {
+          const uint32_t slot = static_cast<uint32_t>((fl - f0) % kVQ);
+          const uint8_t *src = pack + s_lead * kWcsrPackBytes;
+          mbar_arrive_expect_tx(vfull0 + 8 * slot, kWcsrPackBytes);
+          tma_bulk_load(smem_addr(vring + slot * kValBytes), src + kWcsrPackValOff, kValBytes, vfull0 + 8 * slot);
+          tma_bulk_load(smem_addr(mring + slot * kMetaBytes), src + kWcsrPackIdxOff, kMetaBytes, vfull0 + 8 * slot);
+        }
+        fl += kStep;
+        advance_pos(s_lead);
+      };
+#pragma unroll 1
+      for (int u = 0; u < kVLead; ++u) load_pack();
+      int64_t s_cur = f % n_stages;
+      int tile = static_cast<int>(f / n_stages);
+      bool ok = true;
+      for (; f < f1; f += kStep) {
+        const int64_t it = f - f0;
         const uint32_t stage = static_cast<uint32_t>(it % Q);
         const uint32_t phase = static_cast<uint32_t>((it / Q) & 1);
+        // the stage is free once the MMAs of item it - Q are complete
         ok = mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns);
         ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
         if (!ok) break;
-        const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
+        load_pack();  // record of item it + kLead, into the slot of item it - Q
+        const uint32_t vslot = static_cast<uint32_t>(it % kVQ);
+        ok = mbar_wait_warp(vfull0 + 8 * vslot, static_cast<uint32_t>((it / kVQ) & 1), p.wait_limit_ns);
+        ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
+        if (!ok) break;
+        const uint8_t *meta = mring + vslot * kMetaBytes;
+        const int4 d = *reinterpret_cast<const int4 *>(meta + (kWcsrPackDescOff - kWcsrPackIdxOff));
+        const int32_t lo = reinterpret_cast<const int32_t *>(meta)[lane];
+        const int32_t hi = reinterpret_cast<const int32_t *>(meta)[32 + lane];
         const uint32_t fb = full0 + 8 * stage;
-        const int tile = static_cast<int>(fi / n_stages);
         if (lane == 0) {
-          stage_rec[stage] = StageRec{d.z, d.w, d.y, tile};  // released by this arrive
+          stage_rec[stage] = StageRec{d.x, d.y, d.z, tile};  // released by this arrive
           mbar_arrive(fb);
         }
-        const int n0 = tile * C_::kBN;
-        if constexpr (NACC == 2) {
-          // one B row (32 units of 16 B) per warp instruction
-          const int n = n0 + lane * 8;
-          const bool n_live = n < p.N;
-          const uint32_t dst_col = (lane >> 3) * kChunkBytes;
-          const uint32_t uu = static_cast<uint32_t>(lane & 7);
-          // 16 rows at a time (ncols is a multiple of 16): the shuffles of a
-          // group issue back to back instead of each waiting for the last
-          for (int r0 = 0; r0 < d.z; r0 += 16) {
-            const int32_t src = r0 < 32 ? lo : hi;
-            int32_t col[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) col[j] = __shfl_sync(0xffffffffu, src, (r0 + j) & 31);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int r = r0 + j;
-              // caller-supplied indices (no-allocation variant) are clamped to B's rows
-              const bool live = n_live && col[j] >= 0 && (!NOALLOC || col[j] < p.K);
-              cp_async_16(st + dst_col + r * 128 + ((uu ^ static_cast<uint32_t>(r & 7)) << 4),
-                          live ? static_cast<const void *>(Bp + static_cast<int64_t>(col[j]) * p.N + n)
-                               : static_cast<const void *>(Bp),
-                          live ? 16u : 0u);
-            }
-          }
-        } else {
-          // two B rows (16 units each) per warp instruction
-          const int v = lane & 15;
-          const int half = lane >> 4;
-          const int n = n0 + v * 8;
-          const bool n_live = n < p.N;
-          const uint32_t dst_col = (v >> 3) * kChunkBytes;
-          const uint32_t uu = static_cast<uint32_t>(v & 7);
-          for (int r0 = 0; r0 < d.z; r0 += 16) {
-            const int32_t src = r0 < 32 ? lo : hi;
-            int32_t col[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) col[j] = __shfl_sync(0xffffffffu, src, (r0 + 2 * j + half) & 31);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int r = r0 + 2 * j + half;
-              const bool live = n_live && col[j] >= 0 && (!NOALLOC || col[j] < p.K);
-              cp_async_16(st + dst_col + r * 128 + ((uu ^ static_cast<uint32_t>(r & 7)) << 4),
-                          live ? static_cast<const void *>(Bp + static_cast<int64_t>(col[j]) * p.N + n)
-                               : static_cast<const void *>(Bp),
-                          live ? 16u : 0u);
-            }
-          }
-        }
+        gather(smem_addr(smem + stage * C_::kStageBytes), tile * C_::kBN, d.x, lo, hi);
         cp_async_arrive_noinc(fb);
+        s_cur += kStep;
+        while (s_cur >= n_stages) {
+          s_cur -= n_stages;
+          ++tile;
+        }
       }
-    }
-    cp_async_wait<0>();
-    if (!ok && lane == 0) {
-      atomicOr(p.status, kDevTimeout);
-      *abort_flag = 1;
+      cp_async_wait<0>();
+      if (!ok && lane == 0) {
+        atomicOr(p.status, kDevTimeout);
+        *abort_flag = 1;
+      }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -405,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           umma_commit(empty0 + 8 * stage);
-          umma_commit(vempty0 + 8 * vslot);
+          if constexpr (NOALLOC) umma_commit(vempty0 + 8 * vslot);
         }
         ksteps_done += ksteps;
         if (seg_last) {
@@ -693,8 +745,8 @@ cudaError_t launch_wcsr_noalloc(WcsrParams p, const int64_t *window_row_ptr, int
 cudaError_t launch_wcsr(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
                         cudaStream_t stream) {
   if (p.n_stages == 0 || p.N == 0 || p.grid == 0) return cudaSuccess;
-  if (p.N <= 128) return launch_dtypes<1, 10>(tmV, p, in_bf16, out_bf16, stream);
-  return launch_dtypes<2, 5>(tmV, p, in_bf16, out_bf16, stream);
+  if (p.N <= 128) return launch_dtypes<1, 11>(tmV, p, in_bf16, out_bf16, stream);
+  return launch_dtypes<2, 6>(tmV, p, in_bf16, out_bf16, stream);
 }
 
 }  // namespace spmm
