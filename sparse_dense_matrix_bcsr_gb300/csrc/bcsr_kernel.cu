@@ -71,31 +71,34 @@ struct TileRec {
   int32_t pad_;
 };
 
-template <int BN, int Q, bool OUT_BF16>
+// BN columns per tile, Q pipeline stages, NBUF TMEM accumulators, the
+// epilogue writing a tile in PARTS column parts through two alternating
+// staging buffers, MINB CTAs per SM.
+template <int BN, int Q, int NBUF, int PARTS, int MINB, bool OUT_BF16>
 struct Cfg {
   static constexpr int kBN = BN;
   static constexpr int kNmma = BN < 256 ? BN : 256;           // N of one MMA
   static constexpr int kMmas = BN / kNmma;                    // MMAs per 16-deep k step
   static constexpr int kChunks = BN / 64;                     // 64-column chunks of the B tile
   static constexpr int kStageBytes = kBlkBytes + kChunks * kChunkBytes;
-  static constexpr int kTmemCols = 2 * BN;                    // two accumulators of BN columns
+  static constexpr int kTmemCols = NBUF * BN;                 // NBUF accumulators of BN columns
   static constexpr int kOutBytes = OUT_BF16 ? 2 : 4;
   static constexpr int kBoxCols = 128 / kOutBytes;            // C columns of one store box
-  // The epilogue writes a tile out in two parts through two staging buffers,
-  // so the TMA stores of one part overlap the TMEM reads of the next.
-  static constexpr int kPartCols = BN / 2;
+  static constexpr int kPartCols = BN / PARTS;
   static constexpr int kPartGroups = kPartCols / 16;          // 16-column TMEM loads per part
-  static constexpr int kBatches = kPartGroups / 4;            // batches of four loads per part
+  static constexpr int kBatch = kPartGroups < 4 ? kPartGroups : 4;  // TMEM loads per wait
+  static constexpr int kBatches = kPartGroups / kBatch;
   static constexpr int kPartBoxes = kPartCols / kBoxCols;     // store boxes per part
   static constexpr int kPartBytes = kPartBoxes * kBoxBytes;
   static constexpr int kWarpStaging = 2 * kPartBytes;
   static constexpr int kStagingBytes = kEpiWarps * kWarpStaging;
   static constexpr int kMiscBytes = 1024;                     // barriers, records, TMEM address
   static constexpr int kSmemBytes = Q * kStageBytes + kStagingBytes + kMiscBytes + 1024;  // + alignment slack
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static_assert(kSmemBytes <= 227 * 1024 && MINB * (kSmemBytes + 1024) <= 228 * 1024, "shared memory");
+  static_assert(MINB * kTmemCols <= 512 && (kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512), "TMEM");
   static_assert((2 * Q + 6) * 8 + (Q + 2) * 16 + 16 <= kMiscBytes, "barrier area");
-  static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocation");
-  static_assert(BN % 128 == 0 && kNmma % 16 == 0 && kPartBoxes >= 1, "tile shape");
+  static_assert(BN % 128 == 0 && kNmma % 16 == 0 && kPartBoxes >= 1 && PARTS % 2 == 0 &&
+                    kPartGroups % kBatch == 0, "tile shape");
 };
 
 // Tile t -> (block row, column tile).  Consecutive tile ids walk kGroupN
@@ -111,11 +114,11 @@ __device__ __forceinline__ void tile_coords(int64_t t, int n_block_rows, int n_c
   nt = static_cast<int>(g) * kGroupN + static_cast<int>(r % gsz);
 }
 
-template <int BN, int Q, bool IN_BF16, bool OUT_BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, int Q, int NBUF, int PARTS, int MINB, bool IN_BF16, bool OUT_BF16>
+__global__ void __launch_bounds__(kThreads, MINB)
     bcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const BcsrParams p) {
-  using C_ = Cfg<BN, Q, OUT_BF16>;
+  using C_ = Cfg<BN, Q, NBUF, PARTS, MINB, OUT_BF16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *staging = smem + Q * C_::kStageBytes;
@@ -142,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(full0 + 8 * q, 1);   // the producer's arrive (with the TMA transaction bytes)
       mbar_init(empty0 + 8 * q, 1);  // the MMA commit
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NBUF; ++b) {
       mbar_init(accf0 + 8 * b, 2);  // the MMA thread's arrive (record) + its commit (MMAs done)
       mbar_init(acce0 + 8 * b, kEpiWarps);
     }
@@ -268,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileRec rec = tile_rec[stage];
       if (rec.flags & (kRecFirst | kRecEnd)) {
         // Wait until the epilogue has drained this accumulator.
-        buf = tcount & 1u;
-        const bool r = mbar_wait_warp(acce0 + 8 * buf, ((tcount >> 1) & 1u) ^ 1u, p.wait_limit_ns);
+        buf = tcount % NBUF;
+        const bool r = mbar_wait_warp(acce0 + 8 * buf, ((tcount / NBUF) & 1u) ^ 1u, p.wait_limit_ns);
         ok = __shfl_sync(0xffffffffu, r && !*abort_flag, 0);
         if (!ok) break;
         tc_fence_after_sync();
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_warp(drain_bar, 0, 1000000ull);
       if (leader) {
         // let the epilogue see the abort flag without waiting out its limit
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NBUF; ++b) {
           mbar_arrive(accf0 + 8 * b);
           mbar_arrive(accf0 + 8 * b);
         }
@@ -347,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t row_sw = static_cast<uint32_t>(lane & 7);
     uint32_t tcount = 0;
     while (true) {
-      const uint32_t buf = tcount & 1u;
-      const bool r = mbar_wait_warp(accf0 + 8 * buf, (tcount >> 1) & 1u, p.wait_limit_ns);
+      const uint32_t buf = tcount % NBUF;
+      const bool r = mbar_wait_warp(accf0 + 8 * buf, (tcount / NBUF) & 1u, p.wait_limit_ns);
       if (!__shfl_sync(0xffffffffu, r && !*abort_flag, 0)) {
         if (lane == 0 && !r) {
           atomicOr(p.status, kDevTimeout);
@@ -364,10 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ncg = min(BN / 16, (p.N - n0 + 15) / 16);  // 16-column groups holding columns of C
       tc_fence_after_sync();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(sp * 32) << 16) + buf * BN;
-      // four 16-column groups starting at group g0 -> registers
-      auto load_batch = [&](int g0, uint32_t (&v)[4][16]) {
+      // kBatch 16-column groups starting at group g0 -> registers
+      auto load_batch = [&](int g0, uint32_t (&v)[C_::kBatch][16]) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
+        for (int g = 0; g < C_::kBatch; ++g) {
           if (g0 + g < ncg && !zero) {
             tmem_ld_32x32b_x16(tbase + (g0 + g) * 16, v[g]);
           } else {
@@ -377,10 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       // registers -> staging part `pst` (gl0: first group of the part)
-      auto store_batch = [&](uint8_t *pst, int g0, int gl0, const uint32_t (&v)[4][16]) {
+      auto store_batch = [&](uint8_t *pst, int g0, int gl0, const uint32_t (&v)[C_::kBatch][16]) {
         if (lane < kBoxRows) {
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
+          for (int g = 0; g < C_::kBatch; ++g) {
             const int col = (g0 + g - gl0) * 16;  // column within the part
             uint8_t *row_base = pst + (col / C_::kBoxCols) * kBoxBytes + lane * 128;
             const uint32_t u0 = static_cast<uint32_t>((col % C_::kBoxCols) * C_::kOutBytes / 16);
@@ -404,31 +407,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
+      for (int part = 0; part < PARTS; ++part) {
         const int gl0 = part * C_::kPartGroups;
-        uint8_t *pst = stg + part * C_::kPartBytes;
+        uint8_t *pst = stg + (part & 1) * C_::kPartBytes;
         // this part's staging buffer is free once at most one store group
         // (the other part's) is still reading shared memory
         if (lane == 0) bulk_wait_group_read<1>();
         __syncwarp();
-        uint32_t va[4][16], vb[4][16];
+        uint32_t va[C_::kBatch][16], vb[C_::kBatch][16];
+        constexpr int kB = C_::kBatch;
         load_batch(gl0, va);
 #pragma unroll
         for (int b = 0; b < C_::kBatches; b += 2) {
           tmem_ld_wait();
-          if (b + 1 < C_::kBatches) load_batch(gl0 + (b + 1) * 4, vb);
-          store_batch(pst, gl0 + b * 4, gl0, va);
+          if (b + 1 < C_::kBatches) load_batch(gl0 + (b + 1) * kB, vb);
+          store_batch(pst, gl0 + b * kB, gl0, va);
           if (b + 1 < C_::kBatches) {
             tmem_ld_wait();
-            if (b + 2 < C_::kBatches) load_batch(gl0 + (b + 2) * 4, va);
-            store_batch(pst, gl0 + (b + 1) * 4, gl0, vb);
+            if (b + 2 < C_::kBatches) load_batch(gl0 + (b + 2) * kB, va);
+            store_batch(pst, gl0 + (b + 1) * kB, gl0, vb);
           }
         }
-        if (part == 1) tc_fence_before_sync();  // this warp's reads of the accumulator are complete
+        if (part == PARTS - 1) tc_fence_before_sync();  // this warp's reads of the accumulator are complete
         fence_proxy_async_smem();               // the staging writes -> the TMA engine's reads
         __syncwarp();
         if (lane == 0) {
-          if (part == 1) mbar_arrive(acce0 + 8 * buf);
+          if (part == PARTS - 1) mbar_arrive(acce0 + 8 * buf);
           if (row0 < p.M) {
             for (int b = 0; b < C_::kPartBoxes; ++b) {
               const int x = n0 + part * C_::kPartCols + b * C_::kBoxCols;
@@ -452,11 +456,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int Q, bool IN_BF16, bool OUT_BF16>
+template <int BN, int Q, int NBUF, int PARTS, int MINB, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_variant(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                            const BcsrParams &p, cudaStream_t stream) {
-  using C_ = Cfg<BN, Q, OUT_BF16>;
-  auto kern = bcsr_spmm_kernel<BN, Q, IN_BF16, OUT_BF16>;
+  using C_ = Cfg<BN, Q, NBUF, PARTS, MINB, OUT_BF16>;
+  auto kern = bcsr_spmm_kernel<BN, Q, NBUF, PARTS, MINB, IN_BF16, OUT_BF16>;
   static bool attr_set = false;  // per instantiation; the attribute is per device function
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::kSmemBytes);
@@ -464,19 +468,17 @@ cudaError_t launch_variant(const CUtensorMap &tmA, const CUtensorMap &tmB, const
     attr_set = true;
   }
   const int64_t tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + BN - 1) / BN);
-  const int64_t grid = tiles < p.max_ctas ? tiles : p.max_ctas;
+  const int64_t cap = p.max_ctas > 0 ? p.max_ctas : static_cast<int64_t>(MINB) * p.num_sms;
+  const int64_t grid = tiles < cap ? tiles : cap;
   kern<<<static_cast<unsigned>(grid), kThreads, C_::kSmemBytes, stream>>>(tmA, tmB, tmC, p);
   return cudaGetLastError();
 }
 
-template <int BN, int Q>
-cudaError_t launch_dtypes(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
-                          const BcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t s) {
-  if (in_bf16)
-    return out_bf16 ? launch_variant<BN, Q, true, true>(tmA, tmB, tmC, p, s)
-                    : launch_variant<BN, Q, true, false>(tmA, tmB, tmC, p, s);
-  return out_bf16 ? launch_variant<BN, Q, false, true>(tmA, tmB, tmC, p, s)
-                  : launch_variant<BN, Q, false, false>(tmA, tmB, tmC, p, s);
+template <int BN, int Q, int NBUF, int PARTS, int MINB, bool OUT_BF16>
+cudaError_t launch_in(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const BcsrParams &p,
+                      bool in_bf16, cudaStream_t s) {
+  return in_bf16 ? launch_variant<BN, Q, NBUF, PARTS, MINB, true, OUT_BF16>(tmA, tmB, tmC, p, s)
+                 : launch_variant<BN, Q, NBUF, PARTS, MINB, false, OUT_BF16>(tmA, tmB, tmC, p, s);
 }
 
 }  // namespace
@@ -484,10 +486,23 @@ cudaError_t launch_dtypes(const CUtensorMap &tmA, const CUtensorMap &tmB, const 
 cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const BcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream) {
   if (p.n_block_rows == 0 || p.N == 0) return cudaSuccess;
-  // Tile width: 128 columns (one MMA of N = 128 per k step) when N is small,
-  // else 256 (one MMA of N = 256).
-  if (p.N <= 128) return launch_dtypes<128, 6>(tmA, tmB, tmC, p, in_bf16, out_bf16, stream);
-  return launch_dtypes<256, 4>(tmA, tmB, tmC, p, in_bf16, out_bf16, stream);
+  // N <= 128: 128-column tiles (one MMA of N = 128 per k step), two
+  // accumulators, one CTA per SM.  Wider: 256-column tiles (one MMA of
+  // N = 256).  With at least two tiles per SM, two CTAs share each SM, each
+  // with one accumulator (the two fill TMEM), two stages and 64-column
+  // epilogue parts (32 for fp32 C), so each CTA's barrier handshakes and
+  // accumulator drain overlap the other's MMAs and loads (8% faster on a
+  // 90%-sparse 18944 x 3584 x 65536 product); with fewer tiles one CTA per SM
+  // keeps two accumulators and four stages.
+  if (p.N <= 128)
+    return out_bf16 ? launch_in<128, 6, 2, 2, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                    : launch_in<128, 6, 2, 2, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
+  const int64_t tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + 255) / 256);
+  if (tiles < 2ll * p.num_sms)
+    return out_bf16 ? launch_in<256, 4, 2, 2, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                    : launch_in<256, 4, 2, 2, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
+  return out_bf16 ? launch_in<256, 2, 1, 4, 2, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                  : launch_in<256, 2, 1, 8, 2, false>(tmA, tmB, tmC, p, in_bf16, stream);
 }
 
 }  // namespace spmm

@@ -17,7 +17,8 @@ struct BcsrParams {
   int64_t ldc;                   // row stride of C in elements (= N)
   int32_t M, N, K;
   int32_t n_block_rows;
-  int32_t max_ctas;              // persistent grid size (one CTA per SM)
+  int32_t max_ctas;              // cap on the persistent grid (0: the kernel's default CTAs per SM)
+  int32_t num_sms;
   uint32_t *status;              // device status word
   uint64_t wait_limit_ns;        // bound of every mbarrier wait
 };

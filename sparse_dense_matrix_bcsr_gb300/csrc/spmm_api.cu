@@ -319,7 +319,8 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(h->k);
     p.n_block_rows = static_cast<int32_t>(h->n_groups);
-    p.max_ctas = std::max(h->max_ctas > 0 ? std::min(h->max_ctas, h->num_sms) : h->num_sms, 1);
+    p.max_ctas = h->max_ctas;
+    p.num_sms = std::max(h->num_sms, 1);
     p.status = h->d_status;
     p.wait_limit_ns = h->wait_limit_ns;
     cudaError_t e = spmm::launch_bcsr(h->tm_vals, h->tm_B, h->tm_C, p, in_bf16, out_bf16, s);

@@ -46,6 +46,20 @@ def test_bcsr_parity_small(m, k, n, keep, dt, out_dt):
     full_check(m, k, n, rp, ci, vals, dt, out_dt, B)
 
 
+@pytest.mark.parametrize("m,k,n,keep,dt,out_dt", [
+    (19460, 256, 264, 0.5, "bf16", "bf16"),   # >= 2 tiles per SM: two CTAs per SM, bf16 C, ragged M and N
+    (9730, 192, 520, 0.7, "f16", "f32"),      # same path with fp32 C (32-column epilogue parts), 3 column tiles
+])
+def test_bcsr_parity_two_ctas_per_sm(m, k, n, keep, dt, out_dt):
+    """Enough 256-column tiles for the configuration with two CTAs per SM
+    (one accumulator each); compared element by element."""
+    rng = np.random.default_rng(m + n)
+    rp, ci = W.block_pattern(rng, m, k, 64, 64, keep=keep)
+    vals = W.draw_values(rng, len(ci), "u1", dt)
+    B = W.dense_bits(rng, (k, n), "u1", dt)
+    full_check(m, k, n, rp, ci, vals, dt, out_dt, B, runs=2)
+
+
 def test_bcsr_tiny_workload():
     w = W.bcsr_tiny()
     outs, info = full_check(w.m, w.k, w.n, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.B(), runs=2)
