@@ -78,6 +78,12 @@ struct WcsrParams {
   uint64_t wait_limit_ns;
 };
 
+// Persistent WCSR CTAs per SM at dense width N (the default grid is this
+// times the SM count), and the most it can be (the partial-sum workspace is
+// sized for it).
+int wcsr_ctas_per_sm(int64_t N);
+constexpr int kWcsrMaxCtasPerSm = 2;
+
 // Workspace floats per partial slot (16 rows x 256 columns).
 constexpr int64_t kWcsrSlotFloats = 16 * 256;
 

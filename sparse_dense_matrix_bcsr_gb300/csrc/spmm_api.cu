@@ -125,7 +125,7 @@ struct spmm_handle_s {
 
   // WCSR work decomposition: stages of <= 64 packed columns, and the
   // partial-sum workspace of windows cut between persistent CTAs
-  int32_t max_ctas = 0;  // 0: one CTA per SM
+  int32_t max_ctas = 0;  // 0: the kernels' default CTAs per SM
   int64_t n_stages = 0;
   uint8_t *d_stage_pack = nullptr;
   float *d_ws = nullptr;
@@ -263,7 +263,7 @@ spmm_status build_stages(spmm_handle h, const std::vector<int64_t> &wptr, const 
   if (!pack.empty())
     CUDA_TRY(cudaMemcpy(h->d_stage_pack, pack.data(), pack.size(), cudaMemcpyHostToDevice), "upload stage records");
   // Two partial slots per CTA, sized for the largest grid.
-  h->ws_slots = 2 * static_cast<int64_t>(std::max(h->num_sms, 1));
+  h->ws_slots = 2 * static_cast<int64_t>(spmm::kWcsrMaxCtasPerSm) * std::max(h->num_sms, 1);
   CUDA_TRY(cudaMalloc(&h->d_ws, h->ws_slots * spmm::kWcsrSlotFloats * sizeof(float)), "cudaMalloc(workspace)");
   CUDA_TRY(cudaMalloc(&h->d_partials, h->ws_slots * sizeof(spmm::WcsrPartial)), "cudaMalloc(partials)");
   return SPMM_OK;
@@ -273,7 +273,9 @@ spmm_status build_stages(spmm_handle h, const std::vector<int64_t> &wptr, const 
 int32_t wcsr_grid(spmm_handle h, int64_t N) {
   const int64_t bn = N <= 128 ? 128 : 256;
   const int64_t items = h->n_stages * ((N + bn - 1) / bn);
-  int64_t g = h->max_ctas > 0 ? std::min<int64_t>(h->max_ctas, h->num_sms) : h->num_sms;
+  const int64_t most = static_cast<int64_t>(spmm::kWcsrMaxCtasPerSm) * h->num_sms;
+  int64_t g = h->max_ctas > 0 ? std::min<int64_t>(h->max_ctas, most)
+                              : static_cast<int64_t>(spmm::wcsr_ctas_per_sm(N)) * h->num_sms;
   return static_cast<int32_t>(std::max<int64_t>(0, std::min(g, items)));
 }
 

@@ -21,27 +21,29 @@
 // The product is computed transposed: the 128 columns of an accumulator are
 // the MMA's M (TMEM lanes) and the 16 rows of a window are the MMA's N.
 //
-// Only the producer warps read global memory.  Their loads of stage
-// descriptors and column indices queue behind the SM's outstanding gathers,
-// so they are independent of each other (the column indices of stage s sit
-// at a fixed place, stage_idx[64*s ...]) and issued two work items ahead.
-// The MMA thread learns a stage's shape from a record the producer writes to
-// shared memory, and the epilogue learns a window's identity from a record
-// the MMA thread writes, so neither waits on a global load.
+// Only the producer warps read global memory.  Each stage is one record
+// (its 2 KB value tile, 64 column indices and descriptor) fetched with TMA
+// bulk copies into shared-memory rings ahead of use, so the producers read
+// indices from shared memory and no global load stalls their issue behind
+// the SM's outstanding gathers.  The MMA thread learns a stage's shape from a
+// record the producer writes to shared memory, and the epilogue learns a
+// window's identity from a record the MMA thread writes, so neither waits on
+// a global load.
 //
-// 9 warps:
-//   warps 0..3  producers; warp w loads the work items w, w+4, ... of the
-//               CTA's range: the 64 B rows with 16-byte cp.async (one B row,
-//               512 B, per warp instruction at BN = 256) and, two of its items
-//               ahead, the item's 2 KB value tile with one TMA bulk copy into
-//               a separate ring; every lane ends the item with
-//               cp.async.mbarrier.arrive.noinc, so producers never block on
-//               their own copies and one warp's barrier handling overlaps
-//               another's copies
-//   warp 4      TMEM allocator and MMA issuer; fences the generic proxy
-//               against the async proxy before reading a stage
-//   warps 5..8  epilogue (warp w reads TMEM sub-partition w % 4), four
-//               accumulator buffers in TMEM rotate between windows
+// PW + 5 warps (PW producer warps; two CTAs per SM run with PW = 2, so one
+// CTA's barrier handshakes and MMA issue stalls overlap the other's work):
+//   warps 0..PW-1  producers; warp w owns the work items w, w+PW, ... of the
+//                  CTA's range: it fetches an item's record kVLead of its
+//                  items ahead, then copies the item's 64 B rows with 16-byte
+//                  cp.async (one B row, 512 B, per warp instruction at
+//                  BN = 256); every lane ends the item with
+//                  cp.async.mbarrier.arrive.noinc, so producers never block
+//                  on their own copies and one warp's barrier handling
+//                  overlaps another's copies
+//   warp PW        TMEM allocator and MMA issuer; fences the generic proxy
+//                  against the async proxy before reading a stage
+//   warps PW+1..   epilogue (warp w reads TMEM sub-partition w % 4), four
+//                  accumulator buffers in TMEM rotate between windows
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -59,17 +61,17 @@ constexpr int kKC = 64;                      // packed columns per stage
 constexpr int kValBytes = kH * kKC * 2;      // 2 KB value tile per stage
 constexpr int kMetaBytes = kWcsrPackBytes - kWcsrPackIdxOff;  // a stage record's indices + descriptor
 constexpr int kChunkBytes = kKC * 64 * 2;    // 64 gathered rows x 64 columns
-constexpr int kProducerWarps = 4;
-constexpr int kMmaWarp = kProducerWarps;
 constexpr int kEpiWarps = 4;
-constexpr int kThreads = 32 * (kProducerWarps + 1 + kEpiWarps);
 constexpr int kAccBufs = 4;
 
 constexpr int kVLead = 2;      // a producer fetches stage records (value tiles) this many of its own items ahead
-constexpr int kLead = kVLead * kProducerWarps;  // = this many work items ahead
 
-template <int NACC, int Q>
+// NACC accumulators of 128 columns, Q stages, PW producer warps, MINB CTAs per SM.
+template <int NACC, int Q, int PW, int MINB>
 struct Cfg {
+  static constexpr int kMmaWarp = PW;                        // warps 0..PW-1 produce, PW issues MMAs
+  static constexpr int kThreads = 32 * (PW + 1 + kEpiWarps);
+  static constexpr int kLead = kVLead * PW;                  // records are fetched this many work items ahead
   static constexpr int kBN = 128 * NACC;
   static constexpr int kChunks = 2 * NACC;
   static constexpr int kStageBytes = kChunks * kChunkBytes;  // gathered B rows only
@@ -81,10 +83,11 @@ struct Cfg {
   static constexpr int kVQ = Q + kLead;
   static constexpr int kMetaRing = (kVQ * kMetaBytes + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes = Q * kStageBytes + kVQ * kValBytes + kMetaRing + 2048 + 1024;
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static_assert(kSmemBytes <= 227 * 1024 && MINB * (kSmemBytes + 1024) <= 228 * 1024, "shared memory");
+  static_assert(MINB * kTmemCols <= 512, "TMEM");
   // no-allocation variant: a value slot is reused by the item kVQ later and a
   // producer fills it kVLead of its items (kVLead * 4 work items) ahead
-  static_assert(kVQ > kVLead * kProducerWarps, "value slots must outlast the lead");
+  static_assert(kVQ > kVLead * PW, "value slots must outlast the lead");
   static_assert(kAccBufs * kAccCols <= kTmemCols, "accumulator buffers exceed the TMEM allocation");
 };
 
@@ -121,10 +124,12 @@ struct SegRec {     // MMA -> epilogue, one per accumulator buffer
 // read from device memory (the stage list is built on the device), CTAs
 // beyond the number of work items leave at once, and column indices are read
 // from window_col_idx at each stage's first packed column.
-template <int NACC, int Q, bool IN_BF16, bool OUT_BF16, bool NOALLOC = false>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NACC, int Q, int PW, int MINB, bool IN_BF16, bool OUT_BF16, bool NOALLOC = false>
+__global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
     wcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmV, const WcsrParams p) {
-  using C_ = Cfg<NACC, Q>;
+  using C_ = Cfg<NACC, Q, PW, MINB>;
+  constexpr int kMmaWarp = C_::kMmaWarp;
+  constexpr int kLead = C_::kLead;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int kVQ = C_::kVQ;
@@ -192,10 +197,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < kProducerWarps) {
+  if (warp < PW) {
     // ------------------------------------------------------------ producers
     const uint16_t *Bp = reinterpret_cast<const uint16_t *>(p.B);
-    constexpr int kStep = kProducerWarps;
+    constexpr int kStep = PW;
     // The B rows of one work item -> stage `st` with 16-byte cp.async
     // (zero-fill for padding positions and columns past N); lo / hi hold the
     // item's column indices for positions lane and 32 + lane.
@@ -595,17 +600,17 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
+template <int NACC, int Q, int PW, int MINB, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_variant(const CUtensorMap &tmV, const WcsrParams &p, cudaStream_t stream) {
-  using C_ = Cfg<NACC, Q>;
-  auto kern = wcsr_spmm_kernel<NACC, Q, IN_BF16, OUT_BF16>;
+  using C_ = Cfg<NACC, Q, PW, MINB>;
+  auto kern = wcsr_spmm_kernel<NACC, Q, PW, MINB, IN_BF16, OUT_BF16>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<p.grid, kThreads, C_::kSmemBytes, stream>>>(tmV, p);
+  kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(tmV, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, 0, stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
@@ -613,12 +618,14 @@ cudaError_t launch_variant(const CUtensorMap &tmV, const WcsrParams &p, cudaStre
   return cudaGetLastError();
 }
 
-template <int NACC, int Q>
+template <int NACC, int Q, int PW, int MINB>
 cudaError_t launch_dtypes(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
                           cudaStream_t s) {
   if (in_bf16)
-    return out_bf16 ? launch_variant<NACC, Q, true, true>(tmV, p, s) : launch_variant<NACC, Q, true, false>(tmV, p, s);
-  return out_bf16 ? launch_variant<NACC, Q, false, true>(tmV, p, s) : launch_variant<NACC, Q, false, false>(tmV, p, s);
+    return out_bf16 ? launch_variant<NACC, Q, PW, MINB, true, true>(tmV, p, s)
+                    : launch_variant<NACC, Q, PW, MINB, true, false>(tmV, p, s);
+  return out_bf16 ? launch_variant<NACC, Q, PW, MINB, false, true>(tmV, p, s)
+                  : launch_variant<NACC, Q, PW, MINB, false, false>(tmV, p, s);
 }
 
 // ------------------------------------------------------------ no-allocation variant
@@ -666,8 +673,8 @@ __global__ void __launch_bounds__(1024)
 
 template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_noalloc_variant(const WcsrParams &p, cudaStream_t stream) {
-  using C_ = Cfg<NACC, Q>;
-  auto kern = wcsr_spmm_kernel<NACC, Q, IN_BF16, OUT_BF16, true>;
+  using C_ = Cfg<NACC, Q, 4, 1>;
+  auto kern = wcsr_spmm_kernel<NACC, Q, 4, 1, IN_BF16, OUT_BF16, true>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::kSmemBytes);
@@ -676,7 +683,7 @@ cudaError_t launch_noalloc_variant(const WcsrParams &p, cudaStream_t stream) {
   }
   CUtensorMap unused;  // the kernel loads values with cp.async; the map is not read
   memset(&unused, 0, sizeof unused);
-  kern<<<p.grid, kThreads, C_::kSmemBytes, stream>>>(unused, p);
+  kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(unused, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, 0, stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
@@ -742,11 +749,18 @@ cudaError_t launch_wcsr_noalloc(WcsrParams p, const int64_t *window_row_ptr, int
                   : launch_noalloc_variant<2, 5, false, false>(p, stream);
 }
 
+// Two CTAs per SM, each with two producer warps: one CTA's barrier
+// handshakes and MMA issue stalls overlap the other's work.
+int wcsr_ctas_per_sm(int64_t N) {
+  (void)N;
+  return 2;
+}
+
 cudaError_t launch_wcsr(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
                         cudaStream_t stream) {
   if (p.n_stages == 0 || p.N == 0 || p.grid == 0) return cudaSuccess;
-  if (p.N <= 128) return launch_dtypes<1, 11>(tmV, p, in_bf16, out_bf16, stream);
-  return launch_dtypes<2, 6>(tmV, p, in_bf16, out_bf16, stream);
+  if (p.N <= 128) return launch_dtypes<1, 5, 2, 2>(tmV, p, in_bf16, out_bf16, stream);
+  return launch_dtypes<2, 2, 2, 2>(tmV, p, in_bf16, out_bf16, stream);
 }
 
 }  // namespace spmm
