@@ -55,8 +55,7 @@ constexpr int kMmaWarp = 1;
 constexpr int kEpiWarp0 = 2;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int kBoxRows = 16;                  // C rows of one TMA store box (one epilogue warp)
-constexpr int kBoxBytes = kBoxRows * 128;     // 16 rows of 128 bytes, 128-byte swizzle
+constexpr int kBoxBytes = 2048;               // one TMA store box of C in shared memory
 
 // Stage record flags (producer -> MMA) and accumulator record flags (MMA -> epilogue).
 constexpr int32_t kRecFirst = 1;  // first stored block of its tile
@@ -72,19 +71,33 @@ struct TileRec {
 };
 
 // BN columns per tile, Q pipeline stages, NBUF TMEM accumulators, the
-// epilogue writing a tile in PARTS column parts through two alternating
-// staging buffers, MINB CTAs per SM.
+// epilogue writing each warp's share of a tile in PARTS column parts through
+// two alternating staging buffers, MINB CTAs per SM.
+//
+// Narrow tiles (BN = 128) use the plain MMA, M = 64 x N = 128: the
+// accumulator's rows 16s..16s+15 sit in TMEM lanes 32s..32s+15, so epilogue
+// warp s holds 16 rows x BN columns and stores 16-row x 128-byte boxes (128-byte
+// swizzle).  Wide tiles (BN = 256) use the weight-stationary MMA, M = 64 x
+// N = 256 (~93 cycles on GB300 against 128): rows 0..63 sit in lanes 0..63 for
+// columns 0..127 and in lanes 64..127 for columns 128..255, in 128 TMEM
+// columns, so warp s holds rows 32(s%2)..32(s%2)+31 x columns 128(s/2) ..
+// 128(s/2)+127 and stores 32-row x 64-byte boxes (64-byte swizzle).
 template <int BN, int Q, int NBUF, int PARTS, int MINB, bool OUT_BF16>
 struct Cfg {
   static constexpr int kBN = BN;
+  static constexpr bool kWS = BN >= 256;                      // weight-stationary MMA
   static constexpr int kNmma = BN < 256 ? BN : 256;           // N of one MMA
   static constexpr int kMmas = BN / kNmma;                    // MMAs per 16-deep k step
   static constexpr int kChunks = BN / 64;                     // 64-column chunks of the B tile
   static constexpr int kStageBytes = kBlkBytes + kChunks * kChunkBytes;
-  static constexpr int kTmemCols = NBUF * BN;                 // NBUF accumulators of BN columns
+  static constexpr int kAccCols = kWS ? BN / 2 : BN;          // TMEM columns of one accumulator
+  static constexpr int kTmemCols = NBUF * kAccCols;
   static constexpr int kOutBytes = OUT_BF16 ? 2 : 4;
-  static constexpr int kBoxCols = 128 / kOutBytes;            // C columns of one store box
-  static constexpr int kPartCols = BN / PARTS;
+  static constexpr int kWarpRows = kWS ? 32 : 16;             // rows of C an epilogue warp holds
+  static constexpr int kWarpCols = kWS ? BN / 2 : BN;         // columns of C an epilogue warp holds
+  static constexpr int kRowBytes = kWS ? 64 : 128;            // bytes of a store box row
+  static constexpr int kBoxCols = kRowBytes / kOutBytes;      // C columns of one store box
+  static constexpr int kPartCols = kWarpCols / PARTS;
   static constexpr int kPartGroups = kPartCols / 16;          // 16-column TMEM loads per part
   static constexpr int kBatch = kPartGroups < 4 ? kPartGroups : 4;  // TMEM loads per wait
   static constexpr int kBatches = kPartGroups / kBatch;
@@ -94,10 +107,11 @@ struct Cfg {
   static constexpr int kStagingBytes = kEpiWarps * kWarpStaging;
   static constexpr int kMiscBytes = 1024;                     // barriers, records, TMEM address
   static constexpr int kSmemBytes = Q * kStageBytes + kStagingBytes + kMiscBytes + 1024;  // + alignment slack
+  static_assert(kWarpRows * kRowBytes == kBoxBytes, "store box");
   static_assert(kSmemBytes <= 227 * 1024 && MINB * (kSmemBytes + 1024) <= 228 * 1024, "shared memory");
   static_assert(MINB * kTmemCols <= 512 && (kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512), "TMEM");
   static_assert((2 * Q + 6) * 8 + (Q + 2) * 16 + 16 <= kMiscBytes, "barrier area");
-  static_assert(BN % 128 == 0 && kNmma % 16 == 0 && kPartBoxes >= 1 && PARTS % 2 == 0 &&
+  static_assert(BN % 128 == 0 && BN <= 256 && kNmma % 16 == 0 && kPartBoxes >= 1 && PARTS % 2 == 0 &&
                     kPartGroups % kBatch == 0, "tile shape");
 };
 
@@ -291,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
           const int nmma = min(C_::kMmas, (p.N - rec.nt * BN + C_::kNmma - 1) / C_::kNmma);
           const uint32_t a_blk = smem_addr(smem + stage * C_::kStageBytes);  // block: MMA operand A (K-major)
           const uint32_t b_til = a_blk + kBlkBytes;                          // B tile: MMA operand B (MN-major)
-          const uint32_t acc = tmem + buf * BN;
+          const uint32_t acc = tmem + buf * C_::kAccCols;
           const bool first = (rec.flags & kRecFirst) != 0;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
@@ -301,7 +315,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
               if (m < nmma) {
                 const uint64_t bdesc = smem_desc_sw128(b_til + m * (C_::kNmma / 64) * kChunkBytes + kk * 2048,
                                                        kChunkBytes, 1024);
-                umma_f16(acc + m * C_::kNmma, adesc, bdesc, idesc, (first && kk == 0) ? 0u : 1u);
+                if constexpr (C_::kWS)
+                  umma_ws_f16(acc, adesc, bdesc, idesc, (first && kk == 0) ? 0u : 1u);
+                else
+                  umma_f16(acc + m * C_::kNmma, adesc, bdesc, idesc, (first && kk == 0) ? 0u : 1u);
               }
             }
           }
@@ -339,15 +356,17 @@ __global__ void __launch_bounds__(kThreads, MINB)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // Lane t < 16 of warp w holds row 16*(w%4) + t of the block row.  Its
-    // 16-column pieces go to the warp's staging area as 16-row x 128-byte
-    // boxes in the 128-byte swizzled layout the TMA store reads.  Each batch
-    // of four TMEM loads is issued before the previous batch is written to
-    // shared memory, so the load latency overlaps that work.
+    // Warp w reads TMEM sub-partition s = w % 4; lane t holds one row of C
+    // (see Cfg for which rows and columns).  Its 16-column pieces go to the
+    // warp's staging area as store boxes in the swizzled layout the TMA store
+    // reads.  Each batch of TMEM loads is issued before the previous batch is
+    // written to shared memory, so the load latency overlaps that work.
     const int sp = warp & 3;
     uint8_t *stg = staging + (warp - kEpiWarp0) * C_::kWarpStaging;
     const uint32_t stg_addr = smem_addr(stg);
-    const uint32_t row_sw = static_cast<uint32_t>(lane & 7);
+    // 16-byte unit u of box row t is stored at unit u ^ row_sw
+    const uint32_t row_sw = static_cast<uint32_t>(C_::kWS ? (lane >> 1) & 3 : lane & 7);
+    const bool row_lane = lane < C_::kWarpRows;
     uint32_t tcount = 0;
     while (true) {
       const uint32_t buf = tcount % NBUF;
@@ -362,11 +381,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
       const int32_t flags = acc_rec[buf].flags;
       if (flags & kRecEnd) break;
       const bool zero = (flags & kRecEmpty) != 0;
-      const int row0 = acc_rec[buf].br * kBlk + sp * kBoxRows;
-      const int n0 = acc_rec[buf].nt * BN;
-      const int ncg = min(BN / 16, (p.N - n0 + 15) / 16);  // 16-column groups holding columns of C
+      const int row0 = acc_rec[buf].br * kBlk + (C_::kWS ? (sp & 1) * 32 : sp * 16);
+      const int n0 = acc_rec[buf].nt * BN + (C_::kWS ? (sp >> 1) * C_::kWarpCols : 0);  // this warp's first column
+      const int ncg = max(0, min(C_::kWarpCols / 16, (p.N - n0 + 15) / 16));  // 16-column groups holding C
       tc_fence_after_sync();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(sp * 32) << 16) + buf * BN;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(sp * 32) << 16) + buf * C_::kAccCols;
       // kBatch 16-column groups starting at group g0 -> registers
       auto load_batch = [&](int g0, uint32_t (&v)[C_::kBatch][16]) {
 #pragma unroll
@@ -381,11 +400,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
       };
       // registers -> staging part `pst` (gl0: first group of the part)
       auto store_batch = [&](uint8_t *pst, int g0, int gl0, const uint32_t (&v)[C_::kBatch][16]) {
-        if (lane < kBoxRows) {
+        if (row_lane) {
 #pragma unroll
           for (int g = 0; g < C_::kBatch; ++g) {
             const int col = (g0 + g - gl0) * 16;  // column within the part
-            uint8_t *row_base = pst + (col / C_::kBoxCols) * kBoxBytes + lane * 128;
+            uint8_t *row_base = pst + (col / C_::kBoxCols) * kBoxBytes + lane * C_::kRowBytes;
             const uint32_t u0 = static_cast<uint32_t>((col % C_::kBoxCols) * C_::kOutBytes / 16);
             if constexpr (OUT_BF16) {
               uint32_t w[8];
@@ -486,23 +505,22 @@ cudaError_t launch_in(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUte
 cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const BcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream) {
   if (p.n_block_rows == 0 || p.N == 0) return cudaSuccess;
-  // N <= 128: 128-column tiles (one MMA of N = 128 per k step), two
-  // accumulators, one CTA per SM.  Wider: 256-column tiles (one MMA of
-  // N = 256).  With at least two tiles per SM, two CTAs share each SM, each
-  // with one accumulator (the two fill TMEM), two stages and 64-column
-  // epilogue parts (32 for fp32 C), so each CTA's barrier handshakes and
-  // accumulator drain overlap the other's MMAs and loads (8% faster on a
-  // 90%-sparse 18944 x 3584 x 65536 product); with fewer tiles one CTA per SM
-  // keeps two accumulators and four stages.
-  if (p.N <= 128)
+  // N <= 128: 128-column tiles (one plain MMA of N = 128 per k step), two
+  // accumulators, one CTA per SM.  Wider (bcsr_wide_tiles): 256-column tiles,
+  // one weight-stationary MMA of N = 256 per k step, two accumulators of 128
+  // TMEM columns; with at least two tiles per SM two CTAs share each SM (two
+  // stages each), so one CTA's barrier handshakes overlap the other's MMAs
+  // and loads; with fewer tiles one CTA per SM runs four stages.  Epilogue
+  // parts are one 32-row x 64-byte store box (32 bf16 or 16 fp32 columns).
+  if (!bcsr_wide_tiles(p.N))
     return out_bf16 ? launch_in<128, 6, 2, 2, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
                     : launch_in<128, 6, 2, 2, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
   const int64_t tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + 255) / 256);
   if (tiles < 2ll * p.num_sms)
-    return out_bf16 ? launch_in<256, 4, 2, 2, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
-                    : launch_in<256, 4, 2, 2, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
-  return out_bf16 ? launch_in<256, 2, 1, 4, 2, true>(tmA, tmB, tmC, p, in_bf16, stream)
-                  : launch_in<256, 2, 1, 8, 2, false>(tmA, tmB, tmC, p, in_bf16, stream);
+    return out_bf16 ? launch_in<256, 4, 2, 4, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                    : launch_in<256, 4, 2, 8, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
+  return out_bf16 ? launch_in<256, 2, 2, 4, 2, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                  : launch_in<256, 2, 2, 8, 2, false>(tmA, tmB, tmC, p, in_bf16, stream);
 }
 
 }  // namespace spmm

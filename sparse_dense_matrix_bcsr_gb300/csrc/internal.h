@@ -23,10 +23,14 @@ struct BcsrParams {
   uint64_t wait_limit_ns;        // bound of every mbarrier wait
 };
 
+// The BCSR kernel's C store boxes: for N <= 128, 16 rows x 128 bytes with the
+// 128-byte swizzle; wider, 32 rows x 64 bytes with the 64-byte swizzle.
+inline bool bcsr_wide_tiles(int64_t N) { return N > 128; }
+
 // in_bf16: A/B are bf16 (else fp16); out_bf16: C is bf16 (else fp32).
 // tmA covers the blocks array as [n_blocks*64 rows, 64 cols], tmB covers B as
 // [K rows, N cols]; both with 64 x 64 boxes and 128-byte swizzle.  tmC covers
-// C as [M rows, N cols] with boxes of 16 rows x 128 bytes and 128-byte swizzle.
+// C as [M rows, N cols] with the boxes of bcsr_wide_tiles(N).
 cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const BcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream);
 

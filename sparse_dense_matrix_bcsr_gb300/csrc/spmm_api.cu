@@ -81,19 +81,22 @@ spmm_status encode_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t ro
 }
 
 // C as the destination of TMA stores: `rows` x `cols` row-major elements of
-// bf16 or fp32, boxes of 16 rows x 128 bytes (64 bf16 or 32 fp32 columns)
-// with the 128-byte swizzle.
+// bf16 or fp32.  Narrow (N <= 128) tiles store 16-row x 128-byte boxes with the
+// 128-byte swizzle, wide ones 32-row x 64-byte boxes with the 64-byte swizzle
+// (see bcsr_wide_tiles).
 spmm_status encode_c(CUtensorMap *map, void *base, bool bf16, uint64_t rows, uint64_t cols) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(SPMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const uint64_t esz = bf16 ? 2 : 4;
+  const bool wide = spmm::bcsr_wide_tiles(static_cast<int64_t>(cols));
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * esz};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), 16};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>((wide ? 64 : 128) / esz), wide ? 32u : 16u};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  wide ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SPMM_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", static_cast<int>(r));
   return SPMM_OK;
 }
