@@ -47,11 +47,11 @@ L2_FLUSH_BYTES = 256 << 20
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
 # valid only for the kernel source it was taken on (sha256 of the file).
 MEASURED_TRAFFIC = {
-    # bcsr_weight: 373 MB at N = 8192 (profiles/bcsr_kernel_bcsr_weight_N8192.md); B and C scale with
-    # N, A (13.6 MB) does not: 13.6 MB + 8 x 359.4 MB at N = 65536
-    "bcsr_kernel.cu": {"src_sha": "b27a9529ee16e40e", "bytes_per_launch": 2.889e9},
+    # bcsr_weight: 376 MB at N = 8192 (profiles/bcsr_kernel_bcsr_weight_N8192.md); B and C scale with
+    # N, A (13.6 MB) does not: 13.6 MB + 8 x 362.5 MB at N = 65536
+    "bcsr_kernel.cu": {"src_sha": "ed1bfeca25516e04", "bytes_per_launch": 2.914e9},
     # wcsr_uniform at its benchmark size (profiles/wcsr_kernel_wcsr_uniform.md)
-    "wcsr_kernel.cu": {"src_sha": "d86fc15b6ce8e5c4", "bytes_per_launch": 1.083e8},
+    "wcsr_kernel.cu": {"src_sha": "f609920ff4ac7c63", "bytes_per_launch": 1.084e8},
 }
 
 
