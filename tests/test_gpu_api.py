@@ -79,6 +79,34 @@ def test_run_host_matches_run(S, fmt):
     assert np.array_equal(C.astype(np.float64), outs[0])
 
 
+@pytest.mark.parametrize("fmt,out_dt", [("bcsr", "bf16"), ("wcsr", "f32")])
+def test_run_host_wide(S, fmt, out_dt):
+    """spmm_run_host at N = 4104 (several column tiles and a ragged last one),
+    called twice so the second call reuses the handle's staging buffers."""
+    import oracle
+    from spmm_testlib import assert_parity, ocode
+    rng = np.random.default_rng(2)
+    m, k, n = 260, 333, 4104
+    rp, ci, vals = W.random_csr(rng, m, k, 0.04, "bf16")
+    B = W.dense_bits(rng, (k, n), "n1", "bf16")
+    outs, _ = run_library(fmt, m, k, rp, ci, vals, "bf16", out_dt, B)
+    h = (S.spmm_bcsr_create if fmt == "bcsr" else S.spmm_wcsr_create)(m, k, rp, ci, vals, "bf16", out_dt)
+    try:
+        if out_dt == "f32":
+            C = np.full((m, n), np.nan, np.float32)
+        else:
+            C = np.full((m, n), 0xFFFF, np.uint16)  # bf16 NaN bits
+        for _ in range(2):
+            S.spmm_run_host(h, np.ascontiguousarray(B), C, n)
+    finally:
+        S.spmm_destroy(h)
+    Cd = C.astype(np.float64) if out_dt == "f32" else (C.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    C_ref, S_ref = oracle.spmm_csr(m, k, rp, ci, vals, ocode("bf16"), B)
+    assert_parity(Cd, C_ref, S_ref, f"{fmt} run_host N={n}")
+    if fmt == "bcsr":  # same blocks in the same order per tile: bitwise equal to the device-buffer run
+        assert np.array_equal(Cd, outs[0])
+
+
 def test_bounded_wait_reports_timeout(S):
     """A wait that nothing completes ends after its limit with a recorded
     timeout; the context stays usable afterwards."""
