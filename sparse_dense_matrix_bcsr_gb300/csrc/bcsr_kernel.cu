@@ -9,20 +9,18 @@
 // 2-D TMA loads).  On sm_103a the consumer is a single thread issuing
 // tcgen05.mma into TMEM:
 //   C[r, n] += sum_k blk[r, k] * B[k, n]
-// with the block as the M = 64 operand (K-major) and the B tile as the
-// N <= 256 operand (MN-major).  On GB300 an M=128 x N=64 MMA costs as long
-// as an M=64 x N=128 one (about 97 cycles), while M=64 x N=256 takes 128
-// cycles for twice the work, so the block rows are the MMA's M and the dense
-// columns its N.  An M=64 accumulator occupies TMEM lanes 0-15 of each
-// 32-lane sub-partition (rows 16s..16s+15 in lanes 32s..32s+15), one column
-// per output column.
+// with the block as the M = 64 operand (K-major) and the B tile as the N
+// operand (MN-major).  On GB300 an M=128 x N=64 MMA costs as long as an
+// M=64 x N=128 one (about 97 cycles), and the weight-stationary M=64 x N=256
+// form takes about 93 cycles for four times the work, so the block rows are
+// the MMA's M and the dense columns its N (see Cfg for the TMEM layouts).
 //
 // Work unit ("tile") = one block row x BN columns of C.  The kernel is
 // persistent: CTA c takes tiles c, c + G, c + 2G, ... (G = grid size); see
 // tile_coords for the order.  Two TMEM accumulators alternate between tiles,
 // so the epilogue of one tile overlaps the loads and MMAs of the next (with a
-// single accumulator of 512 columns the tensor pipe drains at every tile
-// boundary and the kernel measured 13% slower on GB300 than with two of 256).
+// single accumulator the tensor pipe drains at every tile boundary: 13%
+// slower on GB300).  Wide tiles run two CTAs per SM when there are enough.
 // 6 warps:
 //   warp 0      producer: reads the block-row pointers and block-column
 //               indices, waits for a free stage, writes the stage's tile
@@ -32,9 +30,9 @@
 //               global load, and hands each finished accumulator to the
 //               epilogue with a record of its own
 //   warps 2..5  epilogue: TMEM -> registers -> a per-warp staging area in
-//               shared memory -> TMA stores of 16-row boxes (warp w reads the
-//               TMEM lanes of sub-partition w % 4, i.e. rows 16(w%4) ..
-//               16(w%4)+15 of the block row)
+//               shared memory -> TMA stores (warp w reads the TMEM lanes of
+//               sub-partition w % 4; which rows and columns those hold
+//               depends on the tile width, see Cfg)
 // A block row without stored blocks still passes through the pipeline as
 // one stage without loads, so its rows of C are written (zeros) by the same
 // TMA stores.

@@ -110,16 +110,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-// Same, with an L2 cache-policy hint (createpolicy value).
-__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                                 int32_t x, int32_t y, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
-      : "memory");
-}
-
 // Contiguous bulk copy global -> shared (size a multiple of 16 bytes, both
 // addresses 16-byte aligned); completion is reported to `bar` as transaction
 // bytes.  Runs on the TMA engine, outside the issuing thread's cp.async
@@ -128,17 +118,6 @@ __device__ __forceinline__ void tma_bulk_load(uint32_t dst, const void *src, uin
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// Gather four rows (y0..y3) of a 2-D tensor, columns [x, x + box width), into
-// four consecutive box rows at dst.  The tensor map's box is one row high.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x,
-                                            int32_t y0, int32_t y1, int32_t y2, int32_t y3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3)
       : "memory");
 }
 
@@ -161,18 +140,6 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 // Wait until the issuing thread's bulk stores are complete.
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
 // ---------------------------------------------------------------- cp.async
 // 16-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros and
 // reads nothing.
@@ -187,12 +154,10 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+// Wait until all of this thread's cp.async copies are complete (the copies
+// here are tracked by mbarriers, not commit groups, so wait_all is the form
+// that covers them).
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Make this thread's completed generic-proxy shared-memory writes visible to
 // the async proxy (tcgen05.mma operand reads).

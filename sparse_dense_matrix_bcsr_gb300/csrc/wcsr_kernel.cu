@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
           cp_async_arrive_noinc(fb);
         }
       }
-      cp_async_wait<0>();
+      cp_async_wait_all();
       if (!ok && lane == 0) {
         atomicOr(p.status, kDevTimeout);
         *abort_flag = 1;
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
           ++tile;
         }
       }
-      cp_async_wait<0>();
+      cp_async_wait_all();
       if (!ok && lane == 0) {
         atomicOr(p.status, kDevTimeout);
         *abort_flag = 1;
