@@ -147,6 +147,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ---------------------------------------------------------------- multi-rank host logic
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest of the ranks' values of x (all-reduce MAX over the default
+    process group; a GPU tensor under NCCL, a host tensor under gloo)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as tdist
+    dev = f"cuda:{torch.cuda.current_device()}" if tdist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step_per_rank: float, steps: int, world: int, max_ms: float) -> float:
+    """Throughput of the whole job: every rank's work over the slowest rank's time."""
+    return flops_per_step_per_rank * steps * world / (max_ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank, world):
     import torch
@@ -225,13 +244,9 @@ def run_ours(args, rank, world):
         ms = [a.elapsed_time(b) for a, b in times[p["name"]]]
         per_part[p["name"]] = ms
     step_ms = [sum(per_part[p["name"]][i] for p in parts) for i in range(args.steps)]
-    total_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world)
     eff_per_step = sum(p["eff"] for p in parts)
-    value = eff_per_step * args.steps * world / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(eff_per_step, args.steps, world, total_ms)
 
     # roofline of each part; the dominant kernel (largest time share) is reported
     breakdown = []
@@ -279,12 +294,8 @@ def run_ours(args, rank, world):
         for _ in range(e2e_steps):
             for p, (hb, hc) in zip(parts, hosts):
                 S.spmm_run_host_ptr(p["h"], hb.data_ptr(), hc.data_ptr(), p["w"].n, sptr)
-        t_e2e = time.perf_counter() - t0
-        if dist:
-            t = torch.tensor([t_e2e], dtype=torch.float64)
-            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-            t_e2e = float(t.item())
-        e2e = {"value": round(eff_per_step * e2e_steps * world / t_e2e / 1e12, 4), "unit": UNIT,
+        t_e2e = max_over_ranks(time.perf_counter() - t0, world)
+        e2e = {"value": round(whole_job_tflops(eff_per_step, e2e_steps, world, t_e2e * 1e3), 4), "unit": UNIT,
                "h2d_bytes_per_step": int(sum(hb.numel() * 2 for hb, _ in hosts)),
                "d2h_bytes_per_step": int(sum(hc.numel() * hc.element_size() for _, hc in hosts)),
                "steps": e2e_steps}
