@@ -575,28 +575,53 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
 // Second pass: slot s holds a window's first stage but not its last -> this
 // block adds that partial and the first-segment partials of the following
 // CTAs (in CTA order) until the one holding the window's last stage, and
-// writes the window's rows of C.
+// writes the window's rows of C.  The list of contributing slots is found
+// once per block (dynamic shared memory, one int per CTA of the first pass);
+// each thread then sums four adjacent columns with independent loads.
 template <bool OUT_BF16>
 __global__ void __launch_bounds__(256)
     wcsr_reduce_kernel(const WcsrPartial *partials, const float *ws, void *C, int32_t M, int32_t N, int32_t grid,
                        int32_t bn) {
+  extern __shared__ int32_t contrib[];  // [grid]
+  __shared__ int32_t n_contrib;
   const int slot = blockIdx.x;
   const WcsrPartial rec = partials[slot];
   if (rec.window < 0 || !(rec.flags & kStageFirst) || (rec.flags & kStageLast)) return;
-  const int n0 = rec.col_tile * bn;
-  const int width = min(bn, N - n0);
-  for (int e = threadIdx.x; e < kH * width; e += blockDim.x) {
-    const int q = e / width;
-    const int col = e - q * width;
-    const int row = rec.window * kH + q;
-    float acc = ws[static_cast<int64_t>(slot) * kWcsrSlotFloats + q * 256 + col];
+  if (threadIdx.x == 0) {
+    int n = 0;
+    contrib[n++] = slot;
     for (int c = slot / 2 + 1; c < grid; ++c) {
       const WcsrPartial r = partials[2 * c];
       if (r.window != rec.window || r.col_tile != rec.col_tile) break;
-      acc += ws[static_cast<int64_t>(2 * c) * kWcsrSlotFloats + q * 256 + col];
+      contrib[n++] = 2 * c;
       if (r.flags & kStageLast) break;
     }
-    if (row < M) store_out<OUT_BF16>(C, static_cast<int64_t>(row) * N + n0 + col, acc);
+    n_contrib = n;
+  }
+  __syncthreads();
+  const int n = n_contrib;
+  const int n0 = rec.col_tile * bn;
+  const int width = min(bn, N - n0);  // a multiple of 8 (N is)
+  for (int e = 4 * threadIdx.x; e < kH * width; e += 4 * blockDim.x) {
+    const int q = e / width;
+    const int col = e - q * width;  // a multiple of 4
+    const int row = rec.window * kH + q;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < n; ++i) {
+      const float4 v = *reinterpret_cast<const float4 *>(ws + static_cast<int64_t>(contrib[i]) * kWcsrSlotFloats +
+                                                         q * 256 + col);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    if (row < M) {
+      const int64_t o = static_cast<int64_t>(row) * N + n0 + col;
+      store_out<OUT_BF16>(C, o, acc.x);
+      store_out<OUT_BF16>(C, o + 1, acc.y);
+      store_out<OUT_BF16>(C, o + 2, acc.z);
+      store_out<OUT_BF16>(C, o + 3, acc.w);
+    }
   }
 }
 
@@ -613,7 +638,7 @@ cudaError_t launch_variant(const CUtensorMap &tmV, const WcsrParams &p, cudaStre
   kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(tmV, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, 0, stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
+  wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, p.grid * sizeof(int32_t), stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
                                                                C_::kBN);
   return cudaGetLastError();
 }
@@ -686,7 +711,7 @@ cudaError_t launch_noalloc_variant(const WcsrParams &p, cudaStream_t stream) {
   kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(unused, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, 0, stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
+  wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, p.grid * sizeof(int32_t), stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
                                                                C_::kBN);
   return cudaGetLastError();
 }
