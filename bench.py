@@ -51,7 +51,7 @@ MEASURED_TRAFFIC = {
     # N, A (13.6 MB) does not: 13.6 MB + 8 x 362.5 MB at N = 65536
     "bcsr_kernel.cu": {"src_sha": "2acc16b6708d6524", "bytes_per_launch": 2.914e9},
     # wcsr_uniform at its benchmark size (profiles/wcsr_kernel_wcsr_uniform.md)
-    "wcsr_kernel.cu": {"src_sha": "6c9560c779aa0930", "bytes_per_launch": 1.088e8},
+    "wcsr_kernel.cu": {"src_sha": "4a2ab33295fb992a", "bytes_per_launch": 1.086e8},
 }
 
 
