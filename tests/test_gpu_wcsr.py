@@ -40,8 +40,9 @@ def test_wcsr_parity_small(m, k, n, d, dt, out_dt):
     full_check(m, k, n, rp, ci, vals, dt, out_dt, B)
 
 
-@pytest.mark.parametrize("ctas,n", [(3, 256), (7, 128), (13, 72), (5, 520)])
-def test_wcsr_windows_cut_between_ctas(ctas, n):
+@pytest.mark.parametrize("ctas,n,out_dt", [(3, 256, "f32"), (7, 128, "f32"), (13, 72, "f32"), (5, 520, "f32"),
+                                          (6, 264, "bf16")])
+def test_wcsr_windows_cut_between_ctas(ctas, n, out_dt):
     """Few persistent CTAs: long windows are cut between CTAs and finished by
     the second kernel; the result must match and be bitwise reproducible."""
     rng = np.random.default_rng(ctas)
@@ -49,7 +50,7 @@ def test_wcsr_windows_cut_between_ctas(ctas, n):
     rp, ci = W.powerlaw_pattern(rng, m, k, 1.3, 1, 1500, 300, 0.7)
     vals = W.draw_values(rng, len(ci), "u1", "bf16")
     B = W.dense_bits(rng, (k, n), "u1", "bf16")
-    outs, info = full_check(m, k, n, rp, ci, vals, "bf16", "f32", B, max_ctas=ctas, runs=2)
+    outs, info = full_check(m, k, n, rp, ci, vals, "bf16", out_dt, B, max_ctas=ctas, runs=2)
     assert info["n_split_windows"] > 0
     assert np.array_equal(outs[0], outs[1])
 
