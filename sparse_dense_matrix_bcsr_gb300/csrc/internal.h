@@ -103,11 +103,9 @@ cudaError_t launch_wcsr_noalloc(WcsrParams p, const int64_t *window_row_ptr, int
                                 bool in_bf16, bool out_bf16, cudaStream_t stream);
 size_t wcsr_noalloc_scratch_bytes();
 
-// tmV covers the values array as [16 rows, P_total cols] with 64 x 16 boxes
-// and 128-byte swizzle.  Runs the SpMM kernel, then the kernel that adds the
-// partials of windows cut between CTAs.
-cudaError_t launch_wcsr(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
-                        cudaStream_t stream);
+// Runs the SpMM kernel, then the kernel that adds the partials of windows
+// cut between CTAs.
+cudaError_t launch_wcsr(const WcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream);
 
 // Failure-detection self test: wait on an mbarrier nothing arrives at.
 cudaError_t launch_wait_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t stream);

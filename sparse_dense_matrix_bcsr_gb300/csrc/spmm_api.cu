@@ -117,7 +117,7 @@ struct spmm_handle_s {
   int32_t *d_idx = nullptr;
   uint16_t *d_vals = nullptr;
   size_t vals_bytes = 0;
-  CUtensorMap tm_vals;
+  CUtensorMap tm_vals;  // BCSR: the blocks array as [n_blocks*64 rows, 64 cols] for TMA
 
   const void *b_cached = nullptr;
   int64_t n_cached = -1;
@@ -353,7 +353,7 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
   p.grid = wcsr_grid(h, N);
   p.status = h->d_status;
   p.wait_limit_ns = h->wait_limit_ns;
-  cudaError_t e = spmm::launch_wcsr(h->tm_vals, p, in_bf16, out_bf16, s);
+  cudaError_t e = spmm::launch_wcsr(p, in_bf16, out_bf16, s);
   if (e != cudaSuccess) return cuda_fail(e, "WCSR kernel launch");
   return SPMM_OK;
 }
@@ -464,10 +464,6 @@ spmm_status spmm_wcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64
   h->n_units = f.n_units;
   h->stored = f.n_units * window_h;
   st = upload_common(h, f);
-  if (st == SPMM_OK && window_h == 16 && col_pad % 16 == 0)
-    st = encode_2d(&h->tm_vals, h->d_vals, in_t == SPMM_BF16, 16,
-                   static_cast<uint64_t>(f.n_units > 0 ? f.n_units : 64),
-                   static_cast<uint64_t>(f.n_units > 0 ? f.n_units : 64), 16, 64);
   if (st == SPMM_OK) st = build_stages(h, f.ptr, f.idx, f.vals);
   if (st != SPMM_OK) {
     free_handle(h);

@@ -126,7 +126,7 @@ struct SegRec {     // MMA -> epilogue, one per accumulator buffer
 // from window_col_idx at each stage's first packed column.
 template <int NACC, int Q, int PW, int MINB, bool IN_BF16, bool OUT_BF16, bool NOALLOC = false>
 __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
-    wcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmV, const WcsrParams p) {
+    wcsr_spmm_kernel(const WcsrParams p) {
   using C_ = Cfg<NACC, Q, PW, MINB>;
   constexpr int kMmaWarp = C_::kMmaWarp;
   constexpr int kLead = C_::kLead;
@@ -626,7 +626,7 @@ __global__ void __launch_bounds__(256)
 }
 
 template <int NACC, int Q, int PW, int MINB, bool IN_BF16, bool OUT_BF16>
-cudaError_t launch_variant(const CUtensorMap &tmV, const WcsrParams &p, cudaStream_t stream) {
+cudaError_t launch_variant(const WcsrParams &p, cudaStream_t stream) {
   using C_ = Cfg<NACC, Q, PW, MINB>;
   auto kern = wcsr_spmm_kernel<NACC, Q, PW, MINB, IN_BF16, OUT_BF16>;
   static bool attr_set = false;
@@ -635,7 +635,7 @@ cudaError_t launch_variant(const CUtensorMap &tmV, const WcsrParams &p, cudaStre
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(tmV, p);
+  kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, p.grid * sizeof(int32_t), stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
@@ -644,13 +644,12 @@ cudaError_t launch_variant(const CUtensorMap &tmV, const WcsrParams &p, cudaStre
 }
 
 template <int NACC, int Q, int PW, int MINB>
-cudaError_t launch_dtypes(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
-                          cudaStream_t s) {
+cudaError_t launch_dtypes(const WcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t s) {
   if (in_bf16)
-    return out_bf16 ? launch_variant<NACC, Q, PW, MINB, true, true>(tmV, p, s)
-                    : launch_variant<NACC, Q, PW, MINB, true, false>(tmV, p, s);
-  return out_bf16 ? launch_variant<NACC, Q, PW, MINB, false, true>(tmV, p, s)
-                  : launch_variant<NACC, Q, PW, MINB, false, false>(tmV, p, s);
+    return out_bf16 ? launch_variant<NACC, Q, PW, MINB, true, true>(p, s)
+                    : launch_variant<NACC, Q, PW, MINB, true, false>(p, s);
+  return out_bf16 ? launch_variant<NACC, Q, PW, MINB, false, true>(p, s)
+                  : launch_variant<NACC, Q, PW, MINB, false, false>(p, s);
 }
 
 // ------------------------------------------------------------ no-allocation variant
@@ -706,9 +705,7 @@ cudaError_t launch_noalloc_variant(const WcsrParams &p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  CUtensorMap unused;  // the kernel loads values with cp.async; the map is not read
-  memset(&unused, 0, sizeof unused);
-  kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(unused, p);
+  kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, p.grid * sizeof(int32_t), stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
@@ -784,11 +781,10 @@ int wcsr_ctas_per_sm(int64_t N) {
   return 2;
 }
 
-cudaError_t launch_wcsr(const CUtensorMap &tmV, const WcsrParams &p, bool in_bf16, bool out_bf16,
-                        cudaStream_t stream) {
+cudaError_t launch_wcsr(const WcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream) {
   if (p.n_stages == 0 || p.N == 0 || p.grid == 0) return cudaSuccess;
-  if (p.N <= 128) return launch_dtypes<1, 5, 2, 2>(tmV, p, in_bf16, out_bf16, stream);
-  return launch_dtypes<2, 3, 2, 2>(tmV, p, in_bf16, out_bf16, stream);
+  if (p.N <= 128) return launch_dtypes<1, 5, 2, 2>(p, in_bf16, out_bf16, stream);
+  return launch_dtypes<2, 3, 2, 2>(p, in_bf16, out_bf16, stream);
 }
 
 }  // namespace spmm
