@@ -89,6 +89,13 @@ def part_model(w, info):
     return eff_flops, stored_flops, bytes_min
 
 
+def gather_model(w, info):
+    """WCSR's secondary roof: bytes of B rows gathered from L2 by one launch,
+    one row of N 16-bit values per packed (padded) column.  No HBM roofline
+    counts them; there is no measured L2 peak to set them against."""
+    return 2.0 * info["n_units"] * w.n if w.fmt == "wcsr" else 0.0
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
@@ -274,6 +281,10 @@ def run_ours(args, rank, world):
             "format": {k: p["info"][k] for k in ("nnz", "stored", "padding", "n_units", "n_tasks",
                                                  "n_split_windows")},
         })
+        gb = gather_model(p["w"], p["info"])
+        if gb:
+            breakdown[-1]["gather"] = {"bytes": int(gb), "achieved_gbs": round(gb / t / 1e9, 1),
+                                       "note": "B rows gathered from L2; no measured L2 peak"}
     dom = max(breakdown, key=lambda b: b["ms_mean"])
 
     # end to end through the public API with pinned host buffers
@@ -481,7 +492,9 @@ def run_sweep(args):
                 "eff_tflops": round(eff / t / 1e12, 3), "eff_tflops_warm": round(eff / (warm * 1e-3) / 1e12, 3),
                 "roofline_frac": round(max(t_tc, t_hbm) / t, 4), "bound": "hbm" if t_hbm >= t_tc else "tensor",
                 "t_roof_us": round(max(t_tc, t_hbm) * 1e6, 2), "n_tasks": info["n_tasks"],
-                "n_split_windows": info["n_split_windows"]}), flush=True)
+                "n_split_windows": info["n_split_windows"],
+                "gather_gbs": round(gather_model(w, info) / t / 1e9, 1) if w.fmt == "wcsr" else None}),
+                flush=True)
         for hh in cache.values():
             S.spmm_destroy(hh)
 

@@ -68,3 +68,11 @@ def test_traffic_key_ignores_comments_only(tmp_path, monkeypatch):
     assert bench.src_sha("k.cu") == h0
     (csrc / "k.cu").write_text("int a = 1;\nint b = 3;\n")
     assert bench.src_sha("k.cu") != h0
+
+
+def test_gather_model_counts_one_b_row_per_packed_column():
+    class _W:  # the two fields gather_model reads
+        fmt, n = "wcsr", 256
+    assert bench.gather_model(_W, {"n_units": 1000}) == 2.0 * 1000 * 256
+    _W.fmt = "bcsr"
+    assert bench.gather_model(_W, {"n_units": 1000}) == 0.0
