@@ -47,10 +47,10 @@ L2_FLUSH_BYTES = 256 << 20
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
 # valid only for the kernel source it was taken on (sha256 of the file).
 MEASURED_TRAFFIC = {
-    # bcsr_weight: 376 MB at N = 8192 (profiles/bcsr_kernel_bcsr_weight_N8192.md); B and C scale with
-    # N, A (13.6 MB) does not: 13.6 MB + 8 x 362.5 MB at N = 65536
+    # bcsr_weight: 376 MB measured at N = 8192; B and C scale with N, A (13.6 MB)
+    # does not: 13.6 MB + 8 x 362.5 MB at N = 65536
     "bcsr_kernel.cu": {"src_sha": "2acc16b6708d6524", "bytes_per_launch": 2.914e9},
-    # wcsr_uniform at its benchmark size (profiles/wcsr_kernel_wcsr_uniform.md)
+    # wcsr_uniform at its benchmark size
     "wcsr_kernel.cu": {"src_sha": "4a2ab33295fb992a", "bytes_per_launch": 1.086e8},
 }
 
@@ -515,6 +515,9 @@ def main():
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.gpus != world:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}: run N > 1 GPUs under "
+                         "python -m torch.distributed.run --nproc-per-node N")
     if args.sweep is not None:
         run_sweep(args)
         return

@@ -478,12 +478,9 @@ cudaError_t launch_variant(const CUtensorMap &tmA, const CUtensorMap &tmB, const
                            const BcsrParams &p, cudaStream_t stream) {
   using C_ = Cfg<BN, Q, NBUF, PARTS, MINB, OUT_BF16>;
   auto kern = bcsr_spmm_kernel<BN, Q, NBUF, PARTS, MINB, IN_BF16, OUT_BF16>;
-  static bool attr_set = false;  // per instantiation; the attribute is per device function
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};  // per instantiation, one bit per device
+  cudaError_t e = set_smem_limit_once(kern, C_::kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   const int64_t tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + BN - 1) / BN);
   const int64_t cap = p.max_ctas > 0 ? p.max_ctas : static_cast<int64_t>(MINB) * p.num_sms;
   const int64_t grid = tiles < cap ? tiles : cap;

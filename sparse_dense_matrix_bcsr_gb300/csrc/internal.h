@@ -5,7 +5,26 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace spmm {
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device: the attribute is held per device, so a process
+// that runs on several GPUs sets it on each.  `done` holds one bit per device
+// ordinal (below 64; others set it on every call).  Two host threads may both
+// set it; the call is idempotent.
+template <typename Kernel>
+cudaError_t set_smem_limit_once(Kernel kern, int bytes, std::atomic<uint64_t> &done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t{1} << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // BCSR SpMM: one CTA per (block row, tile of N columns).
 struct BcsrParams {

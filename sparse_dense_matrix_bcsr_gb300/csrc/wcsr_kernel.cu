@@ -629,14 +629,11 @@ template <int NACC, int Q, int PW, int MINB, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_variant(const WcsrParams &p, cudaStream_t stream) {
   using C_ = Cfg<NACC, Q, PW, MINB>;
   auto kern = wcsr_spmm_kernel<NACC, Q, PW, MINB, IN_BF16, OUT_BF16>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};  // per instantiation, one bit per device
+  cudaError_t e = set_smem_limit_once(kern, C_::kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, p.grid * sizeof(int32_t), stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
                                                                C_::kBN);
@@ -657,9 +654,17 @@ cudaError_t launch_dtypes(const WcsrParams &p, bool in_bf16, bool out_bf16, cuda
 // each thread walks a contiguous run of windows, counts their stages
 // (ceil(P_w / 64), at least 1), a block-wide exclusive scan places the runs,
 // and the threads write their stages.  The total goes to *n_stages.
+//
+// The caller's window_row_ptr is checked first, since the host cannot read
+// it: window_row_ptr[0] == 0, entries non-decreasing and multiples of 16 (the
+// value copies are 16-byte cp.async and the MMA takes 16 columns per step),
+// window_row_ptr[n_windows] == p_total, and the stage count within the
+// scratch's stage area.  On any failure no stage is written, *n_stages is 0
+// (the product kernel then does no work and C is left as it was) and
+// kDevIndex is set in the scratch's status word.
 __global__ void __launch_bounds__(1024)
-    wcsr_noalloc_stages_kernel(const int64_t *window_row_ptr, int64_t n_windows, WcsrStage *stages,
-                               int64_t *n_stages, uint32_t *status) {
+    wcsr_noalloc_stages_kernel(const int64_t *window_row_ptr, int64_t n_windows, int64_t p_total,
+                               WcsrStage *stages, int64_t *n_stages, uint32_t *status) {
   __shared__ int64_t part[1024];
   const int t = threadIdx.x;
   if (t == 0) *status = 0;  // the scratch keeps the previous call's contents
@@ -667,8 +672,14 @@ __global__ void __launch_bounds__(1024)
   const int64_t w0 = t * per < n_windows ? t * per : n_windows;
   const int64_t w1 = w0 + per < n_windows ? w0 + per : n_windows;
   int64_t cnt = 0;
-  for (int64_t w = w0; w < w1; ++w) {
-    const int64_t pw = window_row_ptr[w + 1] - window_row_ptr[w];
+  bool bad = (t == 0 && window_row_ptr[0] != 0) || (t == 1023 && window_row_ptr[n_windows] != p_total);
+  for (int64_t w = w0; w < w1 && !bad; ++w) {
+    const int64_t b = window_row_ptr[w], e = window_row_ptr[w + 1];
+    if (e < b || (e & 15) != 0) {
+      bad = true;
+      break;
+    }
+    const int64_t pw = e - b;
     cnt += pw > 0 ? (pw + kKC - 1) / kKC : 1;
   }
   part[t] = cnt;
@@ -678,6 +689,14 @@ __global__ void __launch_bounds__(1024)
     __syncthreads();
     part[t] += v;
     __syncthreads();
+  }
+  // every thread sees the same total; a bad entry anywhere rejects the call
+  if (__syncthreads_or(bad ? 1 : 0) || part[1023] > kNoallocMaxStages) {
+    if (t == 0) {
+      *n_stages = 0;
+      *status = kDevIndex;
+    }
+    return;
   }
   int64_t pos = part[t] - cnt;
   for (int64_t w = w0; w < w1; ++w) {
@@ -699,14 +718,11 @@ template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_noalloc_variant(const WcsrParams &p, cudaStream_t stream) {
   using C_ = Cfg<NACC, Q, 4, 1>;
   auto kern = wcsr_spmm_kernel<NACC, Q, 4, 1, IN_BF16, OUT_BF16, true>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C_::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> smem_set{0};  // per instantiation, one bit per device
+  cudaError_t e = set_smem_limit_once(kern, C_::kSmemBytes, smem_set);
+  if (e != cudaSuccess) return e;
   kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, p.grid * sizeof(int32_t), stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
                                                                C_::kBN);
@@ -755,7 +771,7 @@ cudaError_t launch_wcsr_noalloc(WcsrParams p, const int64_t *window_row_ptr, int
   p.n_stages_dev = reinterpret_cast<int64_t *>(tail);
   p.status = reinterpret_cast<uint32_t *>(tail + 8);  // bounded-wait timeouts (not reported by this entry point)
   p.grid = num_sms < kNoallocMaxCtas ? num_sms : kNoallocMaxCtas;
-  wcsr_noalloc_stages_kernel<<<1, 1024, 0, stream>>>(window_row_ptr, n_windows, stages,
+  wcsr_noalloc_stages_kernel<<<1, 1024, 0, stream>>>(window_row_ptr, n_windows, p.P_total, stages,
                                                       reinterpret_cast<int64_t *>(tail), p.status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

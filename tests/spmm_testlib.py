@@ -64,3 +64,32 @@ def assert_parity(C_gpu, C_ref, S_ref, what=""):
     ok, worst = oracle.within_tolerance(C_gpu, C_ref, S_ref)
     assert ok, f"{what}: |err| exceeds 4*2^-8*S + 1e-6 (worst err/bound = {worst:.3g})"
     return worst
+
+
+def stratified_positions(m, n, group_rows, nsamp_random=0, seed=0, strata_cols=128):
+    """Sample positions of C: one random (row, column) inside every
+    (row group, column stratum) cell -- a BCSR block row or WCSR window by a
+    strip of `strata_cols` columns, finer than either kernel's column tile --
+    plus `nsamp_random` uniform positions.  Every tile the kernels write is
+    therefore sampled at least once."""
+    rng = np.random.default_rng(seed)
+    ng = -(-m // group_rows)
+    nc = -(-n // strata_cols)
+    g = np.repeat(np.arange(ng, dtype=np.int64), nc)
+    c = np.tile(np.arange(nc, dtype=np.int64), ng)
+    r0 = g * group_rows
+    rows = r0 + (rng.random(len(g)) * np.minimum(group_rows, m - r0)).astype(np.int64)
+    c0 = c * strata_cols
+    cols = c0 + (rng.random(len(c)) * np.minimum(strata_cols, n - c0)).astype(np.int64)
+    if nsamp_random:
+        rows = np.concatenate([rows, rng.integers(0, m, nsamp_random)])
+        cols = np.concatenate([cols, rng.integers(0, n, nsamp_random)])
+    return rows, cols
+
+
+def sampled_parity(w, C_dev, rows, cols):
+    """Compare C_dev (a torch tensor on the GPU) with the oracle at (rows, cols)."""
+    import torch
+    Cs = C_dev[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
+    ref, S = oracle.spmm_csr_sample(w.m, w.k, w.row_ptr, w.col_idx, w.vals, ocode(w.dtype), w.B(), rows, cols)
+    return assert_parity(Cs, ref, S, f"{w.name} ({len(rows)} sampled outputs)")

@@ -9,7 +9,8 @@ import pytest
 
 import oracle
 import spmm_workloads as W
-from spmm_testlib import assert_parity, ensure_library, ocode, run_library
+from spmm_testlib import (assert_parity, ensure_library, ocode, run_library, sampled_parity,
+                          stratified_positions)
 
 pytestmark = pytest.mark.gpu
 
@@ -115,27 +116,35 @@ def test_bcsr_all_zero_matrix_writes_zeros():
 
 
 def sampled_check(w, nsamp=6000, seed=0):
+    """Full-size workload: C fully written (no NaN left), then one sampled
+    output in every (block row, 128-column strip) cell plus nsamp uniform
+    ones compared with the oracle."""
     import torch
     outs, info = run_library("bcsr", w.m, w.k, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.B(),
                              keep_device=True)
     C = outs[0]
     assert not torch.isnan(C).any().item(), "C not fully written"
-    rng = np.random.default_rng(seed)
-    rows = rng.integers(0, w.m, nsamp)
-    cols = rng.integers(0, w.n, nsamp)
-    Cs = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
-    ref, S = oracle.spmm_csr_sample(w.m, w.k, w.row_ptr, w.col_idx, w.vals, ocode(w.dtype), w.B(), rows, cols)
-    assert_parity(Cs, ref, S, w.name)
-    return info
+    rows, cols = stratified_positions(w.m, w.n, 64, nsamp, seed)
+    sampled_parity(w, C, rows, cols)
+    return info, C
 
 
 @pytest.mark.parametrize("sp", W.BCSR_SWEEP_SPARSITY)
-def test_bcsr_sweep_full_size_sampled(sp):
-    for n in (8, 256):
-        sampled_check(W.bcsr_sweep(sp, n))
+@pytest.mark.parametrize("n", W.SWEEP_N)
+def test_bcsr_sweep_full_size_sampled(sp, n):
+    sampled_check(W.bcsr_sweep(sp, n))
 
 
-def test_bcsr_weight_like_full_size_sampled():
+def test_bcsr_weight_like_full_size():
+    """bcsr_weight at its full size (N = 65536, C bf16): a sample in every
+    (block row, 128-column strip) cell, and two whole 256-column bands of C
+    (an interior one and the last one) compared element by element."""
     w = W.bcsr_weight()
-    info = sampled_check(w, nsamp=20000)
+    info, C = sampled_check(w, nsamp=20000)
     assert info["n_units"] == 1658
+    B = w.B()
+    for n0 in (256 * 97, w.n - 256):
+        band = np.ascontiguousarray(B[:, n0:n0 + 256])
+        ref, S = oracle.spmm_csr(w.m, w.k, w.row_ptr, w.col_idx, w.vals, ocode(w.dtype), band)
+        got = C[:, n0:n0 + 256].double().cpu().numpy()
+        assert_parity(got, ref, S, f"{w.name} columns {n0}..{n0 + 255}")

@@ -5,7 +5,8 @@ import pytest
 
 import oracle
 import spmm_workloads as W
-from spmm_testlib import assert_parity, ensure_library, ocode, run_library
+from spmm_testlib import (assert_parity, ensure_library, ocode, run_library, sampled_parity,
+                          stratified_positions)
 
 pytestmark = pytest.mark.gpu
 
@@ -100,17 +101,16 @@ def test_wcsr_one_nonzero_per_row_exact():
 
 
 def sampled_check(w, nsamp=8000, seed=0, max_ctas=None):
+    """Full-size workload: C fully written (no NaN left), then one sampled
+    output in every (window, 128-column strip) cell plus nsamp uniform ones
+    compared with the oracle."""
     import torch
     outs, info = run_library("wcsr", w.m, w.k, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.B(),
                              keep_device=True, max_ctas=max_ctas)
     C = outs[0]
     assert not torch.isnan(C).any().item(), "C not fully written"
-    rng = np.random.default_rng(seed)
-    rows = rng.integers(0, w.m, nsamp)
-    cols = rng.integers(0, w.n, nsamp)
-    Cs = C[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()].double().cpu().numpy()
-    ref, S = oracle.spmm_csr_sample(w.m, w.k, w.row_ptr, w.col_idx, w.vals, ocode(w.dtype), w.B(), rows, cols)
-    assert_parity(Cs, ref, S, w.name)
+    rows, cols = stratified_positions(w.m, w.n, 16, nsamp, seed)
+    sampled_parity(w, C, rows, cols)
     return info
 
 
@@ -120,13 +120,15 @@ def test_wcsr_uniform_full_size():
     assert info["n_groups"] == 1024
 
 
-def test_wcsr_irregular_full_size_sampled():
+def test_wcsr_irregular_full_size():
+    """The irregular workload at full size (262144 rows, N = 128), every
+    element of C compared with the oracle."""
     w = W.wcsr_irregular()
-    info = sampled_check(w, nsamp=20000)
+    outs, info = full_check(w.m, w.k, w.n, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.B())
     assert info["n_split_windows"] > 0  # windows cut between CTAs
 
 
 @pytest.mark.parametrize("dens", W.WCSR_SWEEP_DENSITY)
-def test_wcsr_sweep_full_size_sampled(dens):
-    for n in (8, 256):
-        sampled_check(W.wcsr_sweep(dens, n))
+@pytest.mark.parametrize("n", W.SWEEP_N)
+def test_wcsr_sweep_full_size_sampled(dens, n):
+    sampled_check(W.wcsr_sweep(dens, n))

@@ -3,11 +3,13 @@ device memory when they run it (their memory comes from their own pool, or
 cudaMalloc is off limits at that point).  Its work list and partial sums
 live in a static device array instead of memory the handle allocates.
 
-Checked through the C ABI against the ordinary entry point (spmm_run on a
-handle) on two calls in a row, since the static array keeps the previous
-call's contents, within the same per-element bound the other tests use,
-|dC| <= 4*2^-8*sum|a*b| + 1e-6 with the sum from the CPU oracle.  This file
-is collected last so that a failure here comes after every other test."""
+Checked through the C ABI on two calls in a row (the static array keeps the
+previous call's contents), element by element against the CPU oracle's C
+within the bound every parity test uses, |dC| <= 4*2^-8*sum|a*b| + 1e-6, and
+against the ordinary entry point (spmm_run on a handle) within the same
+bound.  A window_row_ptr that breaks the format's rules is turned away on
+the device without touching C.  This file is collected last so that a
+failure here comes after every other test."""
 import numpy as np
 import pytest
 
@@ -59,8 +61,9 @@ def test_noalloc_matches_handle_on_two_calls(S, name, out_t):
     finally:
         S.spmm_destroy(h)
     ref = ref.double().cpu().numpy()
-    _, Sabs = oracle.spmm_csr(m, k, rp, ci, vals, oracle.BF16, B)
+    C_orc, Sabs = oracle.spmm_csr(m, k, rp, ci, vals, oracle.BF16, B)
     bound = 4.0 * 2.0 ** -8 * Sabs + 1e-6
+    assert np.all(np.abs(ref - C_orc) <= bound), "spmm_run differs from the oracle"
     d_ptr = torch.from_numpy(ptr).cuda()
     d_idx = torch.from_numpy(np.ascontiguousarray(idx) if len(idx) else np.zeros(1, np.int32)).cuda()
     d_val = torch.from_numpy(np.ascontiguousarray(values).view(np.int16).reshape(-1)).cuda()
@@ -72,7 +75,48 @@ def test_noalloc_matches_handle_on_two_calls(S, name, out_t):
         torch.cuda.synchronize()
         got = C.double().cpu().numpy()
         assert not np.isnan(got).any(), f"call {call}: C not fully written"
-        assert np.all(np.abs(got - ref) <= bound), f"call {call}: differs from spmm_run beyond the bound"
+        assert np.all(np.abs(got - C_orc) <= bound), f"call {call}: differs from the oracle beyond the bound"
+        assert np.all(np.abs(got - ref) <= 2 * bound), f"call {call}: differs from spmm_run beyond the bound"
+
+
+@pytest.mark.parametrize("defect", ["not_multiple_of_16", "decreasing", "last_not_p_total", "first_not_zero"])
+def test_noalloc_turns_away_a_bad_window_row_ptr(S, defect):
+    """A window_row_ptr of the right length whose entries break the format
+    (entry not a multiple of 16, decreasing, last entry != p_total, first
+    entry != 0): the stage-list kernel finds it before any work is listed, so
+    C keeps its contents, and a following valid call still works."""
+    import torch
+    m, k, n, rp, ci, vals, B = _case("tiny")
+    h = S.spmm_wcsr_create(m, k, rp, ci, vals, "bf16", "f32")
+    try:
+        ptr, idx, values = S.spmm_export_format(h)
+    finally:
+        S.spmm_destroy(h)
+    bad = ptr.copy()
+    if defect == "not_multiple_of_16":
+        bad[1] += 8
+    elif defect == "decreasing":
+        bad[1], bad[2] = bad[2] + 16, bad[1]
+    elif defect == "last_not_p_total":
+        bad[-1] -= 16
+    else:
+        bad[0] = 16
+    assert len(bad) == len(ptr)
+    d_idx = torch.from_numpy(np.ascontiguousarray(idx)).cuda()
+    d_val = torch.from_numpy(np.ascontiguousarray(values).view(np.int16).reshape(-1)).cuda()
+    dB = to_device_bits(B, "bf16")
+    stream = torch.cuda.current_stream().cuda_stream
+    C = torch.full((m, n), 7.0, dtype=torch.float32, device="cuda")
+    S.spmm_wcsr_run_noalloc(torch.from_numpy(bad).cuda().data_ptr(), d_idx.data_ptr(), d_val.data_ptr(), m, k,
+                            len(idx), "bf16", "f32", dB.data_ptr(), C.data_ptr(), n, stream)
+    torch.cuda.synchronize()
+    assert bool((C == 7.0).all().item()), "C was written although window_row_ptr was rejected"
+    d_ptr = torch.from_numpy(ptr).cuda()
+    S.spmm_wcsr_run_noalloc(d_ptr.data_ptr(), d_idx.data_ptr(), d_val.data_ptr(), m, k, len(idx), "bf16", "f32",
+                            dB.data_ptr(), C.data_ptr(), n, stream)
+    torch.cuda.synchronize()
+    C_orc, Sabs = oracle.spmm_csr(m, k, rp, ci, vals, oracle.BF16, B)
+    assert np.all(np.abs(C.double().cpu().numpy() - C_orc) <= 4.0 * 2.0 ** -8 * Sabs + 1e-6)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(S):
