@@ -36,11 +36,21 @@
 // A block row without stored blocks still passes through the pipeline as
 // one stage without loads, so its rows of C are written (zeros) by the same
 // TMA stores.
+//
+// Split schedule (BcsrParams::split_grid > 0), for problems with too few
+// tiles to keep every SM busy (the paper's static grid of one CTA per tile,
+// Section III-F, leaves SMs idle there): the stages of all tiles are listed
+// tile after tile, and CTA c takes an equal contiguous share of that list, so
+// a tile's blocks may be spread over several CTAs.  A CTA's run of stages of
+// one tile is a "segment"; a segment holding the whole tile is stored to C as
+// usual, a cut one is written as fp32 partial sums to the CTA's workspace
+// slot and split_reduce_kernel adds the slots of each cut tile in CTA order.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "split_reduce.cuh"
 
 namespace spmm {
 namespace {
@@ -56,10 +66,14 @@ constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kBoxBytes = 2048;               // one TMA store box of C in shared memory
 
 // Stage record flags (producer -> MMA) and accumulator record flags (MMA -> epilogue).
-constexpr int32_t kRecFirst = 1;  // first stored block of its tile
-constexpr int32_t kRecLast = 2;   // last stage of its tile
-constexpr int32_t kRecEmpty = 4;  // block row without stored blocks: no loads, no MMA, C rows = 0
-constexpr int32_t kRecEnd = 8;    // no more tiles
+constexpr int32_t kRecFirst = 1;       // first stage of a segment: the MMA overwrites the accumulator
+constexpr int32_t kRecLast = 2;        // last stage of a segment: the accumulator goes to the epilogue
+constexpr int32_t kRecEmpty = 4;       // block row without stored blocks: no loads, no MMA, C rows = 0
+constexpr int32_t kRecEnd = 8;         // no more tiles
+constexpr int32_t kRecTileFirst = 16;  // the tile's first stage
+constexpr int32_t kRecTileLast = 32;   // the tile's last stage
+constexpr int32_t kRecAtF0 = 64;       // the CTA's first stage (split schedule: partial slot 2c, else 2c + 1)
+constexpr int32_t kRecWhole = kRecTileFirst | kRecTileLast;
 
 struct TileRec {
   int32_t br;     // block row
@@ -164,6 +178,10 @@ __global__ void __launch_bounds__(kThreads, MINB)
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
+    if (p.split_grid > 0) {  // this CTA's partial-sum records (overwritten below when used)
+      p.partials[2 * blockIdx.x] = PartialRec{-1, 0, 0, 0};
+      p.partials[2 * blockIdx.x + 1] = PartialRec{-1, 0, 0, 0};
+    }
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmC);
@@ -194,62 +212,136 @@ __global__ void __launch_bounds__(kThreads, MINB)
         phase ^= 1u;
       }
     };
-    // Block-row extent of the first tile; the next tile's is loaded while
-    // this one's stages are issued.
-    int br = 0, nt = 0;
-    int64_t jb = 0, je = 0;
-    if (static_cast<int64_t>(blockIdx.x) < n_tiles) {
-      tile_coords(blockIdx.x, p.n_block_rows, n_col_tiles, br, nt);
-      jb = p.block_row_ptr[br];
-      je = p.block_row_ptr[br + 1];
-    }
-    for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-      int br_n = 0, nt_n = 0;
-      int64_t jb_n = 0, je_n = 0;
-      const int64_t tn = t + gridDim.x;
-      if (tn < n_tiles) {
-        tile_coords(tn, p.n_block_rows, n_col_tiles, br_n, nt_n);
-        jb_n = p.block_row_ptr[br_n];
-        je_n = p.block_row_ptr[br_n + 1];
+    // One stage: its tile record (released to the MMA thread by the arrive)
+    // and, unless the block row is empty, the TMA loads of block j and of the
+    // 64 rows of B it multiplies (block column bcol) for column tile nt.
+    auto issue = [&](int br, int nt, int64_t j, int32_t bcol, int32_t flags) {
+      if (lane == 0) {
+        tile_rec[stage] = TileRec{br, nt, flags, 0};
+        const uint32_t fb = full0 + 8 * stage;
+        if (flags & kRecEmpty) {
+          mbar_arrive(fb);
+        } else {
+          const int n0 = nt * C_::kBN;
+          const int nch = min(C_::kChunks, (p.N - n0 + 63) / 64);
+          const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
+          mbar_arrive_expect_tx(fb, kBlkBytes + nch * kChunkBytes);
+          tma_load_2d(st, &tmA, fb, 0, static_cast<int32_t>(j * kBlk));
+          for (int c = 0; c < nch; ++c)
+            tma_load_2d(st + kBlkBytes + c * kChunkBytes, &tmB, fb, n0 + c * 64, bcol * kBlk);
+        }
       }
-      const int n0 = nt * C_::kBN;
-      const int nch = min(C_::kChunks, (p.N - n0 + 63) / 64);
-      if (jb == je) {
+      advance();
+    };
+    if (p.split_grid > 0) {
+      // Split schedule: stages of all tiles in tile order (tile_coords), a
+      // tile's stages being its block row's blocks in order (one empty stage
+      // for a block row without blocks); this CTA takes [f0, f1).  Within a
+      // group of kGroupN column tiles, tile (br, i) starts at stage
+      // gsz * P[br] + i * len(br) of the group, P = stage_row_ptr.
+      const int nbr = p.n_block_rows;
+      const int64_t s_all = p.stage_row_ptr[nbr];  // stages per column tile
+      const int64_t total = s_all * n_col_tiles;
+      const int64_t f0 = total * blockIdx.x / gridDim.x;
+      const int64_t f1 = total * (blockIdx.x + 1) / gridDim.x;
+      const int64_t n_blocks = p.block_row_ptr[nbr];
+      const int64_t span = s_all * kGroupN;
+      int g = static_cast<int>(f0 / span);
+      int64_t r = f0 - g * span;
+      int gsz = min(kGroupN, n_col_tiles - g * kGroupN);
+      int lo = 0, hi = nbr - 1;  // last block row with gsz * P[br] <= r
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (gsz * p.stage_row_ptr[mid] <= r) lo = mid;
+        else hi = mid - 1;
+      }
+      int br = lo;
+      int64_t len = p.stage_row_ptr[br + 1] - p.stage_row_ptr[br];
+      r -= gsz * p.stage_row_ptr[br];
+      int i = static_cast<int>(r / len);
+      int64_t j = r - i * len;  // stage within the tile
+      int64_t jb = p.block_row_ptr[br], je = p.block_row_ptr[br + 1];
+      // the warp holds 32 consecutive block-column indices from `cbase`
+      int64_t cbase = -64;
+      int32_t cval = 0;
+      for (int64_t f = f0; f < f1; ++f) {
+        const bool empty = je == jb;
+        int32_t bcol = 0;
+        if (!empty) {
+          const int64_t x = jb + j;
+          if (x < cbase || x >= cbase + 32) {
+            cbase = x;
+            cval = x + lane < n_blocks ? p.block_col_idx[x + lane] : 0;
+          }
+          bcol = __shfl_sync(0xffffffffu, cval, static_cast<int>(x - cbase));
+        }
         ok = claim();
         if (!ok) break;
-        if (lane == 0) {
-          tile_rec[stage] = TileRec{br, nt, kRecFirst | kRecLast | kRecEmpty, 0};
-          mbar_arrive(full0 + 8 * stage);  // releases the record
+        const bool tfirst = j == 0, tlast = j == len - 1;
+        const int32_t flags = (tfirst || f == f0 ? kRecFirst : 0) | (tlast || f == f1 - 1 ? kRecLast : 0) |
+                              (tfirst ? kRecTileFirst : 0) | (tlast ? kRecTileLast : 0) | (f == f0 ? kRecAtF0 : 0) |
+                              (empty ? kRecEmpty : 0);
+        issue(br, g * kGroupN + i, jb + j, bcol, flags);
+        if (++j == len) {  // next tile
+          j = 0;
+          if (++i == gsz) {
+            i = 0;
+            if (++br == nbr) {
+              br = 0;
+              ++g;
+              gsz = min(kGroupN, n_col_tiles - g * kGroupN);
+            }
+            if (f + 1 < f1) {
+              jb = p.block_row_ptr[br];
+              je = p.block_row_ptr[br + 1];
+              len = p.stage_row_ptr[br + 1] - p.stage_row_ptr[br];
+            }
+          }
         }
-        advance();
       }
-      for (int64_t jbase = jb; jbase < je && ok; jbase += 32) {
-        // The warp loads the next 32 block-column indices at once.
-        const int64_t jl = jbase + lane;
-        const int32_t my_col = jl < je ? p.block_col_idx[jl] : 0;
-        const int cnt = (je - jbase) < 32 ? static_cast<int>(je - jbase) : 32;
-        for (int i = 0; i < cnt; ++i) {
-          const int32_t bcol = __shfl_sync(0xffffffffu, my_col, i);
+    } else {
+      // Block-row extent of the first tile; the next tile's is loaded while
+      // this one's stages are issued.
+      int br = 0, nt = 0;
+      int64_t jb = 0, je = 0;
+      if (static_cast<int64_t>(blockIdx.x) < n_tiles) {
+        tile_coords(blockIdx.x, p.n_block_rows, n_col_tiles, br, nt);
+        jb = p.block_row_ptr[br];
+        je = p.block_row_ptr[br + 1];
+      }
+      for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        int br_n = 0, nt_n = 0;
+        int64_t jb_n = 0, je_n = 0;
+        const int64_t tn = t + gridDim.x;
+        if (tn < n_tiles) {
+          tile_coords(tn, p.n_block_rows, n_col_tiles, br_n, nt_n);
+          jb_n = p.block_row_ptr[br_n];
+          je_n = p.block_row_ptr[br_n + 1];
+        }
+        if (jb == je) {
           ok = claim();
           if (!ok) break;
-          if (lane == 0) {
-            const int64_t j = jbase + i;
-            const int32_t flags = (j == jb ? kRecFirst : 0) | (j == je - 1 ? kRecLast : 0);
-            tile_rec[stage] = TileRec{br, nt, flags, 0};
-            const uint32_t fb = full0 + 8 * stage;
-            const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
-            mbar_arrive_expect_tx(fb, kBlkBytes + nch * kChunkBytes);  // also releases the record
-            tma_load_2d(st, &tmA, fb, 0, static_cast<int32_t>(j * kBlk));
-            for (int c = 0; c < nch; ++c)
-              tma_load_2d(st + kBlkBytes + c * kChunkBytes, &tmB, fb, n0 + c * 64, bcol * kBlk);
-          }
-          advance();
+          issue(br, nt, 0, 0, kRecFirst | kRecLast | kRecWhole | kRecEmpty);
         }
+        for (int64_t jbase = jb; jbase < je && ok; jbase += 32) {
+          // The warp loads the next 32 block-column indices at once.
+          const int64_t jl = jbase + lane;
+          const int32_t my_col = jl < je ? p.block_col_idx[jl] : 0;
+          const int cnt = (je - jbase) < 32 ? static_cast<int>(je - jbase) : 32;
+          for (int i = 0; i < cnt; ++i) {
+            const int32_t bcol = __shfl_sync(0xffffffffu, my_col, i);
+            ok = claim();
+            if (!ok) break;
+            const int64_t j = jbase + i;
+            issue(br, nt, j, bcol,
+                  (j == jb ? kRecFirst | kRecTileFirst : 0) | (j == je - 1 ? kRecLast | kRecTileLast : 0));
+          }
+        }
+        br = br_n;
+        nt = nt_n;
+        jb = jb_n;
+        je = je_n;
       }
-      br = br_n;
-      nt = nt_n;
-      jb = jb_n;
-      je = je_n;
     }
     if (ok) {
       // end marker for the MMA thread
@@ -275,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     uint32_t stage = 0, phase = 0;
     uint32_t tcount = 0;  // tiles finished
     uint32_t buf = 0;
+    int32_t seg_flags = 0;  // kRecTileFirst / kRecAtF0 of the current segment's first stage
     bool ok = true;
     while (true) {
       ok = mbar_wait_warp(full0 + 8 * stage, phase, p.wait_limit_ns);
@@ -288,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         ok = __shfl_sync(0xffffffffu, r && !*abort_flag, 0);
         if (!ok) break;
         tc_fence_after_sync();
+        seg_flags = rec.flags & (kRecTileFirst | kRecAtF0);
       }
       if (rec.flags & kRecEnd) {
         if (leader) {
@@ -325,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
         if (rec.flags & kRecLast) {
           acc_rec[buf].br = rec.br;
           acc_rec[buf].nt = rec.nt;
-          acc_rec[buf].flags = rec.flags & kRecEmpty;
+          acc_rec[buf].flags = (rec.flags & (kRecEmpty | kRecTileLast)) | seg_flags;
           mbar_arrive(accf0 + 8 * buf);  // releases the record
           umma_commit(accf0 + 8 * buf);  // arrives when the tile's MMAs are done
         }
@@ -378,6 +472,44 @@ __global__ void __launch_bounds__(kThreads, MINB)
       }
       const int32_t flags = acc_rec[buf].flags;
       if (flags & kRecEnd) break;
+      if ((flags & kRecWhole) != kRecWhole) {
+        // A segment of a tile cut between CTAs (split schedule): its fp32
+        // partial sums go to this CTA's workspace slot (64 rows x BN columns,
+        // row-major) for split_reduce_kernel, with a record naming the tile.
+        const int slot = 2 * static_cast<int>(blockIdx.x) + ((flags & kRecAtF0) ? 0 : 1);
+        float *ws = p.workspace + static_cast<int64_t>(slot) * kBcsrSlotFloats;
+        const int br_s = acc_rec[buf].br;
+        const int nt_s = acc_rec[buf].nt;
+        const int row = (C_::kWS ? (sp & 1) * 32 : sp * 16) + lane;
+        const int col0 = C_::kWS ? (sp >> 1) * C_::kWarpCols : 0;
+        tc_fence_after_sync();
+        const uint32_t tbase = tmem + (static_cast<uint32_t>(sp * 32) << 16) + buf * C_::kAccCols;
+#pragma unroll 1
+        for (int g = 0; g < C_::kWarpCols / 16; ++g) {
+          uint32_t v[16];
+          tmem_ld_32x32b_x16(tbase + g * 16, v);
+          tmem_ld_wait();
+          if (row_lane && nt_s * BN + col0 + g * 16 < p.N) {
+            float4 *dst = reinterpret_cast<float4 *>(ws + row * BN + col0 + g * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          if (warp == kEpiWarp0)
+            p.partials[slot] = PartialRec{br_s, nt_s,
+                                          ((flags & kRecTileFirst) ? kStageFirst : 0) |
+                                              ((flags & kRecTileLast) ? kStageLast : 0),
+                                          0};
+          mbar_arrive(acce0 + 8 * buf);
+        }
+        ++tcount;
+        continue;
+      }
       const bool zero = (flags & kRecEmpty) != 0;
       const int row0 = acc_rec[buf].br * kBlk + (C_::kWS ? (sp & 1) * 32 : sp * 16);
       const int n0 = acc_rec[buf].nt * BN + (C_::kWS ? (sp >> 1) * C_::kWarpCols : 0);  // this warp's first column
@@ -481,10 +613,19 @@ cudaError_t launch_variant(const CUtensorMap &tmA, const CUtensorMap &tmB, const
   static std::atomic<uint64_t> smem_set{0};  // per instantiation, one bit per device
   cudaError_t e = set_smem_limit_once(kern, C_::kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
-  const int64_t tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + BN - 1) / BN);
-  const int64_t cap = p.max_ctas > 0 ? p.max_ctas : static_cast<int64_t>(MINB) * p.num_sms;
-  const int64_t grid = tiles < cap ? tiles : cap;
+  int64_t grid;
+  if (p.split_grid > 0) {
+    grid = p.split_grid;
+  } else {
+    const int64_t tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + BN - 1) / BN);
+    const int64_t cap = p.max_ctas > 0 ? p.max_ctas : static_cast<int64_t>(MINB) * p.num_sms;
+    grid = tiles < cap ? tiles : cap;
+  }
   kern<<<static_cast<unsigned>(grid), kThreads, C_::kSmemBytes, stream>>>(tmA, tmB, tmC, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.split_grid == 0) return e;
+  split_reduce_kernel<kBlk, OUT_BF16><<<static_cast<unsigned>(2 * grid), 256, grid * sizeof(int32_t), stream>>>(
+      p.partials, p.workspace, kBcsrSlotFloats, BN, p.C, p.M, p.N, static_cast<int32_t>(grid), BN);
   return cudaGetLastError();
 }
 
@@ -497,23 +638,26 @@ cudaError_t launch_in(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUte
 
 }  // namespace
 
+int bcsr_tile_cols(int64_t N) { return bcsr_wide_tiles(N) ? 256 : 128; }
+
 cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const BcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream) {
   if (p.n_block_rows == 0 || p.N == 0) return cudaSuccess;
   // N <= 128: 128-column tiles (one plain MMA of N = 128 per k step), two
-  // accumulators, one CTA per SM.  Wider (bcsr_wide_tiles): 256-column tiles,
+  // accumulators; one CTA per SM with six stages, or, on the split schedule,
+  // two CTAs per SM with three.  Wider (bcsr_wide_tiles): 256-column tiles,
   // one weight-stationary MMA of N = 256 per k step, two accumulators of 128
-  // TMEM columns; with at least two tiles per SM two CTAs share each SM (two
-  // stages each), so one CTA's barrier handshakes overlap the other's MMAs
-  // and loads; with fewer tiles one CTA per SM runs four stages.  Epilogue
-  // parts are one 32-row x 64-byte store box (32 bf16 or 16 fp32 columns).
-  if (!bcsr_wide_tiles(p.N))
+  // TMEM columns, two CTAs per SM with two stages each, so one CTA's barrier
+  // handshakes overlap the other's MMAs and loads (problems with fewer than
+  // two tiles per SM take the split schedule).  Epilogue parts are one
+  // 32-row x 64-byte store box (32 bf16 or 16 fp32 columns).
+  if (!bcsr_wide_tiles(p.N)) {
+    if (p.split_grid > 0)
+      return out_bf16 ? launch_in<128, 3, 2, 2, 2, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                      : launch_in<128, 3, 2, 2, 2, false>(tmA, tmB, tmC, p, in_bf16, stream);
     return out_bf16 ? launch_in<128, 6, 2, 2, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
                     : launch_in<128, 6, 2, 2, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
-  const int64_t tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + 255) / 256);
-  if (tiles < 2ll * p.num_sms)
-    return out_bf16 ? launch_in<256, 4, 2, 4, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
-                    : launch_in<256, 4, 2, 8, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
+  }
   return out_bf16 ? launch_in<256, 2, 2, 4, 2, true>(tmA, tmB, tmC, p, in_bf16, stream)
                   : launch_in<256, 2, 2, 8, 2, false>(tmA, tmB, tmC, p, in_bf16, stream);
 }

@@ -26,25 +26,61 @@ cudaError_t set_smem_limit_once(Kernel kern, int bytes, std::atomic<uint64_t> &d
   return e;
 }
 
-// BCSR SpMM: one CTA per (block row, tile of N columns).
+// Flags of a stage / segment: it holds the first and/or the last stage of its
+// group (a WCSR window, or a BCSR block row x column tile).
+constexpr int32_t kStageFirst = 1;
+constexpr int32_t kStageLast = 2;
+
+// A partial sum written to a split workspace by a persistent CTA whose share
+// of stages cuts a group: the group (WCSR window or BCSR block row), its
+// column tile and whether it holds the group's first and/or last stage.
+struct PartialRec {
+  int32_t group;     // -1: slot unused in this run
+  int32_t col_tile;
+  int32_t flags;     // kStageFirst | kStageLast
+  int32_t pad_;
+};
+
+// BCSR SpMM.  Work unit ("tile") = one block row x one tile of N columns.
+// Default schedule: persistent CTAs take whole tiles round-robin.  Split
+// schedule (split_grid > 0, for problems with fewer tiles than about two per
+// SM): the tiles' stages (one per stored block, one for a block row without
+// blocks) are listed tile after tile and CTA c takes the equal contiguous
+// share [T*c/G, T*(c+1)/G); tiles cut between CTAs leave fp32 partial sums
+// that split_reduce_kernel adds in CTA order.
 struct BcsrParams {
   const int64_t *block_row_ptr;  // device, n_block_rows + 1
   const int32_t *block_col_idx;  // device, n_blocks
   const void *blocks;            // device, n_blocks x 64 x 64 row-major
+  const int64_t *stage_row_ptr;  // device, n_block_rows + 1: prefix sums of max(1, blocks of the block row)
   const void *B;                 // device, K x N row-major
   void *C;                       // device, M x N row-major
+  float *workspace;              // split schedule: 2 slots per CTA of 64 x 256 fp32
+  PartialRec *partials;          // split schedule: 2 records per CTA
   int64_t ldc;                   // row stride of C in elements (= N)
   int32_t M, N, K;
   int32_t n_block_rows;
   int32_t max_ctas;              // cap on the persistent grid (0: the kernel's default CTAs per SM)
   int32_t num_sms;
+  int32_t split_grid;            // > 0: split schedule over this many CTAs
   uint32_t *status;              // device status word
   uint64_t wait_limit_ns;        // bound of every mbarrier wait
 };
 
+// Split-schedule workspace: floats per slot (64 rows x 256 columns) and the
+// largest grid it is sized for, in CTAs per SM.
+constexpr int64_t kBcsrSlotFloats = 64 * 256;
+constexpr int kBcsrSplitCtasPerSm = 2;
+// The split schedule is used when the tiles number fewer than this many per
+// SM, and gives each CTA at least kBcsrSplitMinStages stages.
+constexpr int kBcsrSplitBelowTilesPerSm = 2;
+constexpr int kBcsrSplitMinStages = 4;
+
 // The BCSR kernel's C store boxes: for N <= 128, 16 rows x 128 bytes with the
 // 128-byte swizzle; wider, 32 rows x 64 bytes with the 64-byte swizzle.
 inline bool bcsr_wide_tiles(int64_t N) { return N > 128; }
+// Columns of C per BCSR tile at dense width N (256 for wide tiles, else 128).
+int bcsr_tile_cols(int64_t N);
 
 // in_bf16: A/B are bf16 (else fp16); out_bf16: C is bf16 (else fp32).
 // tmA covers the blocks array as [n_blocks*64 rows, 64 cols], tmB covers B as
@@ -61,17 +97,6 @@ struct WcsrStage {
   int32_t window;
   int32_t ncols;     // 0..64, a multiple of 16
   int32_t flags;     // kStageFirst | kStageLast
-};
-constexpr int32_t kStageFirst = 1;
-constexpr int32_t kStageLast = 2;
-
-// A partial sum written to the workspace: the window / column tile it
-// belongs to and whether it holds the window's first and/or last stage.
-struct WcsrPartial {
-  int32_t window;    // -1: slot unused in this run
-  int32_t col_tile;
-  int32_t flags;     // kStageFirst | kStageLast
-  int32_t pad_;
 };
 
 // One stage as a record of kWcsrPackBytes in device memory, fetched by one
@@ -92,7 +117,7 @@ struct WcsrParams {
   const void *B;                 // device, K x N row-major
   void *C;                       // device, M x N row-major
   float *workspace;              // device, 2 * grid x 16 x 256 fp32
-  WcsrPartial *partials;         // device, 2 * grid
+  PartialRec *partials;          // device, 2 * grid
   int64_t n_stages;
   int64_t P_total;
   int32_t M, N, K;

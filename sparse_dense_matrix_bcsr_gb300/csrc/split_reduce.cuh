@@ -1,0 +1,80 @@
+// split_reduce.cuh -- second pass of the equal-share schedules: adds the fp32
+// partial sums of the groups (a WCSR window, or a BCSR block row x column
+// tile) whose stages were cut between persistent CTAs, in CTA order, and
+// writes the group's rows of C.
+//
+// The paper adds such partials with atomicAdd ("AsyncSparse", Section III-C);
+// summing the slots in a fixed order instead makes every run bitwise equal.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace spmm {
+
+template <bool OUT_BF16>
+__device__ __forceinline__ void store_out(void *C, int64_t off, float v) {
+  if constexpr (OUT_BF16)
+    reinterpret_cast<__nv_bfloat16 *>(C)[off] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<float *>(C)[off] = v;
+}
+
+// Block b handles slot b.  Slot 2c holds CTA c's first segment (the one that
+// starts at the first stage of its share), slot 2c + 1 its last; a slot whose
+// record has kStageFirst but not kStageLast starts a cut group: this block
+// adds it and the first-segment slots of the following CTAs, in CTA order,
+// until the one whose record has kStageLast, and writes ROWS x bn values of C
+// at rows ROWS * group, columns bn * col_tile.  Slot s holds rows at
+// ws + s * slot_floats + row * ws_ld.  The list of contributing slots is found
+// once per block (dynamic shared memory, one int per CTA of the first pass);
+// each thread then sums four adjacent columns with independent loads.
+template <int ROWS, bool OUT_BF16>
+__global__ void __launch_bounds__(256)
+    split_reduce_kernel(const PartialRec *partials, const float *ws, int64_t slot_floats, int32_t ws_ld, void *C,
+                        int32_t M, int32_t N, int32_t grid, int32_t bn) {
+  extern __shared__ int32_t contrib[];  // [grid]
+  __shared__ int32_t n_contrib;
+  const int slot = blockIdx.x;
+  const PartialRec rec = partials[slot];
+  if (rec.group < 0 || !(rec.flags & kStageFirst) || (rec.flags & kStageLast)) return;
+  if (threadIdx.x == 0) {
+    int n = 0;
+    contrib[n++] = slot;
+    for (int c = slot / 2 + 1; c < grid; ++c) {
+      const PartialRec r = partials[2 * c];
+      if (r.group != rec.group || r.col_tile != rec.col_tile) break;
+      contrib[n++] = 2 * c;
+      if (r.flags & kStageLast) break;
+    }
+    n_contrib = n;
+  }
+  __syncthreads();
+  const int n = n_contrib;
+  const int n0 = rec.col_tile * bn;
+  const int width = min(bn, N - n0);  // a multiple of 8 (N is)
+  for (int e = 4 * threadIdx.x; e < ROWS * width; e += 4 * blockDim.x) {
+    const int q = e / width;
+    const int col = e - q * width;  // a multiple of 4
+    const int row = rec.group * ROWS + q;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < n; ++i) {
+      const float4 v =
+          *reinterpret_cast<const float4 *>(ws + static_cast<int64_t>(contrib[i]) * slot_floats + q * ws_ld + col);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    if (row < M) {
+      const int64_t o = static_cast<int64_t>(row) * N + n0 + col;
+      store_out<OUT_BF16>(C, o, acc.x);
+      store_out<OUT_BF16>(C, o + 1, acc.y);
+      store_out<OUT_BF16>(C, o + 2, acc.z);
+      store_out<OUT_BF16>(C, o + 3, acc.w);
+    }
+  }
+}
+
+}  // namespace spmm

@@ -126,13 +126,16 @@ struct spmm_handle_s {
   int64_t nc_cached = -1;
   CUtensorMap tm_C;
 
-  // WCSR work decomposition: stages of <= 64 packed columns, and the
-  // partial-sum workspace of windows cut between persistent CTAs
+  // Work decomposition.  WCSR: stages of <= 64 packed columns.  BCSR: the
+  // prefix sums of max(1, blocks) per block row (the split schedule's stage
+  // list).  Both: the partial-sum workspace of groups cut between persistent
+  // CTAs (BCSR: allocated only when the split schedule can be chosen).
   int32_t max_ctas = 0;  // 0: the kernels' default CTAs per SM
   int64_t n_stages = 0;
+  int64_t *d_stage_row_ptr = nullptr;
   uint8_t *d_stage_pack = nullptr;
   float *d_ws = nullptr;
-  spmm::WcsrPartial *d_partials = nullptr;
+  spmm::PartialRec *d_partials = nullptr;
   int64_t ws_slots = 0;
   std::vector<int32_t> stage_first;  // host copy of the stage list's first-stage flags (for statistics)
 
@@ -171,6 +174,7 @@ void free_handle(spmm_handle h) {
   cudaFree(h->d_idx);
   cudaFree(h->d_vals);
   cudaFree(h->d_stage_pack);
+  cudaFree(h->d_stage_row_ptr);
   cudaFree(h->d_partials);
   cudaFree(h->d_ws);
   cudaFree(h->d_status);
@@ -268,8 +272,45 @@ spmm_status build_stages(spmm_handle h, const std::vector<int64_t> &wptr, const 
   // Two partial slots per CTA, sized for the largest grid.
   h->ws_slots = 2 * static_cast<int64_t>(spmm::kWcsrMaxCtasPerSm) * std::max(h->num_sms, 1);
   CUDA_TRY(cudaMalloc(&h->d_ws, h->ws_slots * spmm::kWcsrSlotFloats * sizeof(float)), "cudaMalloc(workspace)");
-  CUDA_TRY(cudaMalloc(&h->d_partials, h->ws_slots * sizeof(spmm::WcsrPartial)), "cudaMalloc(partials)");
+  CUDA_TRY(cudaMalloc(&h->d_partials, h->ws_slots * sizeof(spmm::PartialRec)), "cudaMalloc(partials)");
   return SPMM_OK;
+}
+
+// BCSR split schedule: the stage list's prefix sums per block row
+// (max(1, blocks): a block row without blocks is one stage) and, when the
+// problem has few enough block rows that some N can select the schedule, its
+// partial-sum workspace.
+spmm_status build_bcsr_split(spmm_handle h, const std::vector<int64_t> &bptr) {
+  const int64_t nbr = h->n_groups;
+  std::vector<int64_t> srp(nbr + 1, 0);
+  for (int64_t r = 0; r < nbr; ++r) srp[r + 1] = srp[r] + std::max<int64_t>(1, bptr[r + 1] - bptr[r]);
+  h->n_stages = srp[nbr];
+  CUDA_TRY(cudaMalloc(&h->d_stage_row_ptr, srp.size() * sizeof(int64_t)), "cudaMalloc(stage row pointers)");
+  CUDA_TRY(cudaMemcpy(h->d_stage_row_ptr, srp.data(), srp.size() * sizeof(int64_t), cudaMemcpyHostToDevice),
+           "upload stage row pointers");
+  if (nbr < static_cast<int64_t>(spmm::kBcsrSplitBelowTilesPerSm) * std::max(h->num_sms, 1)) {
+    h->ws_slots = 2 * static_cast<int64_t>(spmm::kBcsrSplitCtasPerSm) * std::max(h->num_sms, 1);
+    CUDA_TRY(cudaMalloc(&h->d_ws, h->ws_slots * spmm::kBcsrSlotFloats * sizeof(float)), "cudaMalloc(workspace)");
+    CUDA_TRY(cudaMalloc(&h->d_partials, h->ws_slots * sizeof(spmm::PartialRec)), "cudaMalloc(partials)");
+  }
+  return SPMM_OK;
+}
+
+// BCSR grid of the split schedule at dense width N, or 0 for the default
+// schedule (whole tiles per CTA): the split schedule is taken when the tiles
+// number fewer than kBcsrSplitBelowTilesPerSm per SM, over up to
+// kBcsrSplitCtasPerSm CTAs per SM with at least kBcsrSplitMinStages stages
+// each (and at most the spmm_set_max_ctas cap).
+int32_t bcsr_split_grid(spmm_handle h, int64_t N) {
+  if (!h->d_ws) return 0;
+  const int64_t col_tiles = (N + spmm::bcsr_tile_cols(N) - 1) / spmm::bcsr_tile_cols(N);
+  const int64_t sms = std::max(h->num_sms, 1);
+  if (h->n_groups * col_tiles >= spmm::kBcsrSplitBelowTilesPerSm * sms) return 0;
+  const int64_t stages = h->n_stages * col_tiles;
+  int64_t g = std::min<int64_t>(spmm::kBcsrSplitCtasPerSm * sms,
+                                (stages + spmm::kBcsrSplitMinStages - 1) / spmm::kBcsrSplitMinStages);
+  if (h->max_ctas > 0) g = std::min<int64_t>(g, h->max_ctas);
+  return static_cast<int32_t>(std::max<int64_t>(1, g));
 }
 
 // Persistent grid of the WCSR kernel for N columns.
@@ -317,6 +358,10 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
     p.block_row_ptr = h->d_ptr;
     p.block_col_idx = h->d_idx;
     p.blocks = h->d_vals;
+    p.stage_row_ptr = h->d_stage_row_ptr;
+    p.workspace = h->d_ws;
+    p.partials = h->d_partials;
+    p.split_grid = bcsr_split_grid(h, N);
     p.B = B;
     p.C = C;
     p.ldc = N;
@@ -433,6 +478,7 @@ spmm_status spmm_bcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64
   h->n_units = f.n_units;
   h->stored = f.n_units * b_row * b_col;
   st = upload_common(h, f);
+  if (st == SPMM_OK) st = build_bcsr_split(h, f.ptr);
   if (st == SPMM_OK && b_row == 64 && b_col == 64)
     st = encode_2d(&h->tm_vals, h->d_vals, in_t == SPMM_BF16, static_cast<uint64_t>(std::max<int64_t>(f.n_units, 1) * 64),
                    64, 64, 64, 64);

@@ -52,6 +52,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "split_reduce.cuh"
 
 namespace spmm {
 namespace {
@@ -90,14 +91,6 @@ struct Cfg {
   static_assert(kVQ > kVLead * PW, "value slots must outlast the lead");
   static_assert(kAccBufs * kAccCols <= kTmemCols, "accumulator buffers exceed the TMEM allocation");
 };
-
-template <bool OUT_BF16>
-__device__ __forceinline__ void store_out(void *C, int64_t off, float v) {
-  if constexpr (OUT_BF16)
-    reinterpret_cast<__nv_bfloat16 *>(C)[off] = __float2bfloat16_rn(v);
-  else
-    reinterpret_cast<float *>(C)[off] = v;
-}
 
 __device__ __forceinline__ int4 shfl_int4(const int4 &v, int src) {
   return make_int4(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src),
@@ -150,8 +143,8 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
   const int64_t grid = NOALLOC ? (total < gridDim.x ? total : gridDim.x) : gridDim.x;
   if (NOALLOC && blockIdx.x >= grid) {
     if (threadIdx.x == 0) {
-      p.partials[2 * blockIdx.x] = WcsrPartial{-1, 0, 0, 0};
-      p.partials[2 * blockIdx.x + 1] = WcsrPartial{-1, 0, 0, 0};
+      p.partials[2 * blockIdx.x] = PartialRec{-1, 0, 0, 0};
+      p.partials[2 * blockIdx.x + 1] = PartialRec{-1, 0, 0, 0};
     }
     return;
   }
@@ -185,8 +178,8 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
     *abort_flag = 0;
     fence_barrier_init();
     // partial-sum records of this CTA (overwritten below when used)
-    p.partials[2 * blockIdx.x] = WcsrPartial{-1, 0, 0, 0};
-    p.partials[2 * blockIdx.x + 1] = WcsrPartial{-1, 0, 0, 0};
+    p.partials[2 * blockIdx.x] = PartialRec{-1, 0, 0, 0};
+    p.partials[2 * blockIdx.x + 1] = PartialRec{-1, 0, 0, 0};
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), C_::kTmemCols);
@@ -557,7 +550,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         }
       }
       if (!complete && threadIdx.x == 32 * (kMmaWarp + 1))
-        p.partials[slot] = WcsrPartial{s_window, s_tile, s_flags, 0};
+        p.partials[slot] = PartialRec{s_window, s_tile, s_flags, 0};
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce0 + 8 * buf);
@@ -572,59 +565,6 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
   }
 }
 
-// Second pass: slot s holds a window's first stage but not its last -> this
-// block adds that partial and the first-segment partials of the following
-// CTAs (in CTA order) until the one holding the window's last stage, and
-// writes the window's rows of C.  The list of contributing slots is found
-// once per block (dynamic shared memory, one int per CTA of the first pass);
-// each thread then sums four adjacent columns with independent loads.
-template <bool OUT_BF16>
-__global__ void __launch_bounds__(256)
-    wcsr_reduce_kernel(const WcsrPartial *partials, const float *ws, void *C, int32_t M, int32_t N, int32_t grid,
-                       int32_t bn) {
-  extern __shared__ int32_t contrib[];  // [grid]
-  __shared__ int32_t n_contrib;
-  const int slot = blockIdx.x;
-  const WcsrPartial rec = partials[slot];
-  if (rec.window < 0 || !(rec.flags & kStageFirst) || (rec.flags & kStageLast)) return;
-  if (threadIdx.x == 0) {
-    int n = 0;
-    contrib[n++] = slot;
-    for (int c = slot / 2 + 1; c < grid; ++c) {
-      const WcsrPartial r = partials[2 * c];
-      if (r.window != rec.window || r.col_tile != rec.col_tile) break;
-      contrib[n++] = 2 * c;
-      if (r.flags & kStageLast) break;
-    }
-    n_contrib = n;
-  }
-  __syncthreads();
-  const int n = n_contrib;
-  const int n0 = rec.col_tile * bn;
-  const int width = min(bn, N - n0);  // a multiple of 8 (N is)
-  for (int e = 4 * threadIdx.x; e < kH * width; e += 4 * blockDim.x) {
-    const int q = e / width;
-    const int col = e - q * width;  // a multiple of 4
-    const int row = rec.window * kH + q;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < n; ++i) {
-      const float4 v = *reinterpret_cast<const float4 *>(ws + static_cast<int64_t>(contrib[i]) * kWcsrSlotFloats +
-                                                         q * 256 + col);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
-    }
-    if (row < M) {
-      const int64_t o = static_cast<int64_t>(row) * N + n0 + col;
-      store_out<OUT_BF16>(C, o, acc.x);
-      store_out<OUT_BF16>(C, o + 1, acc.y);
-      store_out<OUT_BF16>(C, o + 2, acc.z);
-      store_out<OUT_BF16>(C, o + 3, acc.w);
-    }
-  }
-}
-
 template <int NACC, int Q, int PW, int MINB, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_variant(const WcsrParams &p, cudaStream_t stream) {
   using C_ = Cfg<NACC, Q, PW, MINB>;
@@ -635,8 +575,8 @@ cudaError_t launch_variant(const WcsrParams &p, cudaStream_t stream) {
   kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, p.grid * sizeof(int32_t), stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
-                                                               C_::kBN);
+  split_reduce_kernel<kH, OUT_BF16><<<2 * p.grid, 256, p.grid * sizeof(int32_t), stream>>>(
+      p.partials, p.workspace, kWcsrSlotFloats, 256, p.C, p.M, p.N, p.grid, C_::kBN);
   return cudaGetLastError();
 }
 
@@ -724,8 +664,8 @@ cudaError_t launch_noalloc_variant(const WcsrParams &p, cudaStream_t stream) {
   kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  wcsr_reduce_kernel<OUT_BF16><<<2 * p.grid, 256, p.grid * sizeof(int32_t), stream>>>(p.partials, p.workspace, p.C, p.M, p.N, p.grid,
-                                                               C_::kBN);
+  split_reduce_kernel<kH, OUT_BF16><<<2 * p.grid, 256, p.grid * sizeof(int32_t), stream>>>(
+      p.partials, p.workspace, kWcsrSlotFloats, 256, p.C, p.M, p.N, p.grid, C_::kBN);
   return cudaGetLastError();
 }
 
@@ -734,7 +674,7 @@ cudaError_t launch_noalloc_variant(const WcsrParams &p, cudaStream_t stream) {
 // the library, for the life of the process.
 constexpr size_t kNoallocStageBytes = static_cast<size_t>(kNoallocMaxStages) * sizeof(WcsrStage);
 constexpr size_t kNoallocWsBytes = static_cast<size_t>(2 * kNoallocMaxCtas) * kWcsrSlotFloats * sizeof(float);
-constexpr size_t kNoallocRecBytes = static_cast<size_t>(2 * kNoallocMaxCtas) * sizeof(WcsrPartial);
+constexpr size_t kNoallocRecBytes = static_cast<size_t>(2 * kNoallocMaxCtas) * sizeof(PartialRec);
 constexpr size_t kNoallocScratchBytes = kNoallocStageBytes + kNoallocWsBytes + kNoallocRecBytes + 256;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
 
@@ -766,7 +706,7 @@ cudaError_t launch_wcsr_noalloc(WcsrParams p, const int64_t *window_row_ptr, int
   WcsrStage *stages = reinterpret_cast<WcsrStage *>(base);
   p.stages = stages;
   p.workspace = reinterpret_cast<float *>(base + kNoallocStageBytes);
-  p.partials = reinterpret_cast<WcsrPartial *>(base + kNoallocStageBytes + kNoallocWsBytes);
+  p.partials = reinterpret_cast<PartialRec *>(base + kNoallocStageBytes + kNoallocWsBytes);
   uint8_t *tail = base + kNoallocStageBytes + kNoallocWsBytes + kNoallocRecBytes;  // 256 spare bytes
   p.n_stages_dev = reinterpret_cast<int64_t *>(tail);
   p.status = reinterpret_cast<uint32_t *>(tail + 8);  // bounded-wait timeouts (not reported by this entry point)

@@ -61,6 +61,40 @@ def test_bcsr_parity_two_ctas_per_sm(m, k, n, keep, dt, out_dt):
     full_check(m, k, n, rp, ci, vals, dt, out_dt, B, runs=2)
 
 
+@pytest.mark.parametrize("m,k,n,keep,ctas,out_dt", [
+    (640, 2048, 264, 0.5, None, "f32"),   # default split grid: 4 stages per CTA, tiles cut into several segments
+    (640, 2048, 264, 0.5, 7, "bf16"),     # few CTAs: shares span several tiles and column tiles, bf16 C
+    (448, 4096, 128, 0.4, 5, "f32"),      # 128-column tiles (two CTAs per SM, three stages)
+    (300, 1024, 72, 0.3, 3, "bf16"),      # ragged M, N < 128
+    (64, 4096, 256, 1.0, None, "f32"),    # one block row of 64 blocks: CTA shares inside a single tile
+    (200, 640, 520, 0.6, 11, "f32"),      # three 256-column tiles in one group, ragged last tile
+])
+def test_bcsr_split_schedule(m, k, n, keep, ctas, out_dt):
+    """Problems with fewer tiles than two per SM take the split schedule:
+    equal stage shares per CTA, cut tiles finished by the partial-sum pass in
+    CTA order.  Compared element by element, and bitwise reproducible."""
+    rng = np.random.default_rng(m * 7 + n + (ctas or 0))
+    rp, ci = W.block_pattern(rng, m, k, 64, 64, keep=keep)
+    vals = W.draw_values(rng, len(ci), "u1", "bf16")
+    B = W.dense_bits(rng, (k, n), "u1", "bf16")
+    outs, _ = run_library("bcsr", m, k, rp, ci, vals, "bf16", out_dt, B, max_ctas=ctas, runs=2)
+    C_ref, S_ref = oracle.spmm_csr(m, k, rp, ci, vals, ocode("bf16"), B)
+    for C in outs:
+        assert_parity(C, C_ref, S_ref, f"bcsr split {m}x{k} N={n} ctas={ctas}")
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_bcsr_many_block_rows_narrow_tiles():
+    """Enough block rows for the default (whole-tile) schedule at N <= 128:
+    128-column tiles, one CTA per SM, six stages."""
+    rng = np.random.default_rng(31)
+    m, k, n = 19460, 192, 120
+    rp, ci = W.block_pattern(rng, m, k, 64, 64, keep=0.5)
+    vals = W.draw_values(rng, len(ci), "u1", "bf16")
+    B = W.dense_bits(rng, (k, n), "u1", "bf16")
+    full_check(m, k, n, rp, ci, vals, "bf16", "f32", B, runs=2)
+
+
 def test_bcsr_tiny_workload():
     w = W.bcsr_tiny()
     outs, info = full_check(w.m, w.k, w.n, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.B(), runs=2)
