@@ -448,6 +448,14 @@ def run_sweep(args):
         if sel and name not in sel:
             continue
         cfgs.append((name, lambda b=b, n=sel.get(name): b(n)))
+    # single sweep points, e.g. bcsr_sweep_95_N256 or wcsr_sweep_0.1_N8
+    for e in sel:
+        parts = e.split("_")
+        if len(parts) == 4 and parts[0] in ("bcsr", "wcsr") and parts[1] == "sweep" and parts[3].startswith("N"):
+            lvl, n = float(parts[2]), int(parts[3][1:])
+            fn = (lambda lvl=lvl, n=n: [W.bcsr_sweep(int(lvl), n)]) if parts[0] == "bcsr" else \
+                (lambda lvl=lvl, n=n: [W.wcsr_sweep(lvl, n)])
+            cfgs.append((e, fn))
     for name, b in cfgs:
         cache = {}
         for w in b():

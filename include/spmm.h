@@ -54,6 +54,13 @@ typedef enum { SPMM_F16 = 0, SPMM_BF16 = 1, SPMM_F32 = 2 } spmm_dtype;
 
 typedef enum { SPMM_FORMAT_BCSR = 0, SPMM_FORMAT_WCSR = 1 } spmm_format;
 
+/* Work schedule of the BCSR kernel (spmm_set_schedule). */
+typedef enum {
+    SPMM_SCHEDULE_AUTO = 0,   /* the library's choice (the default) */
+    SPMM_SCHEDULE_TILES = 1,  /* whole tiles (block row x column tile) per CTA, round-robin */
+    SPMM_SCHEDULE_SPLIT = 2   /* equal shares of the tiles' stages per CTA; cut tiles summed by a second pass */
+} spmm_schedule;
+
 /* Statistics of a handle's format (spmm_format_info). */
 typedef struct {
     int32_t format;          /* spmm_format */
@@ -126,6 +133,23 @@ spmm_status spmm_wcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64
 spmm_status spmm_run(spmm_handle h, const void *B, void *C, int64_t N, void *stream);
 
 /*
+ * spmm_run_linear -- Y = X * A^T for a BCSR handle with 64 x 64 blocks: the
+ * product in the layout of a linear layer whose weight is A (m output
+ * features x k input features), Y[n][i] = sum_j X[n][j] * A[i][j].  X is the
+ * dense operand B = X^T of C = A * B stored column-major, the layout the
+ * paper's BCSR kernel reads B in (Section III-B) and the one of its drop-in
+ * replacement of a linear layer (Section IV-D, Table III); Y = C^T.
+ *   X  device pointer, N x k row-major, in_t, 16-byte aligned; k % 8 == 0.
+ *   Y  device pointer, N x m row-major, out_t, 16-byte aligned, fully
+ *      overwritten; m % 8 == 0 for bf16 Y, m % 4 == 0 for fp32 Y.
+ *   N  rows of X and Y (tokens), N > 0; no multiple is required.
+ * Asynchronous on `stream`; errors as spmm_run, plus UNSUPPORTED for a WCSR
+ * handle.  Rows of X are read by 256-row tiles; results are bitwise
+ * reproducible run to run.
+ */
+spmm_status spmm_run_linear(spmm_handle h, const void *X, void *Y, int64_t N, void *stream);
+
+/*
  * spmm_run_host -- the same product with B and C in HOST memory: copies B to
  * the device, runs, copies C back, all on `stream`, and waits for the stream.
  * Device staging buffers are owned by the handle and grow on demand.  Pinned
@@ -195,6 +219,25 @@ spmm_status spmm_check(spmm_handle h, void *stream);
  * order) but not the result beyond fp32 rounding.
  */
 spmm_status spmm_set_max_ctas(spmm_handle h, int32_t ctas);
+
+/*
+ * spmm_set_schedule -- choose how a BCSR handle's spmm_run spreads work over
+ * the persistent CTAs.  SPMM_SCHEDULE_TILES gives each CTA whole tiles (one
+ * block row x one tile of 128 or 256 columns), as the paper's static grid
+ * does (Section III-F).  SPMM_SCHEDULE_SPLIT lists the stages of all tiles
+ * (one per stored block; one for a block row without blocks) and gives each
+ * CTA an equal contiguous share, so long block rows are spread over several
+ * CTAs (the load balance that the paper's WCSR task decomposition gives
+ * windows, Section III-C); tiles cut between CTAs leave fp32 partial sums
+ * that a second kernel adds in CTA order, so results stay bitwise
+ * reproducible.  SPMM_SCHEDULE_AUTO (the default) takes the split schedule
+ * only when fewer than half the SMs would get a tile and the tiles average at
+ * least 8 stages.  The split schedule needs a handle with fewer than two block
+ * rows per SM (its workspace is allocated at create only then); otherwise
+ * SPLIT runs as TILES.  WCSR handles always use their equal-share schedule.
+ * Errors: INVALID_ARG (null handle, unknown schedule).
+ */
+spmm_status spmm_set_schedule(spmm_handle h, int32_t schedule);
 
 /*
  * spmm_selftest_wait_timeout -- failure-detection self test.  Launches one

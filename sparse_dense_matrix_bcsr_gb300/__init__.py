@@ -48,7 +48,7 @@ EXPORTS = (
     "spmm_bcsr_create", "spmm_wcsr_create", "spmm_run", "spmm_run_host", "spmm_destroy",
     "spmm_format_info", "spmm_export_format", "spmm_bcsr_convert", "spmm_wcsr_convert",
     "spmm_check", "spmm_set_max_ctas", "spmm_selftest_wait_timeout", "spmm_status_str",
-    "spmm_last_error", "spmm_wcsr_run_noalloc",
+    "spmm_last_error", "spmm_wcsr_run_noalloc", "spmm_run_linear", "spmm_set_schedule",
 )
 
 
@@ -87,6 +87,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "spmm_bcsr_create": [ctypes.POINTER(P), I64, I64, P, P, P, I32, I32, I32, I32],
         "spmm_wcsr_create": [ctypes.POINTER(P), I64, I64, P, P, P, I32, I32, I32, I32],
         "spmm_run": [P, P, P, I64, P],
+        "spmm_run_linear": [P, P, P, I64, P],
         "spmm_run_host": [P, P, P, I64, P],
         "spmm_destroy": [P],
         "spmm_format_info": [P, ctypes.POINTER(spmm_info)],
@@ -95,6 +96,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "spmm_wcsr_convert": [I64, I64, P, P, P, I32, I32, ctypes.POINTER(I64), P, P, P],
         "spmm_check": [P, P],
         "spmm_set_max_ctas": [P, ctypes.c_int32],
+        "spmm_set_schedule": [P, ctypes.c_int32],
         "spmm_selftest_wait_timeout": [I64, P, ctypes.POINTER(ctypes.c_int32)],
         "spmm_wcsr_run_noalloc": [P, P, P, I64, I64, I64, I32, I32, P, P, I64, P],
     }
@@ -161,6 +163,11 @@ def spmm_run(h: int, B_ptr: int, C_ptr: int, N: int, stream: int = 0) -> None:
     _check(load_library().spmm_run(h, B_ptr, C_ptr, N, stream or None), "spmm_run")
 
 
+def spmm_run_linear(h: int, X_ptr: int, Y_ptr: int, N: int, stream: int = 0) -> None:
+    """Y = X * A^T on the GPU (BCSR handle; X is N x k, Y is N x m, both row-major device pointers)."""
+    _check(load_library().spmm_run_linear(h, X_ptr, Y_ptr, N, stream or None), "spmm_run_linear")
+
+
 def spmm_run_status(h: int, B_ptr: int, C_ptr: int, N: int, stream: int = 0) -> int:
     """spmm_run returning the raw status instead of raising."""
     return load_library().spmm_run(h, B_ptr, C_ptr, N, stream or None)
@@ -210,6 +217,16 @@ def spmm_check(h: int, stream: int = 0) -> int:
 
 def spmm_set_max_ctas(h: int, ctas: int) -> None:
     _check(load_library().spmm_set_max_ctas(h, ctas), "spmm_set_max_ctas")
+
+
+SPMM_SCHEDULE_AUTO = 0
+SPMM_SCHEDULE_TILES = 1
+SPMM_SCHEDULE_SPLIT = 2
+
+
+def spmm_set_schedule(h: int, schedule: int) -> None:
+    """BCSR work schedule: SPMM_SCHEDULE_AUTO, _TILES or _SPLIT."""
+    _check(load_library().spmm_set_schedule(h, schedule), "spmm_set_schedule")
 
 
 def spmm_selftest_wait_timeout(timeout_ns: int, stream: int = 0) -> int:

@@ -240,20 +240,31 @@ __global__ void __launch_bounds__(kThreads, MINB)
       // group of kGroupN column tiles, tile (br, i) starts at stage
       // gsz * P[br] + i * len(br) of the group, P = stage_row_ptr.
       const int nbr = p.n_block_rows;
-      const int64_t s_all = p.stage_row_ptr[nbr];  // stages per column tile
+      const int64_t s_all = p.split_stages;  // stages per column tile (= P[nbr])
       const int64_t total = s_all * n_col_tiles;
       const int64_t f0 = total * blockIdx.x / gridDim.x;
       const int64_t f1 = total * (blockIdx.x + 1) / gridDim.x;
-      const int64_t n_blocks = p.block_row_ptr[nbr];
+      const int64_t n_blocks = p.n_blocks;
       const int64_t span = s_all * kGroupN;
       int g = static_cast<int>(f0 / span);
       int64_t r = f0 - g * span;
       int gsz = min(kGroupN, n_col_tiles - g * kGroupN);
-      int lo = 0, hi = nbr - 1;  // last block row with gsz * P[br] <= r
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (gsz * p.stage_row_ptr[mid] <= r) lo = mid;
-        else hi = mid - 1;
+      // Last block row with gsz * P[br] <= r, found 32 samples of P at a time
+      // by the whole warp (the range shrinks 32-fold per round of loads).
+      int lo = 0, hi = nbr - 1;
+      while (hi > lo) {
+        const int64_t span_r = hi - lo;
+        const int idx = lo + static_cast<int>((span_r * (lane + 1) + 31) / 32);  // in (lo, hi], lane 31: hi
+        const unsigned ok = __ballot_sync(0xffffffffu, gsz * p.stage_row_ptr[idx] <= r);
+        if (ok == 0) {
+          hi = __shfl_sync(0xffffffffu, idx, 0) - 1;
+        } else {
+          const int k = 31 - __clz(static_cast<int>(ok));
+          const int idx_k = __shfl_sync(0xffffffffu, idx, k);
+          const int idx_n = __shfl_sync(0xffffffffu, idx, k < 31 ? k + 1 : 31);
+          hi = k < 31 ? idx_n - 1 : hi;
+          lo = idx_k;
+        }
       }
       int br = lo;
       int64_t len = p.stage_row_ptr[br + 1] - p.stage_row_ptr[br];
@@ -624,9 +635,8 @@ cudaError_t launch_variant(const CUtensorMap &tmA, const CUtensorMap &tmB, const
   kern<<<static_cast<unsigned>(grid), kThreads, C_::kSmemBytes, stream>>>(tmA, tmB, tmC, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.split_grid == 0) return e;
-  split_reduce_kernel<kBlk, OUT_BF16><<<static_cast<unsigned>(2 * grid), 256, grid * sizeof(int32_t), stream>>>(
-      p.partials, p.workspace, kBcsrSlotFloats, BN, p.C, p.M, p.N, static_cast<int32_t>(grid), BN);
-  return cudaGetLastError();
+  return launch_split_reduce<kBlk, OUT_BF16>(p.partials, p.workspace, kBcsrSlotFloats, BN, p.C, p.M, p.N,
+                                             static_cast<int32_t>(grid), BN, stream);
 }
 
 template <int BN, int Q, int NBUF, int PARTS, int MINB, bool OUT_BF16>
@@ -647,10 +657,11 @@ cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
   // accumulators; one CTA per SM with six stages, or, on the split schedule,
   // two CTAs per SM with three.  Wider (bcsr_wide_tiles): 256-column tiles,
   // one weight-stationary MMA of N = 256 per k step, two accumulators of 128
-  // TMEM columns, two CTAs per SM with two stages each, so one CTA's barrier
-  // handshakes overlap the other's MMAs and loads (problems with fewer than
-  // two tiles per SM take the split schedule).  Epilogue parts are one
-  // 32-row x 64-byte store box (32 bf16 or 16 fp32 columns).
+  // TMEM columns; with at least two tiles per SM (or on the split schedule)
+  // two CTAs share each SM (two stages each), so one CTA's barrier handshakes
+  // overlap the other's MMAs and loads; with fewer tiles one CTA per SM runs
+  // four stages.  Epilogue parts are one 32-row x 64-byte store box (32 bf16
+  // or 16 fp32 columns).
   if (!bcsr_wide_tiles(p.N)) {
     if (p.split_grid > 0)
       return out_bf16 ? launch_in<128, 3, 2, 2, 2, true>(tmA, tmB, tmC, p, in_bf16, stream)
@@ -658,6 +669,10 @@ cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
     return out_bf16 ? launch_in<128, 6, 2, 2, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
                     : launch_in<128, 6, 2, 2, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
   }
+  const int64_t tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + 255) / 256);
+  if (tiles < 2ll * p.num_sms && p.split_grid == 0)
+    return out_bf16 ? launch_in<256, 4, 2, 4, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                    : launch_in<256, 4, 2, 8, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
   return out_bf16 ? launch_in<256, 2, 2, 4, 2, true>(tmA, tmB, tmC, p, in_bf16, stream)
                   : launch_in<256, 2, 2, 8, 2, false>(tmA, tmB, tmC, p, in_bf16, stream);
 }

@@ -63,6 +63,8 @@ struct BcsrParams {
   int32_t max_ctas;              // cap on the persistent grid (0: the kernel's default CTAs per SM)
   int32_t num_sms;
   int32_t split_grid;            // > 0: split schedule over this many CTAs
+  int64_t split_stages;          // split schedule: stages per column tile (stage_row_ptr[n_block_rows])
+  int64_t n_blocks;              // stored blocks (block_row_ptr[n_block_rows])
   uint32_t *status;              // device status word
   uint64_t wait_limit_ns;        // bound of every mbarrier wait
 };
@@ -88,6 +90,14 @@ int bcsr_tile_cols(int64_t N);
 // C as [M rows, N cols] with the boxes of bcsr_wide_tiles(N).
 cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                         const BcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream);
+
+// BCSR product in the layout of a linear layer, Y = X * A^T (bcsr_linear_kernel.cu):
+// p.B is X (N x K row-major), p.C is Y (N x M row-major).  tmA covers the
+// blocks as for launch_bcsr; tmX covers X as [N rows, K cols] with 256-row x
+// 64-column boxes, 128-byte swizzle; tmY covers Y as [N rows, M cols] with
+// 32-row x 128-byte boxes, 128-byte swizzle.
+cudaError_t launch_bcsr_linear(const CUtensorMap &tmA, const CUtensorMap &tmX, const CUtensorMap &tmY,
+                               const BcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream);
 
 // WCSR work is a list of stages: at most 64 packed columns of one window.
 // Every window has at least one stage (ncols = 0 for a window without

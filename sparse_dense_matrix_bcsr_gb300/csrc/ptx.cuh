@@ -121,6 +121,12 @@ __device__ __forceinline__ void tma_bulk_load(uint32_t dst, const void *src, uin
       : "memory");
 }
 
+// Bring `bytes` of global memory (16-byte aligned, a multiple of 16 bytes)
+// into L2 ahead of a later copy, without writing shared memory.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2-D tiled bulk copy shared -> global (a TMA store).  Elements of the box
 // outside the tensor are not written.  x is the innermost coordinate and must
 // be non-negative with x * element size a multiple of 16 bytes.

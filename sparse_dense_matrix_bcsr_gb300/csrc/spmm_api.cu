@@ -101,6 +101,29 @@ spmm_status encode_c(CUtensorMap *map, void *base, bool bf16, uint64_t rows, uin
   return SPMM_OK;
 }
 
+// X of the linear-layer product as a TMA source: N rows x k columns of
+// 16-bit elements, 256-row x 64-column boxes, 128-byte swizzle.
+spmm_status encode_x(CUtensorMap *map, const void *base, bool bf16, uint64_t rows, uint64_t cols) {
+  return encode_2d(map, base, bf16, rows, cols, cols, 256, 64);
+}
+
+// Y of the linear-layer product as a TMA destination: N rows x m columns of
+// bf16 or fp32, 32-row x 128-byte boxes, 128-byte swizzle.
+spmm_status encode_y(CUtensorMap *map, void *base, bool bf16, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(SPMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const uint64_t esz = bf16 ? 2 : 4;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), 32u};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SPMM_ERR_CUDA, "cuTensorMapEncodeTiled (Y) failed (%d)", static_cast<int>(r));
+  return SPMM_OK;
+}
+
 }  // namespace
 
 struct spmm_handle_s {
@@ -125,12 +148,20 @@ struct spmm_handle_s {
   void *c_cached = nullptr;
   int64_t nc_cached = -1;
   CUtensorMap tm_C;
+  // the linear-layer product's X and Y
+  const void *x_cached = nullptr;
+  int64_t nx_cached = -1;
+  CUtensorMap tm_X;
+  void *y_cached = nullptr;
+  int64_t ny_cached = -1;
+  CUtensorMap tm_Y;
 
   // Work decomposition.  WCSR: stages of <= 64 packed columns.  BCSR: the
   // prefix sums of max(1, blocks) per block row (the split schedule's stage
   // list).  Both: the partial-sum workspace of groups cut between persistent
   // CTAs (BCSR: allocated only when the split schedule can be chosen).
   int32_t max_ctas = 0;  // 0: the kernels' default CTAs per SM
+  int32_t schedule = SPMM_SCHEDULE_AUTO;
   int64_t n_stages = 0;
   int64_t *d_stage_row_ptr = nullptr;
   uint8_t *d_stage_pack = nullptr;
@@ -296,16 +327,20 @@ spmm_status build_bcsr_split(spmm_handle h, const std::vector<int64_t> &bptr) {
   return SPMM_OK;
 }
 
-// BCSR grid of the split schedule at dense width N, or 0 for the default
-// schedule (whole tiles per CTA): the split schedule is taken when the tiles
-// number fewer than kBcsrSplitBelowTilesPerSm per SM, over up to
-// kBcsrSplitCtasPerSm CTAs per SM with at least kBcsrSplitMinStages stages
-// each (and at most the spmm_set_max_ctas cap).
+// BCSR grid of the split schedule at dense width N, or 0 for the tile
+// schedule (whole tiles per CTA).  SPMM_SCHEDULE_AUTO takes the split schedule
+// when fewer than half the SMs would get a tile and the tiles average at
+// least 8 stages: there the tile schedule leaves most SMs idle while a few
+// walk long block rows, and spreading the stages outweighs the second pass.
+// The grid is up to kBcsrSplitCtasPerSm CTAs per SM with at least
+// kBcsrSplitMinStages stages each (and at most the spmm_set_max_ctas cap).
 int32_t bcsr_split_grid(spmm_handle h, int64_t N) {
-  if (!h->d_ws) return 0;
+  if (!h->d_ws || h->schedule == SPMM_SCHEDULE_TILES) return 0;
   const int64_t col_tiles = (N + spmm::bcsr_tile_cols(N) - 1) / spmm::bcsr_tile_cols(N);
   const int64_t sms = std::max(h->num_sms, 1);
-  if (h->n_groups * col_tiles >= spmm::kBcsrSplitBelowTilesPerSm * sms) return 0;
+  const int64_t tiles = h->n_groups * col_tiles;
+  if (tiles >= spmm::kBcsrSplitBelowTilesPerSm * sms) return 0;
+  if (h->schedule == SPMM_SCHEDULE_AUTO && (2 * tiles > sms || h->n_stages < 8 * h->n_groups)) return 0;
   const int64_t stages = h->n_stages * col_tiles;
   int64_t g = std::min<int64_t>(spmm::kBcsrSplitCtasPerSm * sms,
                                 (stages + spmm::kBcsrSplitMinStages - 1) / spmm::kBcsrSplitMinStages);
@@ -362,6 +397,8 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
     p.workspace = h->d_ws;
     p.partials = h->d_partials;
     p.split_grid = bcsr_split_grid(h, N);
+    p.split_stages = h->n_stages;
+    p.n_blocks = h->n_units;
     p.B = B;
     p.C = C;
     p.ldc = N;
@@ -526,6 +563,14 @@ spmm_status spmm_set_max_ctas(spmm_handle h, int32_t ctas) {
   return SPMM_OK;
 }
 
+spmm_status spmm_set_schedule(spmm_handle h, int32_t schedule) {
+  if (!h) return fail(SPMM_ERR_INVALID_ARG, "handle is NULL");
+  if (schedule != SPMM_SCHEDULE_AUTO && schedule != SPMM_SCHEDULE_TILES && schedule != SPMM_SCHEDULE_SPLIT)
+    return fail(SPMM_ERR_INVALID_ARG, "unknown schedule %d", schedule);
+  h->schedule = schedule;
+  return SPMM_OK;
+}
+
 spmm_status spmm_wcsr_run_noalloc(const int64_t *window_row_ptr, const int32_t *window_col_idx, const void *values,
                                   int64_t m, int64_t k, int64_t p_total, spmm_dtype in_t, spmm_dtype out_t,
                                   const void *B, void *C, int64_t N, void *stream) {
@@ -576,6 +621,55 @@ spmm_status spmm_run(spmm_handle h, const void *B, void *C, int64_t N, void *str
   spmm_status st = check_run_args(h, B, C, N);
   if (st != SPMM_OK) return st;
   return run_device(h, B, C, N, static_cast<cudaStream_t>(stream));
+}
+
+spmm_status spmm_run_linear(spmm_handle h, const void *X, void *Y, int64_t N, void *stream) {
+  if (!h) return fail(SPMM_ERR_INVALID_ARG, "handle is NULL");
+  if (h->format != SPMM_FORMAT_BCSR) return fail(SPMM_ERR_UNSUPPORTED, "spmm_run_linear takes a BCSR handle");
+  if (N <= 0 || N >= (1ll << 31)) return fail(SPMM_ERR_INVALID_ARG, "N must be in (0, 2^31)");
+  if (!X || !Y) return fail(SPMM_ERR_INVALID_ARG, "X or Y is NULL");
+  if ((reinterpret_cast<uintptr_t>(X) | reinterpret_cast<uintptr_t>(Y)) & 15)
+    return fail(SPMM_ERR_UNSUPPORTED, "X and Y must be 16-byte aligned");
+  spmm_status st = SPMM_OK;
+  if (h->b_row != 64 || h->b_col != 64) return fail(SPMM_ERR_UNSUPPORTED, "the BCSR kernel takes 64 x 64 blocks");
+  const bool in_bf16 = h->in_t == SPMM_BF16;
+  const bool out_bf16 = h->out_t == SPMM_BF16;
+  if (h->k % 8 != 0) return fail(SPMM_ERR_UNSUPPORTED, "k must be a multiple of 8 (16-byte rows of X)");
+  if (h->m % (out_bf16 ? 8 : 4) != 0) return fail(SPMM_ERR_UNSUPPORTED, "m must make 16-byte rows of Y");
+  if (!h->sm103) return fail(SPMM_ERR_UNSUPPORTED, "the kernels need an sm_103 (GB300) device");
+  if (h->m == 0) return SPMM_OK;
+  if (h->x_cached != X || h->nx_cached != N) {
+    st = encode_x(&h->tm_X, X, in_bf16, static_cast<uint64_t>(N), static_cast<uint64_t>(std::max<int64_t>(h->k, 8)));
+    if (st != SPMM_OK) return st;
+    h->x_cached = X;
+    h->nx_cached = N;
+  }
+  if (h->y_cached != Y || h->ny_cached != N) {
+    st = encode_y(&h->tm_Y, Y, out_bf16, static_cast<uint64_t>(N), static_cast<uint64_t>(h->m));
+    if (st != SPMM_OK) return st;
+    h->y_cached = Y;
+    h->ny_cached = N;
+  }
+  spmm::BcsrParams p;
+  std::memset(&p, 0, sizeof p);
+  p.block_row_ptr = h->d_ptr;
+  p.block_col_idx = h->d_idx;
+  p.blocks = h->d_vals;
+  p.B = X;
+  p.C = Y;
+  p.ldc = h->m;
+  p.M = static_cast<int32_t>(h->m);
+  p.N = static_cast<int32_t>(N);
+  p.K = static_cast<int32_t>(h->k);
+  p.n_block_rows = static_cast<int32_t>(h->n_groups);
+  p.max_ctas = h->max_ctas;
+  p.num_sms = std::max(h->num_sms, 1);
+  p.status = h->d_status;
+  p.wait_limit_ns = h->wait_limit_ns;
+  cudaError_t e = spmm::launch_bcsr_linear(h->tm_vals, h->tm_X, h->tm_Y, p, in_bf16, out_bf16,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "BCSR linear kernel launch");
+  return SPMM_OK;
 }
 
 spmm_status spmm_check(spmm_handle h, void *stream) {

@@ -21,20 +21,21 @@
 // The product is computed transposed: the 128 columns of an accumulator are
 // the MMA's M (TMEM lanes) and the 16 rows of a window are the MMA's N.
 //
-// Only the producer warps read global memory.  Each stage is one record
-// (its 2 KB value tile, 64 column indices and descriptor) fetched with TMA
-// bulk copies into shared-memory rings ahead of use, so the producers read
-// indices from shared memory and no global load stalls their issue behind
-// the SM's outstanding gathers.  The MMA thread learns a stage's shape from a
-// record the producer writes to shared memory, and the epilogue learns a
-// window's identity from a record the MMA thread writes, so neither waits on
-// a global load.
+// Only the producer warps read global memory.  Each stage is one record in
+// global memory: its 2 KB value tile, 64 column indices and a descriptor.  A
+// producer warp fetches the index part of its items' records (272 bytes) by
+// TMA bulk copies into a per-warp ring kIdxLead of its items ahead, so it
+// reads an item's indices from shared memory without waiting; when it starts
+// the item it has the value tile copied into the item's stage by TMA and
+// copies the item's rows of B with cp.async, all completing on the stage's
+// barrier.  The MMA thread learns a stage's shape from a record the producer
+// writes to shared memory, and the epilogue learns a window's identity from a
+// record the MMA thread writes, so neither waits on a global load.
 //
 // PW + 5 warps (PW producer warps; two CTAs per SM run with PW = 2, so one
 // CTA's barrier handshakes and MMA issue stalls overlap the other's work):
 //   warps 0..PW-1  producers; warp w owns the work items w, w+PW, ... of the
-//                  CTA's range: it fetches an item's record kVLead of its
-//                  items ahead, then copies the item's 64 B rows with 16-byte
+//                  CTA's range; it copies an item's 64 B rows with 16-byte
 //                  cp.async (one B row, 512 B, per warp instruction at
 //                  BN = 256); every lane ends the item with
 //                  cp.async.mbarrier.arrive.noinc, so producers never block
@@ -65,30 +66,42 @@ constexpr int kChunkBytes = kKC * 64 * 2;    // 64 gathered rows x 64 columns
 constexpr int kEpiWarps = 4;
 constexpr int kAccBufs = 4;
 
-constexpr int kVLead = 1;      // a producer fetches stage records (value tiles) this many of its own items ahead
+// A producer fetches the column-index record of its items this many of its
+// own items ahead (a small TMA bulk copy into a per-warp ring), so reading an
+// item's indices never waits on memory; the item's 2 KB value tile is fetched
+// into the item's stage together with the gather (and brought into L2 when
+// its index record is fetched).
+constexpr int kIdxLead = 4;
 
-// NACC accumulators of 128 columns, Q stages, PW producer warps, MINB CTAs per SM.
-template <int NACC, int Q, int PW, int MINB>
+// NACC accumulators of 128 columns, Q stages, PW producer warps, MINB CTAs per
+// SM, ILEAD index-record slots per producer warp (0: indices are read from
+// global memory, the no-allocation variant).  A stage holds an item's gathered
+// B rows and its value tile.
+template <int NACC, int Q, int PW, int MINB, int ILEAD>
 struct Cfg {
   static constexpr int kMmaWarp = PW;                        // warps 0..PW-1 produce, PW issues MMAs
   static constexpr int kThreads = 32 * (PW + 1 + kEpiWarps);
-  static constexpr int kLead = kVLead * PW;                  // records are fetched this many work items ahead
   static constexpr int kBN = 128 * NACC;
   static constexpr int kChunks = 2 * NACC;
-  static constexpr int kStageBytes = kChunks * kChunkBytes;  // gathered B rows only
+  static constexpr int kGatherBytes = kChunks * kChunkBytes;  // gathered B rows
+  static constexpr int kStageBytes = kGatherBytes + kValBytes;
   static constexpr int kAccCols = kH * NACC;                     // TMEM columns per accumulator buffer
   static constexpr int kTmemCols = kAccBufs * kAccCols <= 32 ? 32 : (kAccBufs * kAccCols <= 64 ? 64 : 128);
-  // Record ring slots.  The record of item i + kLead is fetched by the warp
-  // that has just seen the MMAs of item i - Q complete, into the slot that
-  // item i + kLead - kVQ = i - Q last used, so no other release is needed.
-  static constexpr int kVQ = Q + kLead;
-  static constexpr int kMetaRing = (kVQ * kMetaBytes + 1023) / 1024 * 1024;
-  static constexpr int kSmemBytes = Q * kStageBytes + kVQ * kValBytes + kMetaRing + 2048 + 1024;
+  static constexpr int kIdxRing = (PW * ILEAD * kMetaBytes + 1023) / 1024 * 1024;
+  static constexpr int kBars = 2 * Q + 2 * kAccBufs + 1 + PW * ILEAD;
+  static constexpr int kMiscBytes = 2048;                    // barriers, TMEM address, records between roles
+  static constexpr int kSmemBytes = Q * kStageBytes + kIdxRing + kMiscBytes + 1024;
+  static_assert(kStageBytes % 1024 == 0 && kGatherBytes % 1024 == 0, "MMA operands need 1024-byte alignment");
+  // A producer's wait for stage (it % Q) to be free is a parity wait on the
+  // MMA commit of item it - Q; it is only unambiguous if the commit of item
+  // it - 2Q has already been seen, which the warp's wait for its previous item
+  // (it - PW) guarantees when PW <= Q.  With more producer warps than stages a
+  // warp could run two phases ahead, pass the wait early and overwrite a stage
+  // still in use.
+  static_assert(PW <= Q, "more producer warps than stages");
+  static_assert(kBars * 8 + 16 + Q * 16 + kAccBufs * 32 <= kMiscBytes, "barrier area");
   static_assert(kSmemBytes <= 227 * 1024 && MINB * (kSmemBytes + 1024) <= 228 * 1024, "shared memory");
   static_assert(MINB * kTmemCols <= 512, "TMEM");
-  // no-allocation variant: a value slot is reused by the item kVQ later and a
-  // producer fills it kVLead of its items (kVLead * 4 work items) ahead
-  static_assert(kVQ > kVLead * PW, "value slots must outlast the lead");
   static_assert(kAccBufs * kAccCols <= kTmemCols, "accumulator buffers exceed the TMEM allocation");
 };
 
@@ -120,17 +133,15 @@ struct SegRec {     // MMA -> epilogue, one per accumulator buffer
 template <int NACC, int Q, int PW, int MINB, bool IN_BF16, bool OUT_BF16, bool NOALLOC = false>
 __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
     wcsr_spmm_kernel(const WcsrParams p) {
-  using C_ = Cfg<NACC, Q, PW, MINB>;
+  constexpr int kILead = NOALLOC ? 0 : kIdxLead;
+  using C_ = Cfg<NACC, Q, PW, MINB, kILead>;
   constexpr int kMmaWarp = C_::kMmaWarp;
-  constexpr int kLead = C_::kLead;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int kVQ = C_::kVQ;
-  uint8_t *vring = smem + Q * C_::kStageBytes;  // kVQ value tiles of 2 KB
-  uint8_t *mring = vring + kVQ * kValBytes;     // kVQ index + descriptor records of kMetaBytes
-  uint64_t *bars = reinterpret_cast<uint64_t *>(mring + C_::kMetaRing);
-  // bars: full[Q], empty[Q], acc_full[kAccBufs], acc_empty[kAccBufs], drain, vfull[kVQ], vempty[kVQ]
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * Q + 2 * kAccBufs + 1 + 2 * kVQ);
+  uint8_t *iring = smem + Q * C_::kStageBytes;  // per producer warp: kILead index records of kMetaBytes
+  uint64_t *bars = reinterpret_cast<uint64_t *>(iring + C_::kIdxRing);
+  // bars: full[Q], empty[Q], acc_full[kAccBufs], acc_empty[kAccBufs], drain, ifull[PW][kILead]
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C_::kBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   StageRec *stage_rec = reinterpret_cast<StageRec *>(tmem_slot + 4);        // [Q]
   volatile SegRec *seg_rec = reinterpret_cast<volatile SegRec *>(stage_rec + Q);  // [kAccBufs]
@@ -156,12 +167,14 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
   const uint32_t accf0 = smem_addr(&bars[2 * Q]);
   const uint32_t acce0 = smem_addr(&bars[2 * Q + kAccBufs]);
   const uint32_t drain_bar = smem_addr(&bars[2 * Q + 2 * kAccBufs]);
-  const uint32_t vfull0 = smem_addr(&bars[2 * Q + 2 * kAccBufs + 1]);
-  const uint32_t vempty0 = vfull0 + 8 * kVQ;
+  const uint32_t ifull0 = smem_addr(&bars[2 * Q + 2 * kAccBufs + 1]);
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < Q; ++q) {
-      mbar_init(full0 + 8 * q, 33);  // 32 cp.async lane arrivals + lane 0's arrive (stage record)
+      // 32 cp.async lane arrivals (gathered rows; the value tile too in the
+      // no-allocation variant) + lane 0's arrive, which releases the stage
+      // record and expects the value tile's TMA bytes
+      mbar_init(full0 + 8 * q, 33);
       mbar_init(empty0 + 8 * q, 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
@@ -169,12 +182,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
       mbar_init(acce0 + 8 * b, kEpiWarps);
     }
     mbar_init(drain_bar, 1);
-    for (int v = 0; v < kVQ; ++v) {
-      // TMA bulk copy (lane 0's expect_tx arrive), or cp.async arrivals of the
-      // loading warp's 32 lanes in the no-allocation variant
-      mbar_init(vfull0 + 8 * v, NOALLOC ? 32 : 1);
-      mbar_init(vempty0 + 8 * v, 1);  // the MMA commit
-    }
+    for (int v = 0; v < PW * kILead; ++v) mbar_init(ifull0 + 8 * v, 1);  // lane 0's expect_tx arrive
     *abort_flag = 0;
     fence_barrier_init();
     // partial-sum records of this CTA (overwritten below when used)
@@ -194,52 +202,70 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
     // ------------------------------------------------------------ producers
     const uint16_t *Bp = reinterpret_cast<const uint16_t *>(p.B);
     constexpr int kStep = PW;
-    // The B rows of one work item -> stage `st` with 16-byte cp.async
-    // (zero-fill for padding positions and columns past N); lo / hi hold the
-    // item's column indices for positions lane and 32 + lane.
+    // The B rows of one work item -> stage `st` with 16-byte cp.async; lo /
+    // hi hold the item's column indices for positions lane and 32 + lane.
+    // Only the 16-byte units of the tile's live columns (below N) are copied:
+    // output column m of the transposed product depends on gathered column m
+    // alone, and columns at or past N are never stored, so whatever the stage
+    // holds there does not matter.  A padding position (index -1) is
+    // zero-filled, since its zero values multiply it.  Each warp instruction
+    // copies 32 (row, unit) pairs, U units per row (U = live units rounded up
+    // to a power of two), so at small N a stage costs a few instructions.
     auto gather = [&](uint32_t st, int n0, int ncols, int32_t lo, int32_t hi) {
-      if constexpr (NACC == 2) {
-        // one B row (32 units of 16 B) per warp instruction
-        const int n = n0 + lane * 8;
-        const bool n_live = n < p.N;
-        const uint32_t dst_col = (lane >> 3) * kChunkBytes;
-        const uint32_t uu = static_cast<uint32_t>(lane & 7);
-        // 16 rows at a time (ncols is a multiple of 16): the shuffles of a
-        // group issue back to back instead of each waiting for the last
+      const int live_units = (min(C_::kBN, p.N - n0) + 7) >> 3;  // 1 .. 16 * NACC
+      if (live_units == 16 * NACC) {
+        // every unit live: the row layout is fixed at compile time (one B row
+        // per instruction at BN = 256, two at BN = 128)
+        constexpr int kRowsPerInst = 2 / NACC;
+        const int v = lane & (16 * NACC - 1);
+        const int rl = lane / (16 * NACC);
+        const int n = n0 + v * 8;
+        const uint32_t dst_col = (v >> 3) * kChunkBytes;
+        const uint32_t uu = static_cast<uint32_t>(v & 7);
         for (int r0 = 0; r0 < ncols; r0 += 16) {
           const int32_t src = r0 < 32 ? lo : hi;
-          int32_t col[16];
+          constexpr int kInst = 16 / kRowsPerInst;
+          int32_t col[kInst];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) col[j] = __shfl_sync(0xffffffffu, src, (r0 + j) & 31);
+          for (int j = 0; j < kInst; ++j) col[j] = __shfl_sync(0xffffffffu, src, (r0 + kRowsPerInst * j + rl) & 31);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int r = r0 + j;
+          for (int j = 0; j < kInst; ++j) {
+            const int r = r0 + kRowsPerInst * j + rl;
             // caller-supplied indices (no-allocation variant) are clamped to B's rows
-            const bool live = n_live && col[j] >= 0 && (!NOALLOC || col[j] < p.K);
+            const bool live = col[j] >= 0 && (!NOALLOC || col[j] < p.K);
             cp_async_16(st + dst_col + r * 128 + ((uu ^ static_cast<uint32_t>(r & 7)) << 4),
                         live ? static_cast<const void *>(Bp + static_cast<int64_t>(col[j]) * p.N + n)
                              : static_cast<const void *>(Bp),
                         live ? 16u : 0u);
           }
         }
-      } else {
-        // two B rows (16 units each) per warp instruction
-        const int v = lane & 15;
-        const int half = lane >> 4;
-        const int n = n0 + v * 8;
-        const bool n_live = n < p.N;
-        const uint32_t dst_col = (v >> 3) * kChunkBytes;
-        const uint32_t uu = static_cast<uint32_t>(v & 7);
-        for (int r0 = 0; r0 < ncols; r0 += 16) {
-          const int32_t src = r0 < 32 ? lo : hi;
-          int32_t col[8];
+        return;
+      }
+      const int sh = 32 - __clz(live_units - 1);                 // log2 of U (0 for one unit)
+      const int rsh = 5 - sh;                                    // log2 of rows per instruction
+      const int ninst = (ncols + (1 << rsh) - 1) >> rsh;
+      const int r_lane = lane >> sh;                             // this lane's row within an instruction
+      const int u = lane & ((1 << sh) - 1);                      // this lane's unit within its row
+      const int n = n0 + u * 8;
+      const bool u_live = n < p.N;
+      const uint32_t dst_u = (u >> 3) * kChunkBytes;
+      const uint32_t uu = static_cast<uint32_t>(u & 7);
+      // 16 instructions at a time: their shuffles issue back to back instead
+      // of each copy waiting for the last
+      for (int i0 = 0; i0 < ninst; i0 += 16) {
+        int32_t col[16];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) col[j] = __shfl_sync(0xffffffffu, src, (r0 + 2 * j + half) & 31);
+        for (int j = 0; j < 16; ++j) {
+          const int rb = (i0 + j) << rsh;  // first row of instruction i0 + j
+          col[j] = __shfl_sync(0xffffffffu, rb < 32 ? lo : hi, (rb + r_lane) & 31);
+        }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int r = r0 + 2 * j + half;
-            const bool live = n_live && col[j] >= 0 && (!NOALLOC || col[j] < p.K);
-            cp_async_16(st + dst_col + r * 128 + ((uu ^ static_cast<uint32_t>(r & 7)) << 4),
+        for (int j = 0; j < 16; ++j) {
+          const int r = ((i0 + j) << rsh) + r_lane;
+          if (i0 + j < ninst && u_live && r < ncols) {
+            // caller-supplied indices (no-allocation variant) are clamped to B's rows
+            const bool live = col[j] >= 0 && (!NOALLOC || col[j] < p.K);
+            cp_async_16(st + dst_u + r * 128 + ((uu ^ static_cast<uint32_t>(r & 7)) << 4),
                         live ? static_cast<const void *>(Bp + static_cast<int64_t>(col[j]) * p.N + n)
                              : static_cast<const void *>(Bp),
                         live ? 16u : 0u);
@@ -250,11 +276,12 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
     if constexpr (NOALLOC) {
       // Caller-owned arrays: the stage list built on the device, the column
       // indices read at each stage's first packed column, and the values
-      // copied from the row-major [16][P_total] array (swizzled here).
-      // Work items of this warp: f = f0 + warp + 4*i.  Descriptors are
-      // loaded four of the warp's items ahead and column indices two items
-      // ahead, into ring slots chosen by the (unrolled) item position, so a
-      // register is only read long after its load was issued.
+      // copied from the row-major [16][P_total] array (swizzled here) into the
+      // item's stage with the gather.  Work items of this warp: f = f0 + warp
+      // + PW*i.  Descriptors are loaded four of the warp's items ahead and
+      // column indices two items ahead, into ring slots chosen by the
+      // (unrolled) item position, so a register is only read long after its
+      // load was issued.
       const int4 *stg = reinterpret_cast<const int4 *>(p.stages);
       int4 ring_d[4];
       int32_t ring_lo[2], ring_hi[2];
@@ -263,15 +290,9 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         ring_lo[k] = lane < dd.z ? p.window_col_idx[static_cast<int64_t>(dd.x) + lane] : -2;
         ring_hi[k] = lane + 32 < dd.z ? p.window_col_idx[static_cast<int64_t>(dd.x) + 32 + lane] : -2;
       };
-      // value tile of item fi into slot (fi - f0) % kVQ, with the cp.async
-      // arrivals of this warp's 32 lanes
-      auto load_vals = [&](int64_t fi, const int4 &dd) -> bool {
-        if (fi >= f1) return true;
-        const int64_t it = fi - f0;
-        const uint32_t slot = static_cast<uint32_t>(it % kVQ);
-        if (!mbar_wait_warp(vempty0 + 8 * slot, static_cast<uint32_t>(((it / kVQ) & 1) ^ 1), p.wait_limit_ns))
-          return false;
-        const uint32_t vdst = smem_addr(vring + slot * kValBytes);
+      // value tile of descriptor dd -> the stage's value area (zeros past
+      // ncols: the MMA reads whole 16-column k-steps only up to ncols)
+      auto copy_vals = [&](uint32_t vdst, const int4 &dd) {
         if (dd.z > 0) {
           const uint16_t *Vp = reinterpret_cast<const uint16_t *>(p.values);
           const uint32_t u = static_cast<uint32_t>(lane & 7);
@@ -285,8 +306,6 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
                         in ? 16u : 0u);
           }
         }
-        cp_async_arrive_noinc(vfull0 + 8 * slot);
-        return true;
       };
       int64_t f = f0 + warp;
 #pragma unroll
@@ -294,8 +313,6 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
       load_idx(0, ring_d[0]);
       load_idx(1, ring_d[1]);
       bool ok = true;
-#pragma unroll
-      for (int u = 0; u < kVLead; ++u) ok = ok && load_vals(f + u * kStep, ring_d[u]);
       for (; f < f1 && ok; f += 4 * kStep) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -303,8 +320,6 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
           if (fi >= f1 || !ok) break;
           const int4 d = ring_d[u];
           const int32_t lo = ring_lo[u & 1], hi = ring_hi[u & 1];
-          ok = load_vals(fi + kVLead * kStep, ring_d[(u + kVLead) & 3]);
-          if (!ok) break;
           load_idx(u & 1, ring_d[(u + 2) & 3]);
           ring_d[u] = load_d(fi + 4 * kStep);
           const int64_t it = fi - f0;
@@ -320,6 +335,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
             stage_rec[stage] = StageRec{d.z, d.w, d.y, tile};  // released by this arrive
             mbar_arrive(fb);
           }
+          copy_vals(st + C_::kGatherBytes, d);
           gather(st, tile * C_::kBN, d.z, lo, hi);
           cp_async_arrive_noinc(fb);
         }
@@ -332,38 +348,44 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
     } else {
       // Every stage is one record in global memory (its value tile, its 64
       // column indices and its descriptor).  Warp w owns the work items
-      // f0 + w, f0 + w + 4, ...: it fetches an item's record with two TMA
-      // bulk copies (value ring, index ring) kVLead of its items ahead, then
-      // reads the indices and the descriptor from shared memory, so no
-      // global load stalls its issue behind the SM's outstanding gathers,
-      // and copies the item's B rows.  Four warps keep four items' barrier
-      // handling and copy issue in flight at once.
+      // f0 + w + PW*j (j = 0, 1, ...).  It fetches the index part of its
+      // item j's record (272 bytes) kILead of its items ahead into slot
+      // j % kILead of its ring, and when it starts item j it reads the indices
+      // from there (the slot is then refilled), waits for the item's stage to
+      // be free, has the value tile copied into the stage by TMA and copies
+      // the item's rows of B with cp.async.
       const uint8_t *pack = reinterpret_cast<const uint8_t *>(p.stage_pack);
-      int64_t f = f0 + warp;
-      // stage-list position of the item whose record this warp fetches next
-      int64_t fl = f;
-      int64_t s_lead = f % n_stages;
-      auto advance_pos = [&](int64_t &s) {
-        s += kStep;
-        while (s >= n_stages) s -= n_stages;
-      };
-      auto load_pack = [&]() {
-        if (fl < f1 && lane == 0) {
-          const uint32_t slot = static_cast<uint32_t>((fl - f0) % kVQ);
-          const uint8_t *src = pack + s_lead * kWcsrPackBytes;
-          mbar_arrive_expect_tx(vfull0 + 8 * slot, kWcsrPackBytes);
-          tma_bulk_load(smem_addr(vring + slot * kValBytes), src + kWcsrPackValOff, kValBytes, vfull0 + 8 * slot);
-          tma_bulk_load(smem_addr(mring + slot * kMetaBytes), src + kWcsrPackIdxOff, kMetaBytes, vfull0 + 8 * slot);
+      uint8_t *ring = iring + warp * kILead * kMetaBytes;
+      const uint32_t ifull_w = ifull0 + 8 * (warp * kILead);
+      auto fetch_idx = [&](int64_t j) {
+        const int64_t fj = f0 + warp + j * kStep;
+        if (fj < f1 && lane == 0) {
+          const uint32_t slot = static_cast<uint32_t>(j % kILead);
+          const uint8_t *src = pack + (fj % n_stages) * kWcsrPackBytes;
+          mbar_arrive_expect_tx(ifull_w + 8 * slot, kMetaBytes);
+          tma_bulk_load(smem_addr(ring + slot * kMetaBytes), src + kWcsrPackIdxOff, kMetaBytes, ifull_w + 8 * slot);
+          prefetch_l2_bulk(src + kWcsrPackValOff, kValBytes);
         }
-        fl += kStep;
-        advance_pos(s_lead);
       };
 #pragma unroll 1
-      for (int u = 0; u < kVLead; ++u) load_pack();
-      int64_t s_cur = f % n_stages;
-      int tile = static_cast<int>(f / n_stages);
+      for (int j = 0; j < kILead; ++j) fetch_idx(j);
       bool ok = true;
-      for (; f < f1; f += kStep) {
+      int64_t consumed = 0;  // own items whose indices were read; fetches of the next kILead are in flight
+      for (int64_t j = 0;; ++j) {
+        const int64_t f = f0 + warp + j * kStep;
+        if (f >= f1) break;
+        const uint32_t islot = static_cast<uint32_t>(j % kILead);
+        ok = mbar_wait_warp(ifull_w + 8 * islot, static_cast<uint32_t>((j / kILead) & 1), p.wait_limit_ns);
+        ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
+        if (!ok) break;
+        const uint8_t *meta = ring + islot * kMetaBytes;
+        const int4 d = *reinterpret_cast<const int4 *>(meta + (kWcsrPackDescOff - kWcsrPackIdxOff));
+        const int32_t lo = reinterpret_cast<const int32_t *>(meta)[lane];
+        const int32_t hi = reinterpret_cast<const int32_t *>(meta)[32 + lane];
+        fence_proxy_async_smem();  // these reads before the TMA refill of the slot
+        __syncwarp();
+        fetch_idx(j + kILead);
+        consumed = j + 1;
         const int64_t it = f - f0;
         const uint32_t stage = static_cast<uint32_t>(it % Q);
         const uint32_t phase = static_cast<uint32_t>((it / Q) & 1);
@@ -371,32 +393,25 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         ok = mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns);
         ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
         if (!ok) break;
-        load_pack();  // record of item it + kLead, into the slot of item it - Q
-        const uint32_t vslot = static_cast<uint32_t>(it % kVQ);
-        ok = mbar_wait_warp(vfull0 + 8 * vslot, static_cast<uint32_t>((it / kVQ) & 1), p.wait_limit_ns);
-        ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
-        if (!ok) break;
-        const uint8_t *meta = mring + vslot * kMetaBytes;
-        const int4 d = *reinterpret_cast<const int4 *>(meta + (kWcsrPackDescOff - kWcsrPackIdxOff));
-        const int32_t lo = reinterpret_cast<const int32_t *>(meta)[lane];
-        const int32_t hi = reinterpret_cast<const int32_t *>(meta)[32 + lane];
+        const int tile = static_cast<int>(f / n_stages);
+        const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
         const uint32_t fb = full0 + 8 * stage;
         if (lane == 0) {
           stage_rec[stage] = StageRec{d.x, d.y, d.z, tile};  // released by this arrive
-          mbar_arrive(fb);
+          mbar_arrive_expect_tx(fb, kValBytes);
+          tma_bulk_load(st + C_::kGatherBytes, pack + (f % n_stages) * kWcsrPackBytes + kWcsrPackValOff, kValBytes,
+                        fb);
         }
-        gather(smem_addr(smem + stage * C_::kStageBytes), tile * C_::kBN, d.x, lo, hi);
+        gather(st, tile * C_::kBN, d.x, lo, hi);
         cp_async_arrive_noinc(fb);
-        s_cur += kStep;
-        while (s_cur >= n_stages) {
-          s_cur -= n_stages;
-          ++tile;
-        }
       }
       cp_async_wait_all();
       if (!ok && lane == 0) {
         atomicOr(p.status, kDevTimeout);
         *abort_flag = 1;
+        // let the index records in flight land before the CTA exits
+        for (int64_t i = consumed; i < consumed + kILead && f0 + warp + i * kStep < f1; ++i)
+          mbar_wait(ifull_w + 8 * (i % kILead), static_cast<uint32_t>((i / kILead) & 1), 1000000ull);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -418,9 +433,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         return __shfl_sync(0xffffffffu, r && !*abort_flag, 0);
       };
       for (int64_t f = f0; f < f1 && ok; ++f) {
-        const uint32_t vslot = static_cast<uint32_t>((f - f0) % kVQ);
-        ok = mbar_wait_warp(full0 + 8 * stage, phase, p.wait_limit_ns) &&
-             mbar_wait_warp(vfull0 + 8 * vslot, static_cast<uint32_t>(((f - f0) / kVQ) & 1), p.wait_limit_ns);
+        ok = mbar_wait_warp(full0 + 8 * stage, phase, p.wait_limit_ns);
         ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
         if (!ok) break;
         const StageRec rec = stage_rec[stage];
@@ -440,8 +453,8 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         if (leader) {
           fence_proxy_async_smem();  // the stage's cp.async writes -> async-proxy MMA reads
           tc_fence_after_sync();
-          const uint32_t vals = smem_addr(vring + vslot * kValBytes);        // MMA operand B (K-major)
           const uint32_t gath = smem_addr(smem + stage * C_::kStageBytes);  // MMA operand A (MN-major)
+          const uint32_t vals = gath + C_::kGatherBytes;                     // MMA operand B (K-major)
           const int nacc = min(NACC, (p.N - rec.tile * C_::kBN + 127) / 128);
           const uint32_t acc = tmem + buf * C_::kAccCols;
           for (int kk = 0; kk < ksteps; ++kk) {
@@ -455,7 +468,6 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
             }
           }
           umma_commit(empty0 + 8 * stage);
-          if constexpr (NOALLOC) umma_commit(vempty0 + 8 * vslot);
         }
         ksteps_done += ksteps;
         if (seg_last) {
@@ -567,7 +579,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
 
 template <int NACC, int Q, int PW, int MINB, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_variant(const WcsrParams &p, cudaStream_t stream) {
-  using C_ = Cfg<NACC, Q, PW, MINB>;
+  using C_ = Cfg<NACC, Q, PW, MINB, kIdxLead>;
   auto kern = wcsr_spmm_kernel<NACC, Q, PW, MINB, IN_BF16, OUT_BF16>;
   static std::atomic<uint64_t> smem_set{0};  // per instantiation, one bit per device
   cudaError_t e = set_smem_limit_once(kern, C_::kSmemBytes, smem_set);
@@ -575,9 +587,8 @@ cudaError_t launch_variant(const WcsrParams &p, cudaStream_t stream) {
   kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  split_reduce_kernel<kH, OUT_BF16><<<2 * p.grid, 256, p.grid * sizeof(int32_t), stream>>>(
-      p.partials, p.workspace, kWcsrSlotFloats, 256, p.C, p.M, p.N, p.grid, C_::kBN);
-  return cudaGetLastError();
+  return launch_split_reduce<kH, OUT_BF16>(p.partials, p.workspace, kWcsrSlotFloats, 256, p.C, p.M, p.N, p.grid,
+                                           C_::kBN, stream);
 }
 
 template <int NACC, int Q, int PW, int MINB>
@@ -656,7 +667,7 @@ __global__ void __launch_bounds__(1024)
 
 template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_noalloc_variant(const WcsrParams &p, cudaStream_t stream) {
-  using C_ = Cfg<NACC, Q, 4, 1>;
+  using C_ = Cfg<NACC, Q, 4, 1, 0>;
   auto kern = wcsr_spmm_kernel<NACC, Q, 4, 1, IN_BF16, OUT_BF16, true>;
   static std::atomic<uint64_t> smem_set{0};  // per instantiation, one bit per device
   cudaError_t e = set_smem_limit_once(kern, C_::kSmemBytes, smem_set);
@@ -664,9 +675,8 @@ cudaError_t launch_noalloc_variant(const WcsrParams &p, cudaStream_t stream) {
   kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  split_reduce_kernel<kH, OUT_BF16><<<2 * p.grid, 256, p.grid * sizeof(int32_t), stream>>>(
-      p.partials, p.workspace, kWcsrSlotFloats, 256, p.C, p.M, p.N, p.grid, C_::kBN);
-  return cudaGetLastError();
+  return launch_split_reduce<kH, OUT_BF16>(p.partials, p.workspace, kWcsrSlotFloats, 256, p.C, p.M, p.N, p.grid,
+                                           C_::kBN, stream);
 }
 
 // Scratch of spmm_wcsr_run_noalloc: stage list, partial-sum slots (two per
@@ -739,8 +749,8 @@ int wcsr_ctas_per_sm(int64_t N) {
 
 cudaError_t launch_wcsr(const WcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream) {
   if (p.n_stages == 0 || p.N == 0 || p.grid == 0) return cudaSuccess;
-  if (p.N <= 128) return launch_dtypes<1, 5, 2, 2>(p, in_bf16, out_bf16, stream);
-  return launch_dtypes<2, 3, 2, 2>(p, in_bf16, out_bf16, stream);
+  if (p.N <= 128) return launch_dtypes<1, 5, 4, 2>(p, in_bf16, out_bf16, stream);
+  return launch_dtypes<2, 3, 3, 2>(p, in_bf16, out_bf16, stream);
 }
 
 }  // namespace spmm

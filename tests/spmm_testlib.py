@@ -32,7 +32,7 @@ def to_device_bits(bits, dtype):
 
 
 def run_library(fmt, m, k, rp, ci, vals, dtype, out_dtype, B_bits, b_row=None, b_col=None,
-                max_ctas=None, runs=1, keep_device=False):
+                max_ctas=None, runs=1, keep_device=False, schedule=None):
     """Create a handle, run `runs` times into NaN-filled C, check the device
     status; returns (list of C results as float64 numpy or torch, info)."""
     import torch
@@ -44,6 +44,8 @@ def run_library(fmt, m, k, rp, ci, vals, dtype, out_dtype, B_bits, b_row=None, b
     try:
         if max_ctas is not None:
             S.spmm_set_max_ctas(h, max_ctas)
+        if schedule is not None:
+            S.spmm_set_schedule(h, schedule)
         info = S.spmm_format_info(h)
         N = B_bits.shape[1]
         dB = to_device_bits(B_bits, dtype)

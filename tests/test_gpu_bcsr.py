@@ -70,18 +70,21 @@ def test_bcsr_parity_two_ctas_per_sm(m, k, n, keep, dt, out_dt):
     (200, 640, 520, 0.6, 11, "f32"),      # three 256-column tiles in one group, ragged last tile
 ])
 def test_bcsr_split_schedule(m, k, n, keep, ctas, out_dt):
-    """Problems with fewer tiles than two per SM take the split schedule:
-    equal stage shares per CTA, cut tiles finished by the partial-sum pass in
-    CTA order.  Compared element by element, and bitwise reproducible."""
+    """The split schedule (forced here; the automatic choice takes it for few,
+    long tiles): equal stage shares per CTA, cut tiles finished by the
+    partial-sum pass in CTA order.  Compared element by element and bitwise
+    reproducible; the tile schedule on the same input too."""
     rng = np.random.default_rng(m * 7 + n + (ctas or 0))
     rp, ci = W.block_pattern(rng, m, k, 64, 64, keep=keep)
     vals = W.draw_values(rng, len(ci), "u1", "bf16")
     B = W.dense_bits(rng, (k, n), "u1", "bf16")
-    outs, _ = run_library("bcsr", m, k, rp, ci, vals, "bf16", out_dt, B, max_ctas=ctas, runs=2)
+    outs, _ = run_library("bcsr", m, k, rp, ci, vals, "bf16", out_dt, B, max_ctas=ctas, runs=2, schedule=2)
     C_ref, S_ref = oracle.spmm_csr(m, k, rp, ci, vals, ocode("bf16"), B)
     for C in outs:
         assert_parity(C, C_ref, S_ref, f"bcsr split {m}x{k} N={n} ctas={ctas}")
     assert np.array_equal(outs[0], outs[1])
+    tiles, _ = run_library("bcsr", m, k, rp, ci, vals, "bf16", out_dt, B, max_ctas=ctas, schedule=1)
+    assert_parity(tiles[0], C_ref, S_ref, f"bcsr tiles {m}x{k} N={n} ctas={ctas}")
 
 
 def test_bcsr_many_block_rows_narrow_tiles():
