@@ -448,14 +448,31 @@ def run_sweep(args):
         if sel and name not in sel:
             continue
         cfgs.append((name, lambda b=b, n=sel.get(name): b(n)))
-    # single sweep points, e.g. bcsr_sweep_95_N256 or wcsr_sweep_0.1_N8
+    # a WCSR configuration in 64-row windows with column padding 8 (the
+    # paper's WCSR geometry): its name with the suffix _h64
+    def h64(ws):
+        for w in ws:
+            w.b_row, w.b_col = 64, 8
+            w.name += "_h64"
+            w.meta["desc"] = w.describe().replace(" h16 ", " h64 pad8 ")
+        return ws
+    for name, b in builders:
+        if name.startswith("wcsr") and name + "_h64" in sel:
+            cfgs.append((name + "_h64", lambda b=b, n=sel.get(name + "_h64"): h64(b(n))))
+    # single sweep points, e.g. bcsr_sweep_95_N256 or wcsr_sweep_0.1_N8 (or with _h64)
     for e in sel:
+        if e.startswith("wcsr_sweep_") and e.endswith("_h64"):
+            _, _, lvl, n = e[:-4].split("_")
+            cfgs.append((e, lambda lvl=float(lvl), n=int(n[1:]): h64([W.wcsr_sweep(lvl, n)])))
+            continue
         parts = e.split("_")
         if len(parts) == 4 and parts[0] in ("bcsr", "wcsr") and parts[1] == "sweep" and parts[3].startswith("N"):
             lvl, n = float(parts[2]), int(parts[3][1:])
             fn = (lambda lvl=lvl, n=n: [W.bcsr_sweep(int(lvl), n)]) if parts[0] == "bcsr" else \
                 (lambda lvl=lvl, n=n: [W.wcsr_sweep(lvl, n)])
             cfgs.append((e, fn))
+    if "linear_weight" in sel:
+        run_linear_sweep(args, peaks, stream, flush)
     for name, b in cfgs:
         cache = {}
         for w in b():
@@ -505,6 +522,56 @@ def run_sweep(args):
                 flush=True)
         for hh in cache.values():
             S.spmm_destroy(hh)
+
+
+def run_linear_sweep(args, peaks, stream, flush):
+    """The BCSR product in the layout of a linear layer (Y = X * A^T, X the
+    64K-token activations, A the 90 %-block-sparse gate projection), beside
+    dense torch.mm on the same box (cuBLAS; context, as the pages' Table III
+    sets their kernel beside torch.mm)."""
+    import torch
+    import sparse_dense_matrix_bcsr_gb300 as S
+    w = W.bcsr_weight()
+    sptr = stream.cuda_stream
+    h = S.spmm_bcsr_create(w.m, w.k, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype)
+    info = S.spmm_format_info(h)
+    X = torch.from_numpy(np.ascontiguousarray(w.B().T).view(np.int16)).cuda().view(torch.bfloat16)
+    Y = torch.empty((w.n, w.m), dtype=torch.bfloat16, device="cuda")
+
+    def timed(fn):
+        ms = []
+        for i in range(args.warmup + args.steps):
+            with torch.cuda.stream(stream):
+                flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            if i >= args.warmup:
+                ms.append((e0, e1))
+        stream.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ms)
+
+    t_ours = timed(lambda: S.spmm_run_linear(h, X.data_ptr(), Y.data_ptr(), w.n, sptr))
+    assert S.spmm_check(h, sptr) == S.SPMM_OK
+    dense = np.zeros((w.m, w.k), np.uint16)
+    rows = np.repeat(np.arange(w.m), np.diff(w.row_ptr))
+    dense[rows, w.col_idx] = w.vals
+    Wd = torch.from_numpy(dense.view(np.int16)).cuda().view(torch.bfloat16)
+    Yd = torch.empty_like(Y)
+    with torch.cuda.stream(stream):
+        t_mm = timed(lambda: torch.mm(X, Wd.t(), out=Yd))
+    S.spmm_destroy(h)
+    eff, stored_fl, bytes_min = part_model(w, info)
+    t = t_ours * 1e-3
+    t_tc = stored_fl / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = bytes_min / (peaks["hbm_gbs"] * 1e9)
+    print(json.dumps({
+        "config": "linear_weight", "workload": "Y = X * A^T, " + w.describe() + " (X: 65536 x 3584 rows)",
+        "fmt": "bcsr-linear", "N": w.n, "nnz": w.nnz, "ms_cold_median": round(t_ours, 5),
+        "eff_tflops": round(eff / t / 1e12, 3), "roofline_frac": round(max(t_tc, t_hbm) / t, 4),
+        "bound": "hbm" if t_hbm >= t_tc else "tensor", "t_roof_us": round(max(t_tc, t_hbm) * 1e6, 2),
+        "torch_mm_dense_ms": round(t_mm, 5), "speedup_vs_torch_mm": round(t_mm / t_ours, 3)}), flush=True)
 
 
 def main():

@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspmm_gb300.so")
 
-SOURCES = ["bcsr_kernel.cu", "bcsr_linear_kernel.cu", "wcsr_kernel.cu", "spmm_api.cu", "format.cpp"]
+SOURCES = ["bcsr_kernel.cu", "bcsr_linear_kernel.cu", "wcsr_kernel.cu", "wcsr64_kernel.cu", "spmm_api.cu",
+           "format.cpp"]
 HEADERS = ["ptx.cuh", "internal.h", "format.h", "split_reduce.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

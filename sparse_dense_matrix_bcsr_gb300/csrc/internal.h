@@ -117,6 +117,12 @@ constexpr int kWcsrPackValOff = 0;
 constexpr int kWcsrPackIdxOff = 2048;
 constexpr int kWcsrPackDescOff = 2048 + 256;
 constexpr int kWcsrPackBytes = 2048 + 256 + 16;
+// The same record for a window of h rows (16 or 64): an h x 64 value tile,
+// then the 64 indices and the descriptor.
+constexpr int wcsr_pack_idx_off(int h) { return h * 64 * 2; }
+constexpr int wcsr_pack_desc_off(int h) { return h * 64 * 2 + 256; }
+constexpr int wcsr_pack_bytes(int h) { return h * 64 * 2 + 256 + 16; }
+static_assert(wcsr_pack_bytes(16) == kWcsrPackBytes && wcsr_pack_bytes(64) % 16 == 0, "record layout");
 
 struct WcsrParams {
   const WcsrStage *stages;       // device, n_stages (the no-allocation variant's stage list)
@@ -140,6 +146,8 @@ struct WcsrParams {
 // times the SM count), and the most it can be (the partial-sum workspace is
 // sized for it).
 int wcsr_ctas_per_sm(int64_t N);
+// Columns of C per WCSR work item (window height 16) at dense width N.
+int wcsr_tile_cols(int64_t N);
 constexpr int kWcsrMaxCtasPerSm = 2;
 
 // Workspace floats per partial slot (16 rows x 256 columns).
@@ -160,6 +168,16 @@ size_t wcsr_noalloc_scratch_bytes();
 // Runs the SpMM kernel, then the kernel that adds the partials of windows
 // cut between CTAs.
 cudaError_t launch_wcsr(const WcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream);
+
+// WCSR with 64-row windows (wcsr64_kernel.cu): stage records of
+// wcsr_pack_bytes(64), 256-column tiles, whole windows stored through tmC
+// (C as [M rows, N cols], 32-row x 64-byte boxes, 64-byte swizzle), windows
+// cut between CTAs as 64 x 256 fp32 partials (kWcsr64SlotFloats per slot)
+// added by split_reduce_kernel.
+constexpr int64_t kWcsr64SlotFloats = 64 * 256;
+int wcsr64_ctas_per_sm();
+cudaError_t launch_wcsr64(const CUtensorMap &tmC, const WcsrParams &p, bool in_bf16, bool out_bf16,
+                          cudaStream_t stream);
 
 // Failure-detection self test: wait on an mbarrier nothing arrives at.
 cudaError_t launch_wait_selftest(uint32_t *status, uint64_t limit_ns, cudaStream_t stream);

@@ -84,11 +84,10 @@ spmm_status encode_2d(CUtensorMap *map, const void *base, bool bf16, uint64_t ro
 // bf16 or fp32.  Narrow (N <= 128) tiles store 16-row x 128-byte boxes with the
 // 128-byte swizzle, wide ones 32-row x 64-byte boxes with the 64-byte swizzle
 // (see bcsr_wide_tiles).
-spmm_status encode_c(CUtensorMap *map, void *base, bool bf16, uint64_t rows, uint64_t cols) {
+spmm_status encode_c(CUtensorMap *map, void *base, bool bf16, uint64_t rows, uint64_t cols, bool wide) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return fail(SPMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const uint64_t esz = bf16 ? 2 : 4;
-  const bool wide = spmm::bcsr_wide_tiles(static_cast<int64_t>(cols));
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * esz};
   cuuint32_t box[2] = {static_cast<cuuint32_t>((wide ? 64 : 128) / esz), wide ? 32u : 16u};
@@ -239,38 +238,42 @@ spmm_status upload_common(spmm_handle h, const HostFormat &f) {
 
 // The WCSR stage list: each window cut into stages of at most 64 packed
 // columns, in window order; a window without columns gets one empty stage.
-// The kernel reads each stage as one record (its 16 x 64 value tile, column
-// indices and descriptor; see kWcsrPackBytes).  In those records a window of
-// ns >= 2 stages deals its padded column list round-robin over its stages
-// (stage j takes positions j, j + ns, j + 2 ns, ...; positions past P_w are
-// padding), so each stage's rows of B span the whole window: packed columns
-// are sorted, and windows processed at the same time by different CTAs would
-// otherwise all gather from the same band of B rows and the same L2 slices.
-// The product is the same sum in another order.
+// The kernel reads each stage as one record (its H x 64 value tile, column
+// indices and descriptor; see wcsr_pack_bytes, H = the window height).  In
+// those records a window of ns >= 2 stages deals its padded column list
+// round-robin over its stages (stage j takes positions j, j + ns, j + 2 ns,
+// ...; positions past P_w are padding), so each stage's rows of B span the
+// whole window: packed columns are sorted, and windows processed at the same
+// time by different CTAs would otherwise all gather from the same band of B
+// rows and the same L2 slices.  The product is the same sum in another order.
+// A stage's column count is rounded up to the MMA's 16-deep k step with
+// padding positions (a column padding of 8 leaves odd multiples of 8).
 spmm_status build_stages(spmm_handle h, const std::vector<int64_t> &wptr, const std::vector<int32_t> &widx,
                          const std::vector<uint16_t> &wvals) {
   std::vector<spmm::WcsrStage> st;
   std::vector<uint8_t> pack;
   const int64_t nw = h->n_groups;
   const int64_t P = h->n_units;
-  // stage s's record at s * kWcsrPackBytes
+  const int H = h->b_row;
+  const size_t rec = static_cast<size_t>(spmm::wcsr_pack_bytes(H));
+  // stage s's record at s * rec
   auto new_stage = [&](int32_t p_begin, int32_t window, int32_t ncols, int32_t flags) -> size_t {
     const size_t s = st.size();
     st.push_back({p_begin, window, ncols, flags});
-    pack.resize(pack.size() + spmm::kWcsrPackBytes, 0);
-    int32_t *idx = reinterpret_cast<int32_t *>(&pack[s * spmm::kWcsrPackBytes + spmm::kWcsrPackIdxOff]);
-    for (int c = 0; c < 64; ++c) idx[c] = -2;
+    pack.resize(pack.size() + rec, 0);
+    int32_t *idx = reinterpret_cast<int32_t *>(&pack[s * rec + spmm::wcsr_pack_idx_off(H)]);
+    for (int c = 0; c < 64; ++c) idx[c] = c < ncols ? -1 : -2;
     const int32_t desc[4] = {ncols, flags, window, 0};
-    std::memcpy(&pack[s * spmm::kWcsrPackBytes + spmm::kWcsrPackDescOff], desc, sizeof desc);
+    std::memcpy(&pack[s * rec + spmm::wcsr_pack_desc_off(H)], desc, sizeof desc);
     return s;
   };
   auto put_val = [&](size_t s, int r, int c, uint16_t v) {
     // row r at r * 128 bytes, 16-byte unit u stored at unit u ^ (r % 8)
-    uint16_t *tile = reinterpret_cast<uint16_t *>(&pack[s * spmm::kWcsrPackBytes + spmm::kWcsrPackValOff]);
+    uint16_t *tile = reinterpret_cast<uint16_t *>(&pack[s * rec]);
     tile[r * 64 + (((c >> 3) ^ (r & 7)) << 3) + (c & 7)] = v;
   };
   auto put_idx = [&](size_t s, int c, int32_t col) {
-    std::memcpy(&pack[s * spmm::kWcsrPackBytes + spmm::kWcsrPackIdxOff + 4 * c], &col, 4);
+    std::memcpy(&pack[s * rec + spmm::wcsr_pack_idx_off(H) + 4 * c], &col, 4);
   };
   for (int64_t w = 0; w < nw; ++w) {
     const int64_t b = wptr[w], e = wptr[w + 1], pw = e - b;
@@ -281,28 +284,26 @@ spmm_status build_stages(spmm_handle h, const std::vector<int64_t> &wptr, const 
     const int64_t ns = (pw + 63) / 64;
     for (int64_t j = 0; j < ns; ++j) {
       const int32_t flags = (j == 0 ? spmm::kStageFirst : 0) | (j == ns - 1 ? spmm::kStageLast : 0);
-      const int32_t ncols = ns == 1 ? static_cast<int32_t>(pw) : 64;
+      const int32_t ncols = ns == 1 ? static_cast<int32_t>((pw + 15) / 16 * 16) : 64;
       const size_t s = new_stage(static_cast<int32_t>(b + 64 * j), static_cast<int32_t>(w), ncols, flags);
       for (int c = 0; c < ncols; ++c) {
         const int64_t q = ns == 1 ? c : j + ns * c;  // position within the window
-        if (q >= pw) {
-          put_idx(s, c, -1);  // padding: zero values, no B row
-          continue;
-        }
+        if (q >= pw) continue;                       // padding: zero values, no B row
         put_idx(s, c, widx[b + q]);
-        for (int r = 0; r < 16; ++r) put_val(s, r, c, wvals[r * P + b + q]);
+        for (int r = 0; r < H; ++r) put_val(s, r, c, wvals[r * P + b + q]);
       }
     }
   }
   h->n_stages = static_cast<int64_t>(st.size());
   h->stage_first.resize(st.size());
   for (size_t i = 0; i < st.size(); ++i) h->stage_first[i] = st[i].flags & spmm::kStageFirst;
-  CUDA_TRY(cudaMalloc(&h->d_stage_pack, std::max<size_t>(pack.size(), spmm::kWcsrPackBytes)), "cudaMalloc(stage records)");
+  CUDA_TRY(cudaMalloc(&h->d_stage_pack, std::max<size_t>(pack.size(), rec)), "cudaMalloc(stage records)");
   if (!pack.empty())
     CUDA_TRY(cudaMemcpy(h->d_stage_pack, pack.data(), pack.size(), cudaMemcpyHostToDevice), "upload stage records");
   // Two partial slots per CTA, sized for the largest grid.
   h->ws_slots = 2 * static_cast<int64_t>(spmm::kWcsrMaxCtasPerSm) * std::max(h->num_sms, 1);
-  CUDA_TRY(cudaMalloc(&h->d_ws, h->ws_slots * spmm::kWcsrSlotFloats * sizeof(float)), "cudaMalloc(workspace)");
+  const int64_t slot_floats = H == 64 ? spmm::kWcsr64SlotFloats : spmm::kWcsrSlotFloats;
+  CUDA_TRY(cudaMalloc(&h->d_ws, h->ws_slots * slot_floats * sizeof(float)), "cudaMalloc(workspace)");
   CUDA_TRY(cudaMalloc(&h->d_partials, h->ws_slots * sizeof(spmm::PartialRec)), "cudaMalloc(partials)");
   return SPMM_OK;
 }
@@ -350,11 +351,11 @@ int32_t bcsr_split_grid(spmm_handle h, int64_t N) {
 
 // Persistent grid of the WCSR kernel for N columns.
 int32_t wcsr_grid(spmm_handle h, int64_t N) {
-  const int64_t bn = N <= 128 ? 128 : 256;
+  const int64_t bn = h->b_row == 64 ? 256 : spmm::wcsr_tile_cols(N);
   const int64_t items = h->n_stages * ((N + bn - 1) / bn);
   const int64_t most = static_cast<int64_t>(spmm::kWcsrMaxCtasPerSm) * h->num_sms;
-  int64_t g = h->max_ctas > 0 ? std::min<int64_t>(h->max_ctas, most)
-                              : static_cast<int64_t>(spmm::wcsr_ctas_per_sm(N)) * h->num_sms;
+  const int per_sm = h->b_row == 64 ? spmm::wcsr64_ctas_per_sm() : spmm::wcsr_ctas_per_sm(N);
+  int64_t g = h->max_ctas > 0 ? std::min<int64_t>(h->max_ctas, most) : static_cast<int64_t>(per_sm) * h->num_sms;
   return static_cast<int32_t>(std::max<int64_t>(0, std::min(g, items)));
 }
 
@@ -384,7 +385,8 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
       h->n_cached = N;
     }
     if (h->c_cached != C || h->nc_cached != N) {
-      spmm_status st = encode_c(&h->tm_C, C, out_bf16, static_cast<uint64_t>(h->m), static_cast<uint64_t>(N));
+      spmm_status st = encode_c(&h->tm_C, C, out_bf16, static_cast<uint64_t>(h->m), static_cast<uint64_t>(N),
+                                spmm::bcsr_wide_tiles(N));
       if (st != SPMM_OK) return st;
       h->c_cached = C;
       h->nc_cached = N;
@@ -415,8 +417,17 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
     return SPMM_OK;
   }
   // WCSR
-  if (h->b_row != 16 || h->b_col % 16 != 0)
-    return fail(SPMM_ERR_UNSUPPORTED, "the WCSR kernel takes window height 16 and column padding a multiple of 16");
+  const bool w64 = h->b_row == 64;
+  if (!((h->b_row == 16 && h->b_col % 16 == 0) || (w64 && h->b_col % 8 == 0)))
+    return fail(SPMM_ERR_UNSUPPORTED,
+                "the WCSR kernels take window height 16 with column padding a multiple of 16, or window height 64 "
+                "with column padding a multiple of 8");
+  if (w64 && (h->c_cached != C || h->nc_cached != N)) {
+    spmm_status st = encode_c(&h->tm_C, C, out_bf16, static_cast<uint64_t>(h->m), static_cast<uint64_t>(N), true);
+    if (st != SPMM_OK) return st;
+    h->c_cached = C;
+    h->nc_cached = N;
+  }
   spmm::WcsrParams p;
   p.stages = nullptr;
   p.stage_pack = h->d_stage_pack;
@@ -435,7 +446,7 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
   p.grid = wcsr_grid(h, N);
   p.status = h->d_status;
   p.wait_limit_ns = h->wait_limit_ns;
-  cudaError_t e = spmm::launch_wcsr(p, in_bf16, out_bf16, s);
+  cudaError_t e = w64 ? spmm::launch_wcsr64(h->tm_C, p, in_bf16, out_bf16, s) : spmm::launch_wcsr(p, in_bf16, out_bf16, s);
   if (e != cudaSuccess) return cuda_fail(e, "WCSR kernel launch");
   return SPMM_OK;
 }
@@ -547,7 +558,7 @@ spmm_status spmm_wcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64
   h->n_units = f.n_units;
   h->stored = f.n_units * window_h;
   st = upload_common(h, f);
-  if (st == SPMM_OK) st = build_stages(h, f.ptr, f.idx, f.vals);
+  if (st == SPMM_OK && (window_h == 16 || window_h == 64)) st = build_stages(h, f.ptr, f.idx, f.vals);
   if (st != SPMM_OK) {
     free_handle(h);
     return st;

@@ -747,9 +747,15 @@ int wcsr_ctas_per_sm(int64_t N) {
   return 2;
 }
 
+// Whether N > 128 takes 256-column work items (one gather of a full B row
+// per stage) instead of 128-column ones.
+constexpr bool kWideTiles = true;
+
+int wcsr_tile_cols(int64_t N) { return (N <= 128 || !kWideTiles) ? 128 : 256; }
+
 cudaError_t launch_wcsr(const WcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream) {
   if (p.n_stages == 0 || p.N == 0 || p.grid == 0) return cudaSuccess;
-  if (p.N <= 128) return launch_dtypes<1, 5, 4, 2>(p, in_bf16, out_bf16, stream);
+  if (wcsr_tile_cols(p.N) == 128) return launch_dtypes<1, 5, 4, 2>(p, in_bf16, out_bf16, stream);
   return launch_dtypes<2, 3, 3, 2>(p, in_bf16, out_bf16, stream);
 }
 

@@ -57,6 +57,7 @@ CASES = [
     (1, 1, 1.0, 64, 64), (100, 37, 0.05, 64, 64), (300, 500, 0.01, 64, 64), (64, 4096, 0.002, 64, 64),
     (257, 129, 0.2, 16, 16), (1000, 800, 0.003, 16, 16), (33, 1000, 0.05, 16, 32), (0, 10, 0.1, 16, 16),
     (50, 50, 0.0, 16, 16), (17, 19, 0.3, 4, 4), (129, 200, 0.1, 8, 16),
+    (300, 700, 0.02, 64, 8), (1000, 1000, 0.01, 64, 8), (65, 129, 0.1, 64, 16),
 ]
 
 

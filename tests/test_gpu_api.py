@@ -25,8 +25,10 @@ def small(fmt, S):
     rp, ci, vals = W.random_csr(rng, 200, 300, 0.05, "bf16")
     if fmt == "bcsr":
         h = S.spmm_bcsr_create(200, 300, rp, ci, vals, "bf16", "f32")
-    else:
+    elif fmt == "wcsr":
         h = S.spmm_wcsr_create(200, 300, rp, ci, vals, "bf16", "f32")
+    else:
+        h = S.spmm_wcsr_create(200, 300, rp, ci, vals, "bf16", "f32", 64, 8)
     return h, rp, ci, vals
 
 
@@ -48,7 +50,7 @@ def test_run_argument_errors(S, fmt):
         S.spmm_destroy(h)
 
 
-@pytest.mark.parametrize("fmt", ["bcsr", "wcsr"])
+@pytest.mark.parametrize("fmt", ["bcsr", "wcsr", "wcsr64"])
 def test_device_format_matches_oracle(S, fmt):
     h, rp, ci, vals = small(fmt, S)
     try:
@@ -57,8 +59,10 @@ def test_device_format_matches_oracle(S, fmt):
         S.spmm_destroy(h)
     if fmt == "bcsr":
         ref = oracle.bcsr_build(200, 300, rp, ci, vals, 64, 64)
-    else:
+    elif fmt == "wcsr":
         ref = oracle.wcsr_build(200, 300, rp, ci, vals, 16, 16)
+    else:
+        ref = oracle.wcsr_build(200, 300, rp, ci, vals, 64, 8)
     for x, y in zip(ref, got):
         assert np.array_equal(x, y)
 

@@ -132,3 +132,72 @@ def test_wcsr_irregular_full_size():
 @pytest.mark.parametrize("n", W.SWEEP_N)
 def test_wcsr_sweep_full_size_sampled(dens, n):
     sampled_check(W.wcsr_sweep(dens, n))
+
+
+# ---------------------------------------------------------------- 64-row windows
+@pytest.mark.parametrize("m,k,n,d,pad,out_dt,ctas", [
+    (512, 512, 256, 0.05, 8, "f32", None),
+    (1000, 3000, 256, 0.01, 8, "f32", None),
+    (333, 777, 72, 0.03, 8, "f32", None),        # ragged window, N < 256: live columns only
+    (256, 2048, 264, 0.02, 16, "bf16", None),    # two column tiles + tail, bf16 C
+    (64, 64, 8, 0.2, 8, "f32", None),            # N = 8
+    (400, 5000, 256, 0.02, 8, "f32", 3),         # few CTAs: windows cut between CTAs
+    (400, 5000, 136, 0.02, 8, "bf16", 7),
+])
+def test_wcsr64_parity(m, k, n, d, pad, out_dt, ctas):
+    """Windows of 64 rows with column padding 8 or 16 (the paper's WCSR
+    configuration, Section IV-A), element by element against the oracle and
+    bitwise reproducible."""
+    rng = np.random.default_rng(m + 3 * n + pad)
+    rp, ci, vals = W.random_csr(rng, m, k, d, "bf16")
+    B = W.dense_bits(rng, (k, n), "n1", "bf16")
+    outs, info = run_library("wcsr", m, k, rp, ci, vals, "bf16", out_dt, B, b_row=64, b_col=pad,
+                             max_ctas=ctas, runs=2)
+    C_ref, S_ref = oracle.spmm_csr(m, k, rp, ci, vals, ocode("bf16"), B)
+    for C in outs:
+        assert_parity(C, C_ref, S_ref, f"wcsr64 {m}x{k} N={n} pad={pad}")
+    assert np.array_equal(outs[0], outs[1])
+    if ctas:
+        assert info["n_split_windows"] > 0
+
+
+def test_wcsr64_long_window_over_many_ctas():
+    rng = np.random.default_rng(23)
+    m, k, n = 192, 6000, 264
+    cols = [np.sort(rng.choice(k, 3000 if i == 70 else 5, replace=False)) for i in range(m)]
+    rp = np.zeros(m + 1, np.int64)
+    rp[1:] = np.cumsum([len(c) for c in cols])
+    ci = np.concatenate(cols).astype(np.int32)
+    vals = W.draw_values(rng, len(ci), "u1", "bf16")
+    B = W.dense_bits(rng, (k, n), "u1", "bf16")
+    outs, _ = run_library("wcsr", m, k, rp, ci, vals, "bf16", "f32", B, b_row=64, b_col=8, max_ctas=11)
+    C_ref, S_ref = oracle.spmm_csr(m, k, rp, ci, vals, ocode("bf16"), B)
+    assert_parity(outs[0], C_ref, S_ref, "wcsr64 long window")
+
+
+def test_wcsr64_identity_and_empty_windows_exact():
+    m = 300
+    n = 24
+    keep = np.ones(m, bool)
+    keep[64:192] = False  # two empty windows
+    rows = np.nonzero(keep)[0]
+    rp = np.zeros(m + 1, np.int64)
+    np.cumsum(np.bincount(rows, minlength=m), out=rp[1:])
+    ci = rows.astype(np.int32)
+    one = W.f32_to_bf16_bits(np.ones(len(ci), np.float32))
+    B = W.dense_bits(np.random.default_rng(2), (m, n), "n1", "bf16")
+    outs, _ = run_library("wcsr", m, m, rp, ci, one, "bf16", "f32", B, b_row=64, b_col=8)
+    ref = W.bits_to_f32(B, "bf16").astype(np.float64)
+    ref[64:192] = 0
+    assert np.array_equal(outs[0], ref)
+
+
+def test_wcsr64_uniform_full_size():
+    """The uniform workload (16384^2, 1 %, N = 256) in 64-row windows, every
+    element compared with the oracle."""
+    w = W.wcsr_uniform()
+    outs, info = run_library("wcsr", w.m, w.k, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.B(),
+                             b_row=64, b_col=8)
+    C_ref, S_ref = oracle.spmm_csr(w.m, w.k, w.row_ptr, w.col_idx, w.vals, ocode(w.dtype), w.B())
+    assert_parity(outs[0], C_ref, S_ref, "wcsr_uniform h64")
+    assert info["n_groups"] == 256
