@@ -107,7 +107,10 @@ spmm_status spmm_bcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64
  * array [window_h][P_total]: element (r, p) is A[window_h*w + r][col(p)] for
  * the window w owning position p, 0 where absent or padded.
  * Arguments as for spmm_bcsr_create; window_h and col_pad in 1..256.
- * spmm_run needs window_h == 16 and col_pad a multiple of 16.
+ * spmm_run takes window_h == 16 with col_pad a multiple of 16 (the window
+ * rows are the N = 16 operand of a transposed MMA), or window_h == 64 with
+ * col_pad a multiple of 8 (the paper's geometry, Section IV-A: the window rows
+ * are the M = 64 operand); other shapes are rejected by spmm_run.
  * Windows are cut into stages of at most 64 packed columns; each persistent
  * CTA takes an equal number of stages (see spmm_set_max_ctas).
  */
@@ -248,6 +251,22 @@ spmm_status spmm_set_schedule(spmm_handle h, int32_t schedule);
  * when the bound works).  timeout_ns must be in [1000, 10^10].
  */
 spmm_status spmm_selftest_wait_timeout(int64_t timeout_ns, void *stream, int32_t *dev_status);
+
+/*
+ * spmm_probe_l2_read -- measurement helper, not part of the product: reads
+ * `bytes` of device memory at `buf`, `passes` times, with 16-byte loads that
+ * bypass L1, from four CTAs of 512 threads per SM, enqueued on `stream`.  With
+ * a buffer that stays in L2 (a few tens of MB) and one untimed pass first,
+ * the caller's CUDA-event time gives the L2-to-SM read rate, the ceiling of
+ * the WCSR gather, which fetches rows of an L2-resident B by index
+ * (Section III-B).
+ *   buf    device pointer, 16-byte aligned; bytes > 0 and a multiple of 16.
+ *   sink   device pointer to 16 writable bytes; written only when the XOR of
+ *          the data read equals a fixed constant (it keeps the loads alive).
+ * Errors: INVALID_ARG (null pointers, bytes, passes < 1, alignment); CUDA
+ * (launch).  Asynchronous.
+ */
+spmm_status spmm_probe_l2_read(const void *buf, int64_t bytes, int32_t passes, void *sink, void *stream);
 
 /*
  * spmm_wcsr_run_noalloc -- C = A * B for A in WCSR, for callers that cannot

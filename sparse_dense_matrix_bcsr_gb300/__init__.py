@@ -49,6 +49,7 @@ EXPORTS = (
     "spmm_format_info", "spmm_export_format", "spmm_bcsr_convert", "spmm_wcsr_convert",
     "spmm_check", "spmm_set_max_ctas", "spmm_selftest_wait_timeout", "spmm_status_str",
     "spmm_last_error", "spmm_wcsr_run_noalloc", "spmm_run_linear", "spmm_set_schedule",
+    "spmm_probe_l2_read",
 )
 
 
@@ -98,6 +99,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "spmm_set_max_ctas": [P, ctypes.c_int32],
         "spmm_set_schedule": [P, ctypes.c_int32],
         "spmm_selftest_wait_timeout": [I64, P, ctypes.POINTER(ctypes.c_int32)],
+        "spmm_probe_l2_read": [P, I64, I32, P, P],
         "spmm_wcsr_run_noalloc": [P, P, P, I64, I64, I64, I32, I32, P, P, I64, P],
     }
     for name, args in sig.items():
@@ -234,6 +236,11 @@ def spmm_selftest_wait_timeout(timeout_ns: int, stream: int = 0) -> int:
     _check(load_library().spmm_selftest_wait_timeout(timeout_ns, stream or None, ctypes.byref(out)),
            "spmm_selftest_wait_timeout")
     return out.value
+
+
+def spmm_probe_l2_read(buf: int, nbytes: int, passes: int, sink: int, stream: int = 0) -> None:
+    """Enqueue `passes` reads of nbytes at device pointer buf (measurement helper)."""
+    _check(load_library().spmm_probe_l2_read(buf, nbytes, passes, sink, stream or None), "spmm_probe_l2_read")
 
 
 def spmm_wcsr_run_noalloc(window_row_ptr: int, window_col_idx: int, values: int, m: int, k: int, p_total: int,

@@ -58,11 +58,7 @@ namespace {
 constexpr int kBlk = 64;                      // block rows = block cols = K per block
 constexpr int kBlkBytes = kBlk * kBlk * 2;    // one 64x64 16-bit block
 constexpr int kChunkBytes = 64 * 64 * 2;      // 64 rows (k) x 64 columns (n) of B
-constexpr int kTmaWarp = 0;
-constexpr int kMmaWarp = 1;
-constexpr int kEpiWarp0 = 2;
 constexpr int kEpiWarps = 4;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kBoxBytes = 2048;               // one TMA store box of C in shared memory
 
 // Stage record flags (producer -> MMA) and accumulator record flags (MMA -> epilogue).
@@ -84,7 +80,9 @@ struct TileRec {
 
 // BN columns per tile, Q pipeline stages, NBUF TMEM accumulators, the
 // epilogue writing each warp's share of a tile in PARTS column parts through
-// two alternating staging buffers, MINB CTAs per SM.
+// two alternating staging buffers, MINB CTAs per SM, PW producer warps (warp
+// w issues the stages s with s % PW == w; warps PW and PW+1..PW+4 are the MMA
+// issuer and the epilogue).
 //
 // Narrow tiles (BN = 128) use the plain MMA, M = 64 x N = 128: the
 // accumulator's rows 16s..16s+15 sit in TMEM lanes 32s..32s+15, so epilogue
@@ -94,8 +92,11 @@ struct TileRec {
 // columns 0..127 and in lanes 64..127 for columns 128..255, in 128 TMEM
 // columns, so warp s holds rows 32(s%2)..32(s%2)+31 x columns 128(s/2) ..
 // 128(s/2)+127 and stores 32-row x 64-byte boxes (64-byte swizzle).
-template <int BN, int Q, int NBUF, int PARTS, int MINB, bool OUT_BF16>
+template <int BN, int Q, int NBUF, int PARTS, int MINB, int PW, bool OUT_BF16>
 struct Cfg {
+  static constexpr int kMmaWarp = PW;
+  static constexpr int kEpiWarp0 = PW + 1;
+  static constexpr int kThreads = 32 * (PW + 1 + kEpiWarps);
   static constexpr int kBN = BN;
   static constexpr bool kWS = BN >= 256;                      // weight-stationary MMA
   static constexpr int kNmma = BN < 256 ? BN : 256;           // N of one MMA
@@ -123,6 +124,10 @@ struct Cfg {
   static_assert(kSmemBytes <= 227 * 1024 && MINB * (kSmemBytes + 1024) <= 228 * 1024, "shared memory");
   static_assert(MINB * kTmemCols <= 512 && (kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512), "TMEM");
   static_assert((2 * Q + 6) * 8 + (Q + 2) * 16 + 16 <= kMiscBytes, "barrier area");
+  // A producer warp waits on a stage's empty barrier once per use of that
+  // stage it owns; with PW <= Q the phase it waits for is never two phases
+  // ahead of the barrier, so the parity test cannot pass early.
+  static_assert(PW >= 1 && PW <= Q, "producer warps");
   static_assert(BN % 128 == 0 && BN <= 256 && kNmma % 16 == 0 && kPartBoxes >= 1 && PARTS % 2 == 0 &&
                     kPartGroups % kBatch == 0, "tile shape");
 };
@@ -140,11 +145,13 @@ __device__ __forceinline__ void tile_coords(int64_t t, int n_block_rows, int n_c
   nt = static_cast<int>(g) * kGroupN + static_cast<int>(r % gsz);
 }
 
-template <int BN, int Q, int NBUF, int PARTS, int MINB, bool IN_BF16, bool OUT_BF16>
-__global__ void __launch_bounds__(kThreads, MINB)
+template <int BN, int Q, int NBUF, int PARTS, int MINB, int PW, bool IN_BF16, bool OUT_BF16>
+__global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, OUT_BF16>::kThreads, MINB)
     bcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const BcsrParams p) {
-  using C_ = Cfg<BN, Q, NBUF, PARTS, MINB, OUT_BF16>;
+  using C_ = Cfg<BN, Q, NBUF, PARTS, MINB, PW, OUT_BF16>;
+  constexpr int kMmaWarp = C_::kMmaWarp;
+  constexpr int kEpiWarp0 = C_::kEpiWarp0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *staging = smem + Q * C_::kStageBytes;
@@ -195,13 +202,18 @@ __global__ void __launch_bounds__(kThreads, MINB)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kTmaWarp) {
+  if (warp < PW) {
     // ------------------------------------------------------------ producer
+    // Every producer warp walks the same stage sequence; warp pw claims and
+    // issues the stages s with s % PW == pw and only counts the others.
+    const int pw = warp;
     uint32_t stage = 0, phase = 0;
     int64_t seq = 0;  // stages produced
     bool ok = true;
-    // Waits (whole warp) until the current stage is free.
+    auto mine = [&]() { return PW == 1 || static_cast<int>(seq % PW) == pw; };
+    // Waits (whole warp) until the current stage is free, if it is this warp's.
     auto claim = [&]() -> bool {
+      if (!mine()) return true;
       const bool r = mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns);
       return __shfl_sync(0xffffffffu, r && !*abort_flag, 0);
     };
@@ -216,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     // and, unless the block row is empty, the TMA loads of block j and of the
     // 64 rows of B it multiplies (block column bcol) for column tile nt.
     auto issue = [&](int br, int nt, int64_t j, int32_t bcol, int32_t flags) {
-      if (lane == 0) {
+      if (lane == 0 && mine()) {
         tile_rec[stage] = TileRec{br, nt, flags, 0};
         const uint32_t fb = full0 + 8 * stage;
         if (flags & kRecEmpty) {
@@ -357,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, MINB)
     if (ok) {
       // end marker for the MMA thread
       ok = claim();
-      if (ok && lane == 0) {
+      if (ok && lane == 0 && mine()) {
         tile_rec[stage] = TileRec{-1, -1, kRecEnd, 0};
         mbar_arrive(full0 + 8 * stage);
       }
@@ -368,7 +380,8 @@ __global__ void __launch_bounds__(kThreads, MINB)
       // Let the loads already in flight land before the CTA exits.
       const int64_t first = seq > Q ? seq - Q : 0;
       for (int64_t i = first; i < seq; ++i)
-        mbar_wait(full0 + 8 * (i % Q), static_cast<uint32_t>((i / Q) & 1), 1000000ull);
+        if (PW == 1 || static_cast<int>(i % PW) == pw)
+          mbar_wait(full0 + 8 * (i % Q), static_cast<uint32_t>((i / Q) & 1), 1000000ull);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -616,11 +629,11 @@ __global__ void __launch_bounds__(kThreads, MINB)
   }
 }
 
-template <int BN, int Q, int NBUF, int PARTS, int MINB, bool IN_BF16, bool OUT_BF16>
+template <int BN, int Q, int NBUF, int PARTS, int MINB, int PW, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_variant(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                            const BcsrParams &p, cudaStream_t stream) {
-  using C_ = Cfg<BN, Q, NBUF, PARTS, MINB, OUT_BF16>;
-  auto kern = bcsr_spmm_kernel<BN, Q, NBUF, PARTS, MINB, IN_BF16, OUT_BF16>;
+  using C_ = Cfg<BN, Q, NBUF, PARTS, MINB, PW, OUT_BF16>;
+  auto kern = bcsr_spmm_kernel<BN, Q, NBUF, PARTS, MINB, PW, IN_BF16, OUT_BF16>;
   static std::atomic<uint64_t> smem_set{0};  // per instantiation, one bit per device
   cudaError_t e = set_smem_limit_once(kern, C_::kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
@@ -632,18 +645,18 @@ cudaError_t launch_variant(const CUtensorMap &tmA, const CUtensorMap &tmB, const
     const int64_t cap = p.max_ctas > 0 ? p.max_ctas : static_cast<int64_t>(MINB) * p.num_sms;
     grid = tiles < cap ? tiles : cap;
   }
-  kern<<<static_cast<unsigned>(grid), kThreads, C_::kSmemBytes, stream>>>(tmA, tmB, tmC, p);
+  kern<<<static_cast<unsigned>(grid), C_::kThreads, C_::kSmemBytes, stream>>>(tmA, tmB, tmC, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.split_grid == 0) return e;
   return launch_split_reduce<kBlk, OUT_BF16>(p.partials, p.workspace, kBcsrSlotFloats, BN, p.C, p.M, p.N,
                                              static_cast<int32_t>(grid), BN, stream);
 }
 
-template <int BN, int Q, int NBUF, int PARTS, int MINB, bool OUT_BF16>
+template <int BN, int Q, int NBUF, int PARTS, int MINB, int PW, bool OUT_BF16>
 cudaError_t launch_in(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const BcsrParams &p,
                       bool in_bf16, cudaStream_t s) {
-  return in_bf16 ? launch_variant<BN, Q, NBUF, PARTS, MINB, true, OUT_BF16>(tmA, tmB, tmC, p, s)
-                 : launch_variant<BN, Q, NBUF, PARTS, MINB, false, OUT_BF16>(tmA, tmB, tmC, p, s);
+  return in_bf16 ? launch_variant<BN, Q, NBUF, PARTS, MINB, PW, true, OUT_BF16>(tmA, tmB, tmC, p, s)
+                 : launch_variant<BN, Q, NBUF, PARTS, MINB, PW, false, OUT_BF16>(tmA, tmB, tmC, p, s);
 }
 
 }  // namespace
@@ -664,17 +677,17 @@ cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
   // or 16 fp32 columns).
   if (!bcsr_wide_tiles(p.N)) {
     if (p.split_grid > 0)
-      return out_bf16 ? launch_in<128, 3, 2, 2, 2, true>(tmA, tmB, tmC, p, in_bf16, stream)
-                      : launch_in<128, 3, 2, 2, 2, false>(tmA, tmB, tmC, p, in_bf16, stream);
-    return out_bf16 ? launch_in<128, 6, 2, 2, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
-                    : launch_in<128, 6, 2, 2, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
+      return out_bf16 ? launch_in<128, 3, 2, 2, 2, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                      : launch_in<128, 3, 2, 2, 2, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
+    return out_bf16 ? launch_in<128, 6, 2, 2, 1, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                    : launch_in<128, 6, 2, 2, 1, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
   }
   const int64_t tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + 255) / 256);
   if (tiles < 2ll * p.num_sms && p.split_grid == 0)
-    return out_bf16 ? launch_in<256, 4, 2, 4, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
-                    : launch_in<256, 4, 2, 8, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
-  return out_bf16 ? launch_in<256, 2, 2, 4, 2, true>(tmA, tmB, tmC, p, in_bf16, stream)
-                  : launch_in<256, 2, 2, 8, 2, false>(tmA, tmB, tmC, p, in_bf16, stream);
+    return out_bf16 ? launch_in<256, 4, 2, 4, 1, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                    : launch_in<256, 4, 2, 8, 1, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
+  return out_bf16 ? launch_in<256, 2, 2, 4, 2, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                  : launch_in<256, 2, 2, 8, 2, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
 }
 
 }  // namespace spmm

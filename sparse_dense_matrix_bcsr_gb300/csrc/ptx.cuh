@@ -94,6 +94,21 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, ui
   }
 }
 
+// The same whole-warp wait without sleeping between probes: try_wait itself
+// suspends the warp until the phase completes or a hardware time slice ends,
+// so the waiter resumes as soon as the phase flips instead of up to twice the
+// sleep interval later.  For roles on the critical path of a pipeline whose
+// loads are TMA copies (nothing else in the CTA issues cp.async).
+__device__ __forceinline__ bool mbar_wait_warp_spin(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const long long limit_cycles = static_cast<long long>(limit_ns) * 21 / 10;
+  const long long t0 = clock64();
+  while (true) {
+    int state = mbar_try_wait(bar, parity) ? 1 : (clock64() - t0 > limit_cycles ? 2 : 0);
+    state = __shfl_sync(0xffffffffu, state, 0);
+    if (state != 0) return state == 1;
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -820,3 +820,46 @@ extern "C" spmm_status spmm_selftest_wait_timeout(int64_t timeout_ns, void *stre
   *dev_status = (word & spmm::kDevTimeout) ? SPMM_ERR_TIMEOUT : SPMM_OK;
   return SPMM_OK;
 }
+
+// ---------------------------------------------------------------- L2 read probe
+namespace spmm {
+namespace {
+// Every thread streams 16-byte loads that bypass L1 (ld.global.cg) with four
+// in flight; the XOR of the data decides a store nobody expects, so the loads
+// cannot be dropped.
+__global__ void __launch_bounds__(512) l2_read_kernel(const uint4 *__restrict__ buf, int64_t n16, int32_t passes,
+                                                      uint4 *sink) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  uint32_t acc = 0;
+  for (int32_t pass = 0; pass < passes; ++pass) {
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n16; i += 4 * stride) {
+      const uint4 a = __ldcg(buf + i), b = __ldcg(buf + i + stride);
+      const uint4 c = __ldcg(buf + i + 2 * stride), d = __ldcg(buf + i + 3 * stride);
+      acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^ d.z ^ d.w;
+    }
+    for (; i < n16; i += stride) {
+      const uint4 a = __ldcg(buf + i);
+      acc ^= a.x ^ a.y ^ a.z ^ a.w;
+    }
+  }
+  if (acc == 0x9E3779B9u && threadIdx.x == blockDim.x - 1) sink[0] = make_uint4(acc, blockIdx.x, 0, 0);
+}
+}  // namespace
+}  // namespace spmm
+
+extern "C" spmm_status spmm_probe_l2_read(const void *buf, int64_t bytes, int32_t passes, void *sink,
+                                          void *stream) {
+  if (!buf || !sink) return fail(SPMM_ERR_INVALID_ARG, "buf or sink is NULL");
+  if (bytes <= 0 || bytes % 16 != 0) return fail(SPMM_ERR_INVALID_ARG, "bytes must be positive and a multiple of 16");
+  if (passes < 1) return fail(SPMM_ERR_INVALID_ARG, "passes < 1");
+  if ((reinterpret_cast<uintptr_t>(buf) | reinterpret_cast<uintptr_t>(sink)) % 16 != 0)
+    return fail(SPMM_ERR_INVALID_ARG, "buf and sink must be 16-byte aligned");
+  int dev = 0, sms = 0;
+  CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+  CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "SM count");
+  spmm::l2_read_kernel<<<4 * sms, 512, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4 *>(buf), bytes / 16, passes, static_cast<uint4 *>(sink));
+  CUDA_TRY(cudaGetLastError(), "L2 read probe launch");
+  return SPMM_OK;
+}

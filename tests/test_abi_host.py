@@ -114,3 +114,12 @@ def test_bad_parameters_rejected(lib):
     with pytest.raises(lib.SpmmError) as e:
         lib.spmm_run(0, 16, 16, 8, 0)
     assert e.value.status == lib.SPMM_ERR_INVALID_ARG
+
+
+def test_l2_probe_rejects_bad_arguments_before_any_device_call(lib):
+    L = lib.load_library()
+    sink = ctypes.c_void_p(16)
+    assert L.spmm_probe_l2_read(None, 1024, 1, sink, None) == lib.SPMM_ERR_INVALID_ARG
+    assert L.spmm_probe_l2_read(ctypes.c_void_p(16), 1000, 1, sink, None) == lib.SPMM_ERR_INVALID_ARG
+    assert L.spmm_probe_l2_read(ctypes.c_void_p(16), 1024, 0, sink, None) == lib.SPMM_ERR_INVALID_ARG
+    assert L.spmm_probe_l2_read(ctypes.c_void_p(8), 1024, 1, sink, None) == lib.SPMM_ERR_INVALID_ARG

@@ -118,3 +118,20 @@ def test_bounded_wait_reports_timeout(S):
     assert S.spmm_selftest_wait_timeout(2_000_000) == S.SPMM_ERR_TIMEOUT
     x = torch.ones(4, device="cuda")
     assert float(x.sum().item()) == 4.0
+
+
+def test_l2_read_probe_runs_and_leaves_sink(S):
+    """The L2 read probe (the measured ceiling of the WCSR gather) reads its
+    buffer without writing the sink and reports a plausible positive rate."""
+    import torch
+    buf = torch.ones(1 << 20, dtype=torch.int32, device="cuda")
+    sink = torch.zeros(4, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream()
+    S.spmm_probe_l2_read(buf.data_ptr(), buf.numel() * 4, 3, sink.data_ptr(), s.cuda_stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    S.spmm_probe_l2_read(buf.data_ptr(), buf.numel() * 4, 10, sink.data_ptr(), s.cuda_stream)
+    e1.record(s)
+    torch.cuda.synchronize()
+    assert sink.abs().sum().item() == 0
+    assert e0.elapsed_time(e1) > 0
