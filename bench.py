@@ -96,31 +96,39 @@ def gather_model(w, info):
     return 2.0 * info["n_units"] * w.n if w.fmt == "wcsr" else 0.0
 
 
-L2_PROBE_BYTES = 32 << 20
+_L2_RATES = {}
 
 
-def measure_l2_read_gbs(S, stream, dev):
-    """L2-to-SM read rate of this GPU: spmm_probe_l2_read streams a 32 MiB
-    buffer (resident in L2 after one untimed pass) 20 times with 16-byte loads
-    that bypass L1 from every SM; best of three, CUDA events on the stream."""
+def measure_l2_read_gbs(S, stream, dev, nbytes):
+    """L2-to-SM read rate of this GPU for a footprint of nbytes (the size of
+    the B that a WCSR launch gathers from): spmm_probe_l2_read streams a buffer
+    of that size (resident in L2 after two untimed passes) 20 times with
+    16-byte loads that bypass L1 from every SM; best of three, CUDA events on
+    the stream (at least 4 GiB read per timed launch).  Each footprint gets
+    its own figure, since the rate depends on it."""
     import torch
-    buf = torch.ones(L2_PROBE_BYTES // 4, dtype=torch.int32, device=f"cuda:{dev}")
+    nbytes = max(1 << 20, (int(nbytes) + 15) // 16 * 16)
+    if nbytes in _L2_RATES:
+        return _L2_RATES[nbytes]
+    buf = torch.ones(nbytes // 4, dtype=torch.int32, device=f"cuda:{dev}")
     sink = torch.zeros(4, dtype=torch.int32, device=f"cuda:{dev}")
     sptr = stream.cuda_stream
+    passes = max(20, (4 << 30) // nbytes)  # at least 4 GiB per timed launch: launch cost negligible
     best = 0.0
     for _ in range(3):
-        S.spmm_probe_l2_read(buf.data_ptr(), L2_PROBE_BYTES, 2, sink.data_ptr(), sptr)
+        S.spmm_probe_l2_read(buf.data_ptr(), nbytes, 2, sink.data_ptr(), sptr)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        S.spmm_probe_l2_read(buf.data_ptr(), L2_PROBE_BYTES, 20, sink.data_ptr(), sptr)
+        S.spmm_probe_l2_read(buf.data_ptr(), nbytes, passes, sink.data_ptr(), sptr)
         e1.record(stream)
         stream.synchronize()
-        best = max(best, L2_PROBE_BYTES * 20 / (e0.elapsed_time(e1) * 1e-3) / 1e9)
-    return round(best, 1)
+        best = max(best, nbytes * passes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    _L2_RATES[nbytes] = round(best, 1)
+    return _L2_RATES[nbytes]
 
 
-L2_PEAK_SOURCE = ("measured here: spmm_probe_l2_read, 16-byte L1-bypassing loads of a 32 MiB "
-                  "L2-resident buffer from every SM, best of 3 x 20 passes")
+L2_PEAK_SOURCE = ("measured here: spmm_probe_l2_read, 16-byte L1-bypassing loads of an L2-resident "
+                  "buffer the size of B from every SM, >= 4 GiB per timed launch, best of 3")
 
 
 class ClockSampler:
@@ -229,7 +237,8 @@ def run_ours(args, rank, world):
                           bytes_min=bytes_min, launches=2 if w.fmt == "wcsr" else 1,
                           kernel="bcsr_kernel.cu" if w.fmt == "bcsr" else "wcsr_kernel.cu"))
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=f"cuda:{dev}")
-    l2_gbs = measure_l2_read_gbs(S, stream, dev)
+    for p in parts:
+        p["l2_gbs"] = measure_l2_read_gbs(S, stream, dev, p["B"].nbytes) if p["w"].fmt == "wcsr" else None
 
     def one_step(times):
         for p in parts:
@@ -312,7 +321,7 @@ def run_ours(args, rank, world):
         gb = gather_model(p["w"], p["info"])
         if gb:
             breakdown[-1]["gather"] = {"bytes": int(gb), "achieved": round(gb / t / 1e9, 1), "unit": "GB/s",
-                                       "peak": l2_gbs, "frac": round(gb / t / 1e9 / l2_gbs, 4),
+                                       "peak": p["l2_gbs"], "frac": round(gb / t / 1e9 / p["l2_gbs"], 4),
                                        "peak_source": L2_PEAK_SOURCE,
                                        "note": "B rows gathered from L2 (one row of N values per packed column)"}
     dom = max(breakdown, key=lambda b: b["ms_mean"])
@@ -461,7 +470,6 @@ def run_sweep(args):
     stream = torch.cuda.Stream()
     sptr = stream.cuda_stream
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
-    l2_gbs = measure_l2_read_gbs(S, stream, torch.cuda.current_device())
     cfgs = []
     # entries: a configuration name, optionally ":N" to change the dense width
     # of a single-workload configuration (e.g. a smaller case for a profiler)
@@ -475,45 +483,55 @@ def run_sweep(args):
                 ("bcsr_weight", lambda n: [W.bcsr_weight(n=n) if n else W.bcsr_weight()]),
                 ("bcsr_sweep", lambda n: [W.bcsr_sweep(s, k) for s in W.BCSR_SWEEP_SPARSITY for k in W.SWEEP_N]),
                 ("wcsr_sweep", lambda n: [W.wcsr_sweep(d, k) for d in W.WCSR_SWEEP_DENSITY for k in W.SWEEP_N])]
-    for name, b in builders:
-        if sel and name not in sel:
-            continue
-        cfgs.append((name, lambda b=b, n=sel.get(name): b(n)))
-    # a WCSR configuration in 64-row windows with column padding 8 (the
-    # paper's WCSR geometry): its name with the suffix _h64
-    def h64(ws):
+    # an entry may end in _h64 (the WCSR matrix in 64-row windows with column
+    # padding 8, the paper's WCSR geometry) and/or _dyn (the WCSR dynamic
+    # schedule); bcsr_sweep_95_N256 or wcsr_sweep_0.1_N8 name one sweep point
+    def variant(ws, h64, dyn):
         for w in ws:
-            w.b_row, w.b_col = 64, 8
-            w.name += "_h64"
-            w.meta["desc"] = w.describe().replace(" h16 ", " h64 pad8 ")
+            if h64:
+                w.b_row, w.b_col = 64, 8
+                w.name += "_h64"
+                w.meta["desc"] = w.describe().replace(" h16 ", " h64 pad8 ")
+            if dyn:
+                w.name += "_dyn"
+                w.meta["schedule"] = S.SPMM_SCHEDULE_DYNAMIC
+                w.meta["desc"] = w.describe() + " (dynamic schedule)"
         return ws
-    for name, b in builders:
-        if name.startswith("wcsr") and name + "_h64" in sel:
-            cfgs.append((name + "_h64", lambda b=b, n=sel.get(name + "_h64"): h64(b(n))))
-    # single sweep points, e.g. bcsr_sweep_95_N256 or wcsr_sweep_0.1_N8 (or with _h64)
-    for e in sel:
-        if e.startswith("wcsr_sweep_") and e.endswith("_h64"):
-            _, _, lvl, n = e[:-4].split("_")
-            cfgs.append((e, lambda lvl=float(lvl), n=int(n[1:]): h64([W.wcsr_sweep(lvl, n)])))
+    named = dict(builders)
+    if not sel:
+        cfgs = [(name, lambda b=b: b(None)) for name, b in builders]
+    for e, n in sel.items():
+        if e == "linear_weight":
             continue
-        parts = e.split("_")
-        if len(parts) == 4 and parts[0] in ("bcsr", "wcsr") and parts[1] == "sweep" and parts[3].startswith("N"):
-            lvl, n = float(parts[2]), int(parts[3][1:])
-            fn = (lambda lvl=lvl, n=n: [W.bcsr_sweep(int(lvl), n)]) if parts[0] == "bcsr" else \
-                (lambda lvl=lvl, n=n: [W.wcsr_sweep(lvl, n)])
-            cfgs.append((e, fn))
+        base, h64, dyn = e, False, False
+        if base.endswith("_dyn"):
+            base, dyn = base[:-4], True
+        if base.endswith("_h64"):
+            base, h64 = base[:-4], True
+        parts = base.split("_")
+        if base in named:
+            fn = (lambda b=named[base], n=n: b(n))
+        elif len(parts) == 4 and parts[0] in ("bcsr", "wcsr") and parts[1] == "sweep" and parts[3].startswith("N"):
+            lvl, nn = float(parts[2]), int(parts[3][1:])
+            fn = (lambda lvl=lvl, nn=nn: [W.bcsr_sweep(int(lvl), nn)]) if parts[0] == "bcsr" else \
+                (lambda lvl=lvl, nn=nn: [W.wcsr_sweep(lvl, nn)])
+        else:
+            raise SystemExit(f"unknown configuration {e!r}")
+        cfgs.append((e, lambda fn=fn, h64=h64, dyn=dyn: variant(fn(), h64, dyn)))
     if "linear_weight" in sel:
         run_linear_sweep(args, peaks, stream, flush)
     for name, b in cfgs:
         cache = {}
         for w in b():
-            key = (w.fmt, w.m, w.k, w.nnz, int(w.row_ptr[w.m // 2]))
+            key = (w.fmt, w.m, w.k, w.nnz, int(w.row_ptr[w.m // 2]), w.b_row, w.meta.get("schedule"))
             if key not in cache:
                 for hh in cache.values():
                     S.spmm_destroy(hh)
                 cache.clear()
                 create = S.spmm_bcsr_create if w.fmt == "bcsr" else S.spmm_wcsr_create
                 cache[key] = create(w.m, w.k, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.b_row, w.b_col)
+                if w.meta.get("schedule") is not None:
+                    S.spmm_set_schedule(cache[key], w.meta["schedule"])
             h = cache[key]
             info = S.spmm_format_info(h)
             dB = torch.from_numpy(w.B().view(np.int16)).cuda().view(torch.bfloat16 if w.dtype == "bf16" else torch.float16)
@@ -538,6 +556,8 @@ def run_sweep(args):
             cold = statistics.median(a.elapsed_time(b) for a, b in ms_cold)
             warm = statistics.median(a.elapsed_time(b) for a, b in ms_warm)
             eff, stored_fl, bytes_min = part_model(w, info)
+            l2_gbs = measure_l2_read_gbs(S, stream, torch.cuda.current_device(), 2 * w.k * w.n) \
+                if w.fmt == "wcsr" else None
             t = cold * 1e-3
             t_tc = stored_fl / (peaks["bf16_tflops"] * 1e12)
             t_hbm = bytes_min / (peaks["hbm_gbs"] * 1e9)

@@ -58,7 +58,8 @@ typedef enum { SPMM_FORMAT_BCSR = 0, SPMM_FORMAT_WCSR = 1 } spmm_format;
 typedef enum {
     SPMM_SCHEDULE_AUTO = 0,   /* the library's choice (the default) */
     SPMM_SCHEDULE_TILES = 1,  /* whole tiles (block row x column tile) per CTA, round-robin */
-    SPMM_SCHEDULE_SPLIT = 2   /* equal shares of the tiles' stages per CTA; cut tiles summed by a second pass */
+    SPMM_SCHEDULE_SPLIT = 2,  /* equal shares of the tiles' stages per CTA; cut tiles summed by a second pass */
+    SPMM_SCHEDULE_DYNAMIC = 3 /* WCSR: chunks of the work list taken over at run time (cluster launch control) */
 } spmm_schedule;
 
 /* Statistics of a handle's format (spmm_format_info). */
@@ -224,8 +225,8 @@ spmm_status spmm_check(spmm_handle h, void *stream);
 spmm_status spmm_set_max_ctas(spmm_handle h, int32_t ctas);
 
 /*
- * spmm_set_schedule -- choose how a BCSR handle's spmm_run spreads work over
- * the persistent CTAs.  SPMM_SCHEDULE_TILES gives each CTA whole tiles (one
+ * spmm_set_schedule -- choose how a handle's spmm_run spreads work over CTAs.
+ * BCSR handles: SPMM_SCHEDULE_TILES gives each persistent CTA whole tiles (one
  * block row x one tile of 128 or 256 columns), as the paper's static grid
  * does (Section III-F).  SPMM_SCHEDULE_SPLIT lists the stages of all tiles
  * (one per stored block; one for a block row without blocks) and gives each
@@ -237,8 +238,20 @@ spmm_status spmm_set_max_ctas(spmm_handle h, int32_t ctas);
  * only when fewer than half the SMs would get a tile and the tiles average at
  * least 8 stages.  The split schedule needs a handle with fewer than two block
  * rows per SM (its workspace is allocated at create only then); otherwise
- * SPLIT runs as TILES.  WCSR handles always use their equal-share schedule.
- * Errors: INVALID_ARG (null handle, unknown schedule).
+ * SPLIT runs as TILES.
+ * WCSR handles with window height 16: AUTO, TILES and SPLIT all give each
+ * persistent CTA an equal contiguous share of the work items (stages x column
+ * tiles).  SPMM_SCHEDULE_DYNAMIC cuts the work list into about four times as
+ * many chunks as CTAs fit on the GPU (each of at least 32 items) and launches
+ * one CTA per chunk; a running CTA that finishes a chunk cancels the launch of
+ * a CTA that has not started and takes over its chunk (cluster launch
+ * control, the dynamic scheduling the paper names as future work for
+ * Blackwell, Section V), so faster CTAs take more chunks.  Windows cut
+ * between chunks are summed in chunk order by the second kernel, so results
+ * do not depend on which CTA ran which chunk.  Setting DYNAMIC allocates the
+ * larger partial-sum workspace it needs (about 40 MB at 152 SMs).
+ * Errors: INVALID_ARG (null handle, unknown schedule); UNSUPPORTED (DYNAMIC on
+ * a BCSR handle or a WCSR handle whose windows are not 16 rows high); OOM.
  */
 spmm_status spmm_set_schedule(spmm_handle h, int32_t schedule);
 

@@ -224,10 +224,11 @@ def spmm_set_max_ctas(h: int, ctas: int) -> None:
 SPMM_SCHEDULE_AUTO = 0
 SPMM_SCHEDULE_TILES = 1
 SPMM_SCHEDULE_SPLIT = 2
+SPMM_SCHEDULE_DYNAMIC = 3
 
 
 def spmm_set_schedule(h: int, schedule: int) -> None:
-    """BCSR work schedule: SPMM_SCHEDULE_AUTO, _TILES or _SPLIT."""
+    """Work schedule: SPMM_SCHEDULE_AUTO, _TILES, _SPLIT (BCSR) or _DYNAMIC (WCSR, window height 16)."""
     _check(load_library().spmm_set_schedule(h, schedule), "spmm_set_schedule")
 
 

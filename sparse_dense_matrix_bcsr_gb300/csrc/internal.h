@@ -137,7 +137,8 @@ struct WcsrParams {
   int64_t n_stages;
   int64_t P_total;
   int32_t M, N, K;
-  int32_t grid;                  // persistent CTAs; CTA c owns a contiguous range of (column tile, stage)
+  int32_t grid;                  // CTAs launched = chunks: chunk c is a contiguous range of (column tile, stage)
+  int32_t dynamic;               // window height 16: running CTAs take over chunks of CTAs not yet started
   uint32_t *status;
   uint64_t wait_limit_ns;
 };
@@ -149,6 +150,10 @@ int wcsr_ctas_per_sm(int64_t N);
 // Columns of C per WCSR work item (window height 16) at dense width N.
 int wcsr_tile_cols(int64_t N);
 constexpr int kWcsrMaxCtasPerSm = 2;
+// Dynamic WCSR schedule: chunks per CTA that fits on the GPU, and the fewest
+// work items a chunk may hold.
+constexpr int kWcsrDynChunksPerCta = 4;
+constexpr int64_t kWcsrDynMinChunkItems = 32;
 
 // Workspace floats per partial slot (16 rows x 256 columns).
 constexpr int64_t kWcsrSlotFloats = 16 * 256;

@@ -94,21 +94,6 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, ui
   }
 }
 
-// The same whole-warp wait without sleeping between probes: try_wait itself
-// suspends the warp until the phase completes or a hardware time slice ends,
-// so the waiter resumes as soon as the phase flips instead of up to twice the
-// sleep interval later.  For roles on the critical path of a pipeline whose
-// loads are TMA copies (nothing else in the CTA issues cp.async).
-__device__ __forceinline__ bool mbar_wait_warp_spin(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  const long long limit_cycles = static_cast<long long>(limit_ns) * 21 / 10;
-  const long long t0 = clock64();
-  while (true) {
-    int state = mbar_try_wait(bar, parity) ? 1 : (clock64() - t0 > limit_cycles ? 2 : 0);
-    state = __shfl_sync(0xffffffffu, state, 0);
-    if (state != 0) return state == 1;
-  }
-}
-
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -184,6 +169,34 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // the async proxy (tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- cluster launch control
+// Asks the hardware to cancel the launch of one CTA of this grid that has not
+// started yet; the 16-byte answer is written to `resp` (16-byte aligned
+// shared memory) and completes 16 transaction bytes on `bar`, whose phase the
+// caller has armed with mbar_arrive_expect_tx(bar, 16).
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+               ::"r"(resp), "r"(bar)
+               : "memory");
+}
+
+// Reads an answer of clc_try_cancel once its barrier phase has completed:
+// true and the cancelled CTA's blockIdx.x, or false when no CTA was left.
+__device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t &cta_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 h, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, h;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "r"(resp)
+      : "memory");
+  cta_x = x;
+  return ok != 0;
 }
 
 // ---------------------------------------------------------------- tcgen05

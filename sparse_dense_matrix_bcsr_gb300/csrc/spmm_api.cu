@@ -444,6 +444,18 @@ spmm_status run_device(spmm_handle h, const void *B, void *C, int64_t N, cudaStr
   p.N = static_cast<int32_t>(N);
   p.K = static_cast<int32_t>(h->k);
   p.grid = wcsr_grid(h, N);
+  p.dynamic = 0;
+  if (!w64 && h->schedule == SPMM_SCHEDULE_DYNAMIC && p.grid > 0) {
+    // one CTA per chunk, about kWcsrDynChunksPerCta chunks per CTA that fits,
+    // each of at least kWcsrDynMinChunkItems work items
+    const int64_t items = h->n_stages * ((N + spmm::wcsr_tile_cols(N) - 1) / spmm::wcsr_tile_cols(N));
+    const int64_t chunks = std::min<int64_t>({static_cast<int64_t>(spmm::kWcsrDynChunksPerCta) * p.grid,
+                                              items / spmm::kWcsrDynMinChunkItems, h->ws_slots / 2});
+    if (chunks > p.grid) {
+      p.grid = static_cast<int32_t>(chunks);
+      p.dynamic = 1;
+    }
+  }
   p.status = h->d_status;
   p.wait_limit_ns = h->wait_limit_ns;
   cudaError_t e = w64 ? spmm::launch_wcsr64(h->tm_C, p, in_bf16, out_bf16, s) : spmm::launch_wcsr(p, in_bf16, out_bf16, s);
@@ -576,8 +588,30 @@ spmm_status spmm_set_max_ctas(spmm_handle h, int32_t ctas) {
 
 spmm_status spmm_set_schedule(spmm_handle h, int32_t schedule) {
   if (!h) return fail(SPMM_ERR_INVALID_ARG, "handle is NULL");
-  if (schedule != SPMM_SCHEDULE_AUTO && schedule != SPMM_SCHEDULE_TILES && schedule != SPMM_SCHEDULE_SPLIT)
+  if (schedule != SPMM_SCHEDULE_AUTO && schedule != SPMM_SCHEDULE_TILES && schedule != SPMM_SCHEDULE_SPLIT &&
+      schedule != SPMM_SCHEDULE_DYNAMIC)
     return fail(SPMM_ERR_INVALID_ARG, "unknown schedule %d", schedule);
+  if (schedule == SPMM_SCHEDULE_DYNAMIC) {
+    if (h->format != SPMM_FORMAT_WCSR || h->b_row != 16)
+      return fail(SPMM_ERR_UNSUPPORTED, "the dynamic schedule takes WCSR handles with window height 16");
+    // two partial slots per chunk, for the most chunks any N can give
+    const int64_t slots = 2ll * spmm::kWcsrDynChunksPerCta * spmm::kWcsrMaxCtasPerSm * std::max(h->num_sms, 1);
+    if (slots > h->ws_slots) {
+      float *ws = nullptr;
+      spmm::PartialRec *rec = nullptr;
+      if (cudaMalloc(&ws, slots * spmm::kWcsrSlotFloats * sizeof(float)) != cudaSuccess ||
+          cudaMalloc(&rec, slots * sizeof(spmm::PartialRec)) != cudaSuccess) {
+        cudaFree(ws);
+        cudaGetLastError();
+        return fail(SPMM_ERR_OOM, "cudaMalloc(dynamic-schedule workspace) failed");
+      }
+      cudaFree(h->d_ws);
+      cudaFree(h->d_partials);
+      h->d_ws = ws;
+      h->d_partials = rec;
+      h->ws_slots = slots;
+    }
+  }
   h->schedule = schedule;
   return SPMM_OK;
 }
@@ -825,23 +859,32 @@ extern "C" spmm_status spmm_selftest_wait_timeout(int64_t timeout_ns, void *stre
 namespace spmm {
 namespace {
 // Every thread streams 16-byte loads that bypass L1 (ld.global.cg) with four
-// in flight; the XOR of the data decides a store nobody expects, so the loads
-// cannot be dropped.
+// in flight, over `passes` back-to-back sweeps of the buffer taken as one
+// sequence (so a small buffer still gives every thread a long stream); the
+// XOR of the data decides a store nobody expects, so the loads cannot be
+// dropped.
 __global__ void __launch_bounds__(512) l2_read_kernel(const uint4 *__restrict__ buf, int64_t n16, int32_t passes,
                                                       uint4 *sink) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t total = n16 * passes;
+  const int64_t step = stride % n16;  // index advance per stride, wrapped
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  int64_t j = i % n16;
+  auto next = [&](int64_t x) {
+    x += step;
+    return x >= n16 ? x - n16 : x;
+  };
   uint32_t acc = 0;
-  for (int32_t pass = 0; pass < passes; ++pass) {
-    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (; i + 3 * stride < n16; i += 4 * stride) {
-      const uint4 a = __ldcg(buf + i), b = __ldcg(buf + i + stride);
-      const uint4 c = __ldcg(buf + i + 2 * stride), d = __ldcg(buf + i + 3 * stride);
-      acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^ d.z ^ d.w;
-    }
-    for (; i < n16; i += stride) {
-      const uint4 a = __ldcg(buf + i);
-      acc ^= a.x ^ a.y ^ a.z ^ a.w;
-    }
+  for (; i + 3 * stride < total; i += 4 * stride) {
+    const int64_t j1 = next(j), j2 = next(j1), j3 = next(j2);
+    const uint4 a = __ldcg(buf + j), b = __ldcg(buf + j1), c = __ldcg(buf + j2), d = __ldcg(buf + j3);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^ d.z ^ d.w;
+    j = next(j3);
+  }
+  for (; i < total; i += stride) {
+    const uint4 a = __ldcg(buf + j);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w;
+    j = next(j);
   }
   if (acc == 0x9E3779B9u && threadIdx.x == blockDim.x - 1) sink[0] = make_uint4(acc, blockIdx.x, 0, 0);
 }

@@ -65,6 +65,14 @@ constexpr int kMetaBytes = kWcsrPackBytes - kWcsrPackIdxOff;  // a stage record'
 constexpr int kChunkBytes = kKC * 64 * 2;    // 64 gathered rows x 64 columns
 constexpr int kEpiWarps = 4;
 constexpr int kAccBufs = 4;
+constexpr int kRespSlots = 4;  // cluster-launch-control answers in flight (dynamic schedule)
+
+// Stage record flags besides kStageFirst / kStageLast (the window's first and
+// last stage): the first and last work item of a chunk, and the end of the
+// CTA's work.
+constexpr int32_t kRecChunkFirst = 4;
+constexpr int32_t kRecChunkLast = 8;
+constexpr int32_t kRecEnd = 16;
 
 // A producer fetches the column-index record of its items this many of its
 // own items ahead (a small TMA bulk copy into a per-warp ring), so reading an
@@ -88,8 +96,8 @@ struct Cfg {
   static constexpr int kAccCols = kH * NACC;                     // TMEM columns per accumulator buffer
   static constexpr int kTmemCols = kAccBufs * kAccCols <= 32 ? 32 : (kAccBufs * kAccCols <= 64 ? 64 : 128);
   static constexpr int kIdxRing = (PW * ILEAD * kMetaBytes + 1023) / 1024 * 1024;
-  static constexpr int kBars = 2 * Q + 2 * kAccBufs + 1 + PW * ILEAD;
-  static constexpr int kMiscBytes = 2048;                    // barriers, TMEM address, records between roles
+  static constexpr int kBars = 2 * Q + 2 * kAccBufs + 1 + PW * ILEAD + kRespSlots;
+  static constexpr int kMiscBytes = 2048;  // launch-control answers, barriers, TMEM address, records between roles
   static constexpr int kSmemBytes = Q * kStageBytes + kIdxRing + kMiscBytes + 1024;
   static_assert(kStageBytes % 1024 == 0 && kGatherBytes % 1024 == 0, "MMA operands need 1024-byte alignment");
   // A producer's wait for stage (it % Q) to be free is a parity wait on the
@@ -99,23 +107,20 @@ struct Cfg {
   // warp could run two phases ahead, pass the wait early and overwrite a stage
   // still in use.
   static_assert(PW <= Q, "more producer warps than stages");
-  static_assert(kBars * 8 + 16 + Q * 16 + kAccBufs * 32 <= kMiscBytes, "barrier area");
+  static_assert(kRespSlots * 16 + kBars * 8 + 16 + Q * 32 + kAccBufs * 32 <= kMiscBytes, "barrier area");
   static_assert(kSmemBytes <= 227 * 1024 && MINB * (kSmemBytes + 1024) <= 228 * 1024, "shared memory");
   static_assert(MINB * kTmemCols <= 512, "TMEM");
   static_assert(kAccBufs * kAccCols <= kTmemCols, "accumulator buffers exceed the TMEM allocation");
 };
 
-__device__ __forceinline__ int4 shfl_int4(const int4 &v, int src) {
-  return make_int4(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src),
-                   __shfl_sync(0xffffffffu, v.z, src), __shfl_sync(0xffffffffu, v.w, src));
-}
-
 // Shared-memory records passed between roles.
 struct StageRec {   // producer -> MMA, one per ring stage
   int32_t ncols;
-  int32_t flags;
+  int32_t flags;    // kStageFirst | kStageLast | kRecChunkFirst | kRecChunkLast | kRecEnd
   int32_t window;
   int32_t tile;
+  int32_t chunk;    // the chunk the item belongs to (its partial-sum slots are 2 chunk, 2 chunk + 1)
+  int32_t pad_[3];
 };
 struct SegRec {     // MMA -> epilogue, one per accumulator buffer
   int32_t window;   // -1: no more segments
@@ -139,8 +144,10 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *iring = smem + Q * C_::kStageBytes;  // per producer warp: kILead index records of kMetaBytes
-  uint64_t *bars = reinterpret_cast<uint64_t *>(iring + C_::kIdxRing);
-  // bars: full[Q], empty[Q], acc_full[kAccBufs], acc_empty[kAccBufs], drain, ifull[PW][kILead]
+  uint8_t *resp = iring + C_::kIdxRing;         // kRespSlots x 16-byte launch-control answers
+  uint64_t *bars = reinterpret_cast<uint64_t *>(resp + 16 * kRespSlots);
+  // bars: full[Q], empty[Q], acc_full[kAccBufs], acc_empty[kAccBufs], drain, ifull[PW][kILead],
+  // resp[kRespSlots]
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C_::kBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   StageRec *stage_rec = reinterpret_cast<StageRec *>(tmem_slot + 4);        // [Q]
@@ -168,6 +175,8 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
   const uint32_t acce0 = smem_addr(&bars[2 * Q + kAccBufs]);
   const uint32_t drain_bar = smem_addr(&bars[2 * Q + 2 * kAccBufs]);
   const uint32_t ifull0 = smem_addr(&bars[2 * Q + 2 * kAccBufs + 1]);
+  const uint32_t respb0 = smem_addr(&bars[2 * Q + 2 * kAccBufs + 1 + PW * kILead]);
+  const uint32_t resp0 = smem_addr(resp);
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < Q; ++q) {
@@ -183,11 +192,13 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
     }
     mbar_init(drain_bar, 1);
     for (int v = 0; v < PW * kILead; ++v) mbar_init(ifull0 + 8 * v, 1);  // lane 0's expect_tx arrive
+    for (int v = 0; v < kRespSlots; ++v) mbar_init(respb0 + 8 * v, 1);   // expect_tx arrive + 16-byte answer
     *abort_flag = 0;
     fence_barrier_init();
-    // partial-sum records of this CTA (overwritten below when used)
-    p.partials[2 * blockIdx.x] = PartialRec{-1, 0, 0, 0};
-    p.partials[2 * blockIdx.x + 1] = PartialRec{-1, 0, 0, 0};
+    if (NOALLOC) {  // partial-sum records of this CTA (overwritten below when used)
+      p.partials[2 * blockIdx.x] = PartialRec{-1, 0, 0, 0};
+      p.partials[2 * blockIdx.x + 1] = PartialRec{-1, 0, 0, 0};
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), C_::kTmemCols);
@@ -273,6 +284,22 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         }
       }
     };
+    // The end of the CTA's work: the owner of CTA-local item it_end (the one
+    // after the last, warp it_end % PW) passes an end record to the MMA warp
+    // through stage it_end % Q.
+    auto send_end = [&](int64_t it_end) -> bool {
+      const uint32_t stage = static_cast<uint32_t>(it_end % Q);
+      const uint32_t phase = static_cast<uint32_t>((it_end / Q) & 1);
+      bool r = mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns);
+      r = __shfl_sync(0xffffffffu, r && !*abort_flag, 0);
+      if (!r) return false;
+      if (lane == 0) {
+        stage_rec[stage] = StageRec{0, kRecEnd, -1, 0, 0, {0, 0, 0}};
+        mbar_arrive(full0 + 8 * stage);
+      }
+      cp_async_arrive_noinc(full0 + 8 * stage);
+      return true;
+    };
     if constexpr (NOALLOC) {
       // Caller-owned arrays: the stage list built on the device, the column
       // indices read at each stage's first packed column, and the values
@@ -331,8 +358,9 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
           const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
           const uint32_t fb = full0 + 8 * stage;
           const int tile = static_cast<int>(fi / n_stages);
-          if (lane == 0) {
-            stage_rec[stage] = StageRec{d.z, d.w, d.y, tile};  // released by this arrive
+          if (lane == 0) {  // released by this arrive
+            const int32_t fl = d.w | (fi == f0 ? kRecChunkFirst : 0) | (fi == f1 - 1 ? kRecChunkLast : 0);
+            stage_rec[stage] = StageRec{d.z, fl, d.y, tile, static_cast<int32_t>(blockIdx.x), {0, 0, 0}};
             mbar_arrive(fb);
           }
           copy_vals(st + C_::kGatherBytes, d);
@@ -340,6 +368,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
           cp_async_arrive_noinc(fb);
         }
       }
+      if (ok && (f1 - f0) % PW == warp) ok = send_end(f1 - f0);
       cp_async_wait_all();
       if (!ok && lane == 0) {
         atomicOr(p.status, kDevTimeout);
@@ -347,33 +376,119 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
       }
     } else {
       // Every stage is one record in global memory (its value tile, its 64
-      // column indices and its descriptor).  Warp w owns the work items
-      // f0 + w + PW*j (j = 0, 1, ...).  It fetches the index part of its
-      // item j's record (272 bytes) kILead of its items ahead into slot
-      // j % kILead of its ring, and when it starts item j it reads the indices
-      // from there (the slot is then refilled), waits for the item's stage to
-      // be free, has the value tile copied into the stage by TMA and copies
-      // the item's rows of B with cp.async.
+      // column indices and its descriptor).
+      //
+      // Chunks: the CTA's work is a sequence of chunks, chunk id being the
+      // work items [T*id/G, T*(id+1)/G) (G = gridDim.x).  The first is chunk
+      // blockIdx.x; with p.dynamic every further one is a CTA of this grid
+      // that had not started yet, cancelled through cluster launch control
+      // and taken over here (the paper's future-work dynamic scheduling,
+      // Section V); without it the CTA has just its own chunk.  Warp 0
+      // requests the next chunk when it learns of one, into answer slot
+      // (ordinal % kRespSlots); every producer warp reads the same answers,
+      // so all of them see the same sequence.  CTA-local item it (0, 1, ...
+      // across the chunks) belongs to warp it % PW and stage it % Q.
+      //
+      // Warp w fetches the index part of its own item j's record (272 bytes)
+      // kILead of its items ahead into slot j % kILead of its ring, and when
+      // it starts item j it reads the indices from there (the slot is then
+      // refilled), waits for the item's stage to be free, has the value tile
+      // copied into the stage by TMA and copies the item's rows of B with
+      // cp.async.  Chunks hold at least 32 items (at most 16 of a warp's items
+      // apart are live at once), so the answer slots and the four remembered
+      // chunks are never overwritten while a warp still needs them.
       const uint8_t *pack = reinterpret_cast<const uint8_t *>(p.stage_pack);
       uint8_t *ring = iring + warp * kILead * kMetaBytes;
       const uint32_t ifull_w = ifull0 + 8 * (warp * kILead);
-      auto fetch_idx = [&](int64_t j) {
-        const int64_t fj = f0 + warp + j * kStep;
-        if (fj < f1 && lane == 0) {
-          const uint32_t slot = static_cast<uint32_t>(j % kILead);
-          const uint8_t *src = pack + (fj % n_stages) * kWcsrPackBytes;
-          mbar_arrive_expect_tx(ifull_w + 8 * slot, kMetaBytes);
-          tma_bulk_load(smem_addr(ring + slot * kMetaBytes), src + kWcsrPackIdxOff, kMetaBytes, ifull_w + 8 * slot);
-          prefetch_l2_bulk(src + kWcsrPackValOff, kValBytes);
+      const int64_t n_chunks = gridDim.x;
+      struct Chunk {
+        int64_t lbase, len, g0;  // first CTA-local item, items, first work item
+        int32_t id;
+      };
+      Chunk kn[4] = {};
+      int nk = 0;               // chunks learned
+      bool no_more = false;     // the chunk after the last learned one does not exist
+      int64_t l_end = 0;        // CTA-local items in all (once no_more)
+      int64_t n_req = 0, n_read = 0;  // warp 0: answers requested / read
+      bool ok = true;
+      // Learns chunk nk (false: a wait ran out).
+      auto learn_next = [&]() -> bool {
+        int32_t id = -1;
+        if (nk == 0) {
+          id = static_cast<int32_t>(blockIdx.x);
+        } else if (p.dynamic) {
+          const uint32_t sl = static_cast<uint32_t>((nk - 1) % kRespSlots);
+          bool r = mbar_wait_warp(respb0 + 8 * sl, static_cast<uint32_t>(((nk - 1) / kRespSlots) & 1),
+                                  p.wait_limit_ns);
+          r = __shfl_sync(0xffffffffu, r && !*abort_flag, 0);
+          if (!r) return false;
+          uint32_t x = 0;
+          const bool got = clc_query(resp0 + 16 * sl, x);
+          ++n_read;
+          id = got ? static_cast<int32_t>(x) : -1;
+        }
+        const int64_t lb = nk ? kn[(nk - 1) & 3].lbase + kn[(nk - 1) & 3].len : 0;
+        if (id < 0) {
+          no_more = true;
+          l_end = lb;
+          return true;
+        }
+        Chunk c;
+        c.id = id;
+        c.g0 = total * id / n_chunks;
+        c.len = total * (id + 1) / n_chunks - c.g0;
+        c.lbase = lb;
+        kn[nk & 3] = c;
+        if (p.dynamic && warp == 0) {
+          if (lane == 0) {
+            const uint32_t sl = static_cast<uint32_t>(nk % kRespSlots);
+            mbar_arrive_expect_tx(respb0 + 8 * sl, 16);
+            clc_try_cancel(resp0 + 16 * sl, respb0 + 8 * sl);
+          }
+          ++n_req;
+        }
+        ++nk;
+        return true;
+      };
+      // The remembered chunk holding CTA-local item it (learning chunks as
+      // needed): its ordinal, -1 past the last item, -2 when a wait ran out.
+      auto locate = [&](int64_t it) -> int {
+        while (true) {
+          for (int q = nk > 4 ? nk - 4 : 0; q < nk; ++q)
+            if (it >= kn[q & 3].lbase && it < kn[q & 3].lbase + kn[q & 3].len) return q;
+          if (no_more) return -1;
+          if (!learn_next()) return -2;
         }
       };
+      int64_t n_fetched = 0;  // own items whose index records were requested (a prefix)
+      auto fetch_idx = [&](int64_t j) -> bool {
+        const int q = locate(warp + PW * j);
+        if (q == -2) return false;
+        if (q >= 0) {
+          const Chunk &c = kn[q & 3];
+          const int64_t fj = c.g0 + (warp + PW * j - c.lbase);
+          if (lane == 0) {
+            const uint32_t slot = static_cast<uint32_t>(j % kILead);
+            const uint8_t *src = pack + (fj % n_stages) * kWcsrPackBytes;
+            mbar_arrive_expect_tx(ifull_w + 8 * slot, kMetaBytes);
+            tma_bulk_load(smem_addr(ring + slot * kMetaBytes), src + kWcsrPackIdxOff, kMetaBytes,
+                          ifull_w + 8 * slot);
+            prefetch_l2_bulk(src + kWcsrPackValOff, kValBytes);
+          }
+          n_fetched = j + 1;
+        }
+        return true;
+      };
 #pragma unroll 1
-      for (int j = 0; j < kILead; ++j) fetch_idx(j);
-      bool ok = true;
-      int64_t consumed = 0;  // own items whose indices were read; fetches of the next kILead are in flight
-      for (int64_t j = 0;; ++j) {
-        const int64_t f = f0 + warp + j * kStep;
-        if (f >= f1) break;
+      for (int j = 0; j < kILead && ok; ++j) ok = fetch_idx(j);
+      int64_t consumed = 0;  // own items whose indices were read
+      for (int64_t j = 0; ok; ++j) {
+        const int64_t it = warp + PW * j;
+        const int q = locate(it);
+        if (q == -2) ok = false;
+        if (q < 0) break;
+        const Chunk c = kn[q & 3];
+        const int64_t f = c.g0 + (it - c.lbase);
         const uint32_t islot = static_cast<uint32_t>(j % kILead);
         ok = mbar_wait_warp(ifull_w + 8 * islot, static_cast<uint32_t>((j / kILead) & 1), p.wait_limit_ns);
         ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
@@ -384,9 +499,9 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         const int32_t hi = reinterpret_cast<const int32_t *>(meta)[32 + lane];
         fence_proxy_async_smem();  // these reads before the TMA refill of the slot
         __syncwarp();
-        fetch_idx(j + kILead);
         consumed = j + 1;
-        const int64_t it = f - f0;
+        ok = fetch_idx(j + kILead);
+        if (!ok) break;
         const uint32_t stage = static_cast<uint32_t>(it % Q);
         const uint32_t phase = static_cast<uint32_t>((it / Q) & 1);
         // the stage is free once the MMAs of item it - Q are complete
@@ -397,7 +512,12 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
         const uint32_t fb = full0 + 8 * stage;
         if (lane == 0) {
-          stage_rec[stage] = StageRec{d.x, d.y, d.z, tile};  // released by this arrive
+          if (it == c.lbase) {  // the chunk's partial-sum records (overwritten when used)
+            p.partials[2 * c.id] = PartialRec{-1, 0, 0, 0};
+            p.partials[2 * c.id + 1] = PartialRec{-1, 0, 0, 0};
+          }
+          const int32_t fl = d.y | (it == c.lbase ? kRecChunkFirst : 0) | (it == c.lbase + c.len - 1 ? kRecChunkLast : 0);
+          stage_rec[stage] = StageRec{d.x, fl, d.z, tile, c.id, {0, 0, 0}};  // released by this arrive
           mbar_arrive_expect_tx(fb, kValBytes);
           tma_bulk_load(st + C_::kGatherBytes, pack + (f % n_stages) * kWcsrPackBytes + kWcsrPackValOff, kValBytes,
                         fb);
@@ -405,13 +525,17 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         gather(st, tile * C_::kBN, d.x, lo, hi);
         cp_async_arrive_noinc(fb);
       }
+      if (ok && l_end % PW == warp) ok = send_end(l_end);
       cp_async_wait_all();
       if (!ok && lane == 0) {
         atomicOr(p.status, kDevTimeout);
         *abort_flag = 1;
-        // let the index records in flight land before the CTA exits
-        for (int64_t i = consumed; i < consumed + kILead && f0 + warp + i * kStep < f1; ++i)
+        // let the index records and launch-control answers in flight land
+        // before the CTA exits
+        for (int64_t i = consumed; i < n_fetched; ++i)
           mbar_wait(ifull_w + 8 * (i % kILead), static_cast<uint32_t>((i / kILead) & 1), 1000000ull);
+        for (int64_t r = n_read; r < n_req; ++r)
+          mbar_wait(respb0 + 8 * (r % kRespSlots), static_cast<uint32_t>((r / kRespSlots) & 1), 1000000ull);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -425,20 +549,25 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
       uint32_t buf = 0;
       int ksteps_done = 0;  // MMA k-steps issued into the current segment
       int32_t s_flags = 0;
-      bool s_at_f0 = false;
+      bool s_at_f0 = false;  // the segment starts at its chunk's first item (partial slot 2 chunk)
       bool ok = true;
       auto open_buffer = [&](uint32_t b, uint32_t use) -> bool {
         const bool r = mbar_wait_warp(acce0 + 8 * b, (use & 1u) ^ 1u, p.wait_limit_ns);
         tc_fence_after_sync();
         return __shfl_sync(0xffffffffu, r && !*abort_flag, 0);
       };
-      for (int64_t f = f0; f < f1 && ok; ++f) {
+      // Items arrive in CTA order until the end record; a segment (the run of
+      // one window's stages in this chunk) starts at a window's first stage
+      // or a chunk's first item and ends at a window's last stage or a
+      // chunk's last item.
+      while (ok) {
         ok = mbar_wait_warp(full0 + 8 * stage, phase, p.wait_limit_ns);
         ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
         if (!ok) break;
         const StageRec rec = stage_rec[stage];
-        const bool seg_first = f == f0 || (rec.flags & kStageFirst);
-        const bool seg_last = f == f1 - 1 || (rec.flags & kStageLast);
+        if (rec.flags & kRecEnd) break;
+        const bool seg_first = (rec.flags & (kStageFirst | kRecChunkFirst)) != 0;
+        const bool seg_last = (rec.flags & (kStageLast | kRecChunkLast)) != 0;
         if (seg_first) {
           buf = seg % kAccBufs;
           if (!open_buffer(buf, seg / kAccBufs)) {
@@ -447,7 +576,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
           }
           ksteps_done = 0;
           s_flags = rec.flags & kStageFirst;
-          s_at_f0 = f == f0;
+          s_at_f0 = (rec.flags & kRecChunkFirst) != 0;
         }
         const int ksteps = rec.ncols / 16;
         if (leader) {
@@ -478,7 +607,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
             sr.tile = rec.tile;
             sr.flags = s_flags;
             sr.zero = ksteps_done == 0;
-            sr.slot = 2 * static_cast<int32_t>(blockIdx.x) + (s_at_f0 ? 0 : 1);
+            sr.slot = 2 * rec.chunk + (s_at_f0 ? 0 : 1);
             mbar_arrive(accf0 + 8 * buf);  // releases the record
             umma_commit(accf0 + 8 * buf);  // arrives when the MMAs are done
           }
@@ -721,6 +850,7 @@ cudaError_t launch_wcsr_noalloc(WcsrParams p, const int64_t *window_row_ptr, int
   p.n_stages_dev = reinterpret_cast<int64_t *>(tail);
   p.status = reinterpret_cast<uint32_t *>(tail + 8);  // bounded-wait timeouts (not reported by this entry point)
   p.grid = num_sms < kNoallocMaxCtas ? num_sms : kNoallocMaxCtas;
+  p.dynamic = 0;
   wcsr_noalloc_stages_kernel<<<1, 1024, 0, stream>>>(window_row_ptr, n_windows, p.P_total, stages,
                                                       reinterpret_cast<int64_t *>(tail), p.status);
   e = cudaGetLastError();

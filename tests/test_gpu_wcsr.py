@@ -201,3 +201,74 @@ def test_wcsr64_uniform_full_size():
     C_ref, S_ref = oracle.spmm_csr(w.m, w.k, w.row_ptr, w.col_idx, w.vals, ocode(w.dtype), w.B())
     assert_parity(outs[0], C_ref, S_ref, "wcsr_uniform h64")
     assert info["n_groups"] == 256
+
+
+def _dyn_run(w_or_args, max_ctas=None, runs=2):
+    import sparse_dense_matrix_bcsr_gb300 as S
+    m, k, n, rp, ci, vals, dt, out_dt, B = w_or_args
+    return run_library("wcsr", m, k, rp, ci, vals, dt, out_dt, B, max_ctas=max_ctas, runs=runs,
+                       schedule=S.SPMM_SCHEDULE_DYNAMIC)
+
+
+def test_wcsr_dynamic_schedule_takes_over_chunks():
+    """Dynamic schedule with more chunks than CTAs fit on the GPU (about four
+    per resident CTA), so running CTAs cancel pending ones through cluster
+    launch control and take their chunks: every element matches the oracle,
+    and two runs are bitwise equal (the chunks are fixed and their partial
+    sums are added in chunk order, whichever CTA ran them)."""
+    rng = np.random.default_rng(2026)
+    m, k, n = 20000, 20000, 128
+    rp, ci, vals = W.random_csr(rng, m, k, 0.005, "bf16")
+    B = W.dense_bits(rng, (k, n), "u1", "bf16")
+    outs, info = _dyn_run((m, k, n, rp, ci, vals, "bf16", "f32", B))
+    assert info["n_tasks"] >= 32 * 4 * 152, "too few work items to give every chunk 32"
+    C_ref, S_ref = oracle.spmm_csr(m, k, rp, ci, vals, ocode("bf16"), B)
+    for C in outs:
+        assert_parity(C, C_ref, S_ref, "wcsr dynamic")
+    assert np.array_equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("ctas,n,out_dt", [(3, 256, "f32"), (5, 72, "bf16"), (2, 520, "f32")])
+def test_wcsr_dynamic_schedule_few_chunks(ctas, n, out_dt):
+    """Dynamic schedule with a CTA cap: a handful of chunks (all resident at
+    once, so every cancellation request finds nothing left), long windows cut
+    between chunks; parity with the oracle and bitwise-equal runs."""
+    rng = np.random.default_rng(300 + ctas)
+    m, k = 2400, 5000
+    rp, ci = W.powerlaw_pattern(rng, m, k, 1.3, 1, 1500, 300, 0.7)
+    vals = W.draw_values(rng, len(ci), "u1", "bf16")
+    B = W.dense_bits(rng, (k, n), "u1", "bf16")
+    outs, info = _dyn_run((m, k, n, rp, ci, vals, "bf16", out_dt, B), max_ctas=ctas)
+    C_ref, S_ref = oracle.spmm_csr(m, k, rp, ci, vals, ocode("bf16"), B)
+    for C in outs:
+        assert_parity(C, C_ref, S_ref, f"wcsr dynamic ctas={ctas} N={n}")
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_wcsr_irregular_dynamic_full_size_sampled():
+    """The irregular workload at full size under the dynamic schedule
+    (about 1200 chunks of about 62 work items), sampled in every window and
+    128-column strip."""
+    import sparse_dense_matrix_bcsr_gb300 as S
+    w = W.wcsr_irregular()
+    outs, info = run_library("wcsr", w.m, w.k, w.row_ptr, w.col_idx, w.vals, w.dtype, w.out_dtype, w.B(),
+                             keep_device=True, schedule=S.SPMM_SCHEDULE_DYNAMIC)
+    import torch
+    C = outs[0]
+    assert not torch.isnan(C).any().item(), "C not fully written"
+    rows, cols = stratified_positions(w.m, w.n, 16, 20000, 5)
+    sampled_parity(w, C, rows, cols)
+
+
+def test_dynamic_schedule_rejected_where_not_built():
+    import sparse_dense_matrix_bcsr_gb300 as S
+    rng = np.random.default_rng(5)
+    rp, ci, vals = W.random_csr(rng, 128, 128, 0.05, "bf16")
+    for create, a, b in ((S.spmm_bcsr_create, 64, 64), (S.spmm_wcsr_create, 64, 8)):
+        h = create(128, 128, rp, ci, vals, "bf16", "f32", a, b)
+        try:
+            with pytest.raises(S.SpmmError) as e:
+                S.spmm_set_schedule(h, S.SPMM_SCHEDULE_DYNAMIC)
+            assert e.value.status == S.SPMM_ERR_UNSUPPORTED
+        finally:
+            S.spmm_destroy(h)

@@ -119,6 +119,7 @@ CASES = [
     (5, 200, 0.30, 4, 32, "f16"),
     (100, 100, 0.0, 16, 16, "bf16"),   # empty matrix
     (33, 17, 1.0, 16, 16, "bf16"),     # full matrix, ragged edges
+    (150, 90, 0.05, 64, 8, "bf16"),    # the pages' WCSR geometry: 64-row windows, padding 8
 ]
 
 
