@@ -8,15 +8,19 @@
 //
 // Work list: every window is cut into stages of at most 64 packed columns,
 // listed in window order (a window without columns has one empty stage).  The
-// kernel is persistent: CTA c owns the contiguous range
-// [T*c/G, T*(c+1)/G) of the T = stages x column-tiles work items, so every
-// CTA gets the same number of stages whatever the window lengths, and the
-// column indices a CTA reads are contiguous.  A window whose stages are cut
-// by a range boundary is finished by a second kernel: each CTA writes the
-// fp32 partial sums of its first and last window to two workspace slots, and
-// the CTA that holds the window's first stage adds the slots of the following
-// CTAs in CTA order (the paper adds split partials with atomicAdd; the fixed
-// order here makes results bitwise reproducible).
+// T = stages x column-tiles work items are cut into G equal contiguous chunks,
+// chunk c = [T*c/G, T*(c+1)/G), and the grid has one CTA per chunk.  By
+// default G is the number of CTAs that fit (two per SM) and each CTA runs its
+// own chunk: every CTA gets the same number of stages whatever the window
+// lengths, and the column indices it reads are contiguous.  With p.dynamic
+// (Section V's future work on Blackwell) G is about four times that, and a
+// CTA that finishes a chunk cancels the launch of a CTA that has not started
+// and takes over its chunk (cluster launch control).  A window whose stages
+// are cut by a chunk boundary is finished by a second kernel: each chunk's
+// fp32 partial sums of its first and last window go to two workspace slots,
+// and the slot holding the window's first stage adds the slots of the
+// following chunks in chunk order (the paper adds split partials with
+// atomicAdd; the fixed order here makes results bitwise reproducible).
 //
 // The product is computed transposed: the 128 columns of an accumulator are
 // the MMA's M (TMEM lanes) and the 16 rows of a window are the MMA's N.
@@ -32,12 +36,13 @@
 // writes to shared memory, and the epilogue learns a window's identity from a
 // record the MMA thread writes, so neither waits on a global load.
 //
-// PW + 5 warps (PW producer warps; two CTAs per SM run with PW = 2, so one
-// CTA's barrier handshakes and MMA issue stalls overlap the other's work):
-//   warps 0..PW-1  producers; warp w owns the work items w, w+PW, ... of the
-//                  CTA's range; it copies an item's 64 B rows with 16-byte
-//                  cp.async (one B row, 512 B, per warp instruction at
-//                  BN = 256); every lane ends the item with
+// PW + 5 warps (two CTAs per SM, so one CTA's barrier handshakes and MMA
+// issue stalls overlap the other's work):
+//   warps 0..PW-1  producers, in groups of WPG warps; group g owns the work
+//                  items g, g + PW/WPG, ... of the CTA's sequence, and each
+//                  warp of a group copies its share of an item's 64 B rows
+//                  with 16-byte cp.async (one B row, 512 B, per warp
+//                  instruction at BN = 256); every lane ends the item with
 //                  cp.async.mbarrier.arrive.noinc, so producers never block
 //                  on their own copies and one warp's barrier handling
 //                  overlaps another's copies
@@ -81,12 +86,17 @@ constexpr int32_t kRecEnd = 16;
 // its index record is fetched).
 constexpr int kIdxLead = 4;
 
-// NACC accumulators of 128 columns, Q stages, PW producer warps, MINB CTAs per
+// NACC accumulators of 128 columns, Q stages, PW producer warps in groups of
+// WPG (the WPG warps of a group copy disjoint row ranges of the same work
+// items: a warp's cp.async issue rate is limited, about 13 bytes per clock on
+// GB300, so the gather rate of an SM grows with its copying warps up to about
+// 12), MINB CTAs per
 // SM, ILEAD index-record slots per producer warp (0: indices are read from
 // global memory, the no-allocation variant).  A stage holds an item's gathered
 // B rows and its value tile.
-template <int NACC, int Q, int PW, int MINB, int ILEAD>
+template <int NACC, int Q, int PW, int WPG, int MINB, int ILEAD>
 struct Cfg {
+  static constexpr int kGroups = PW / WPG;                  // producer groups: group g owns items g, g + kGroups, ...
   static constexpr int kMmaWarp = PW;                        // warps 0..PW-1 produce, PW issues MMAs
   static constexpr int kThreads = 32 * (PW + 1 + kEpiWarps);
   static constexpr int kBN = 128 * NACC;
@@ -103,10 +113,11 @@ struct Cfg {
   // A producer's wait for stage (it % Q) to be free is a parity wait on the
   // MMA commit of item it - Q; it is only unambiguous if the commit of item
   // it - 2Q has already been seen, which the warp's wait for its previous item
-  // (it - PW) guarantees when PW <= Q.  With more producer warps than stages a
-  // warp could run two phases ahead, pass the wait early and overwrite a stage
-  // still in use.
-  static_assert(PW <= Q, "more producer warps than stages");
+  // (it - kGroups) guarantees when kGroups <= Q.  With more producer groups
+  // than stages a warp could run two phases ahead, pass the wait early and
+  // overwrite a stage still in use.
+  static_assert(PW % WPG == 0 && 64 % WPG == 0 && WPG <= 4, "producer groups");
+  static_assert(kGroups <= Q, "more producer groups than stages");
   static_assert(kRespSlots * 16 + kBars * 8 + 16 + Q * 32 + kAccBufs * 32 <= kMiscBytes, "barrier area");
   static_assert(kSmemBytes <= 227 * 1024 && MINB * (kSmemBytes + 1024) <= 228 * 1024, "shared memory");
   static_assert(MINB * kTmemCols <= 512, "TMEM");
@@ -135,11 +146,12 @@ struct SegRec {     // MMA -> epilogue, one per accumulator buffer
 // read from device memory (the stage list is built on the device), CTAs
 // beyond the number of work items leave at once, and column indices are read
 // from window_col_idx at each stage's first packed column.
-template <int NACC, int Q, int PW, int MINB, bool IN_BF16, bool OUT_BF16, bool NOALLOC = false>
+template <int NACC, int Q, int PW, int WPG, int MINB, bool IN_BF16, bool OUT_BF16, bool NOALLOC = false>
 __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
     wcsr_spmm_kernel(const WcsrParams p) {
   constexpr int kILead = NOALLOC ? 0 : kIdxLead;
-  using C_ = Cfg<NACC, Q, PW, MINB, kILead>;
+  using C_ = Cfg<NACC, Q, PW, WPG, MINB, kILead>;
+  static_assert(!NOALLOC || WPG == 1, "the no-allocation variant copies each item with one warp");
   constexpr int kMmaWarp = C_::kMmaWarp;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -180,10 +192,11 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < Q; ++q) {
-      // 32 cp.async lane arrivals (gathered rows; the value tile too in the
-      // no-allocation variant) + lane 0's arrive, which releases the stage
-      // record and expects the value tile's TMA bytes
-      mbar_init(full0 + 8 * q, 33);
+      // 32 cp.async lane arrivals per warp of the item's group (gathered rows;
+      // the value tile too in the no-allocation variant) + one arrive of the
+      // group's first warp, which releases the stage record and expects the
+      // value tile's TMA bytes
+      mbar_init(full0 + 8 * q, 1 + 32 * WPG);
       mbar_init(empty0 + 8 * q, 1);
     }
     for (int b = 0; b < kAccBufs; ++b) {
@@ -212,7 +225,10 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
   if (warp < PW) {
     // ------------------------------------------------------------ producers
     const uint16_t *Bp = reinterpret_cast<const uint16_t *>(p.B);
-    constexpr int kStep = PW;
+    constexpr int kStep = PW;                 // (no-allocation variant: one warp per group)
+    constexpr int G = C_::kGroups;
+    const int grp = warp / WPG, sub = warp % WPG;
+    const int rbeg = sub * (64 / WPG), rend = rbeg + 64 / WPG;  // this warp's rows of every item
     // The B rows of one work item -> stage `st` with 16-byte cp.async; lo /
     // hi hold the item's column indices for positions lane and 32 + lane.
     // Only the 16-byte units of the tile's live columns (below N) are copied:
@@ -222,7 +238,9 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
     // zero-filled, since its zero values multiply it.  Each warp instruction
     // copies 32 (row, unit) pairs, U units per row (U = live units rounded up
     // to a power of two), so at small N a stage costs a few instructions.
+    // Only rows [rbeg, rend) are copied by this warp.
     auto gather = [&](uint32_t st, int n0, int ncols, int32_t lo, int32_t hi) {
+      const int rlim = min(ncols, rend);
       const int live_units = (min(C_::kBN, p.N - n0) + 7) >> 3;  // 1 .. 16 * NACC
       if (live_units == 16 * NACC) {
         // every unit live: the row layout is fixed at compile time (one B row
@@ -233,7 +251,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         const int n = n0 + v * 8;
         const uint32_t dst_col = (v >> 3) * kChunkBytes;
         const uint32_t uu = static_cast<uint32_t>(v & 7);
-        for (int r0 = 0; r0 < ncols; r0 += 16) {
+        for (int r0 = rbeg; r0 < rlim; r0 += 16) {
           const int32_t src = r0 < 32 ? lo : hi;
           constexpr int kInst = 16 / kRowsPerInst;
           int32_t col[kInst];
@@ -254,7 +272,8 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
       }
       const int sh = 32 - __clz(live_units - 1);                 // log2 of U (0 for one unit)
       const int rsh = 5 - sh;                                    // log2 of rows per instruction
-      const int ninst = (ncols + (1 << rsh) - 1) >> rsh;
+      const int i_beg = rbeg >> rsh;                             // instructions holding rows [rbeg, rlim)
+      const int i_end = (rlim + (1 << rsh) - 1) >> rsh;
       const int r_lane = lane >> sh;                             // this lane's row within an instruction
       const int u = lane & ((1 << sh) - 1);                      // this lane's unit within its row
       const int n = n0 + u * 8;
@@ -263,7 +282,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
       const uint32_t uu = static_cast<uint32_t>(u & 7);
       // 16 instructions at a time: their shuffles issue back to back instead
       // of each copy waiting for the last
-      for (int i0 = 0; i0 < ninst; i0 += 16) {
+      for (int i0 = i_beg; i0 < i_end; i0 += 16) {
         int32_t col[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -273,7 +292,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int r = ((i0 + j) << rsh) + r_lane;
-          if (i0 + j < ninst && u_live && r < ncols) {
+          if (i0 + j < i_end && u_live && r >= rbeg && r < rlim) {
             // caller-supplied indices (no-allocation variant) are clamped to B's rows
             const bool live = col[j] >= 0 && (!NOALLOC || col[j] < p.K);
             cp_async_16(st + dst_u + r * 128 + ((uu ^ static_cast<uint32_t>(r & 7)) << 4),
@@ -284,16 +303,16 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         }
       }
     };
-    // The end of the CTA's work: the owner of CTA-local item it_end (the one
-    // after the last, warp it_end % PW) passes an end record to the MMA warp
-    // through stage it_end % Q.
+    // The end of the CTA's work: the group owning CTA-local item it_end (the
+    // one after the last, group it_end % G) passes an end record to the MMA
+    // warp through stage it_end % Q.
     auto send_end = [&](int64_t it_end) -> bool {
       const uint32_t stage = static_cast<uint32_t>(it_end % Q);
       const uint32_t phase = static_cast<uint32_t>((it_end / Q) & 1);
       bool r = mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns);
       r = __shfl_sync(0xffffffffu, r && !*abort_flag, 0);
       if (!r) return false;
-      if (lane == 0) {
+      if (lane == 0 && sub == 0) {
         stage_rec[stage] = StageRec{0, kRecEnd, -1, 0, 0, {0, 0, 0}};
         mbar_arrive(full0 + 8 * stage);
       }
@@ -387,9 +406,9 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
       // requests the next chunk when it learns of one, into answer slot
       // (ordinal % kRespSlots); every producer warp reads the same answers,
       // so all of them see the same sequence.  CTA-local item it (0, 1, ...
-      // across the chunks) belongs to warp it % PW and stage it % Q.
+      // across the chunks) belongs to producer group it % G and stage it % Q.
       //
-      // Warp w fetches the index part of its own item j's record (272 bytes)
+      // Each warp fetches the index part of its group's item j's record (272 bytes)
       // kILead of its items ahead into slot j % kILead of its ring, and when
       // it starts item j it reads the indices from there (the slot is then
       // refilled), waits for the item's stage to be free, has the value tile
@@ -462,18 +481,18 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
       };
       int64_t n_fetched = 0;  // own items whose index records were requested (a prefix)
       auto fetch_idx = [&](int64_t j) -> bool {
-        const int q = locate(warp + PW * j);
+        const int q = locate(grp + G * j);
         if (q == -2) return false;
         if (q >= 0) {
           const Chunk &c = kn[q & 3];
-          const int64_t fj = c.g0 + (warp + PW * j - c.lbase);
+          const int64_t fj = c.g0 + (grp + G * j - c.lbase);
           if (lane == 0) {
             const uint32_t slot = static_cast<uint32_t>(j % kILead);
             const uint8_t *src = pack + (fj % n_stages) * kWcsrPackBytes;
             mbar_arrive_expect_tx(ifull_w + 8 * slot, kMetaBytes);
             tma_bulk_load(smem_addr(ring + slot * kMetaBytes), src + kWcsrPackIdxOff, kMetaBytes,
                           ifull_w + 8 * slot);
-            prefetch_l2_bulk(src + kWcsrPackValOff, kValBytes);
+            if (sub == 0) prefetch_l2_bulk(src + kWcsrPackValOff, kValBytes);
           }
           n_fetched = j + 1;
         }
@@ -483,7 +502,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
       for (int j = 0; j < kILead && ok; ++j) ok = fetch_idx(j);
       int64_t consumed = 0;  // own items whose indices were read
       for (int64_t j = 0; ok; ++j) {
-        const int64_t it = warp + PW * j;
+        const int64_t it = grp + G * j;
         const int q = locate(it);
         if (q == -2) ok = false;
         if (q < 0) break;
@@ -511,7 +530,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         const int tile = static_cast<int>(f / n_stages);
         const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
         const uint32_t fb = full0 + 8 * stage;
-        if (lane == 0) {
+        if (lane == 0 && sub == 0) {
           if (it == c.lbase) {  // the chunk's partial-sum records (overwritten when used)
             p.partials[2 * c.id] = PartialRec{-1, 0, 0, 0};
             p.partials[2 * c.id + 1] = PartialRec{-1, 0, 0, 0};
@@ -525,7 +544,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         gather(st, tile * C_::kBN, d.x, lo, hi);
         cp_async_arrive_noinc(fb);
       }
-      if (ok && l_end % PW == warp) ok = send_end(l_end);
+      if (ok && l_end % G == grp) ok = send_end(l_end);
       cp_async_wait_all();
       if (!ok && lane == 0) {
         atomicOr(p.status, kDevTimeout);
@@ -706,10 +725,10 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
   }
 }
 
-template <int NACC, int Q, int PW, int MINB, bool IN_BF16, bool OUT_BF16>
+template <int NACC, int Q, int PW, int WPG, int MINB, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_variant(const WcsrParams &p, cudaStream_t stream) {
-  using C_ = Cfg<NACC, Q, PW, MINB, kIdxLead>;
-  auto kern = wcsr_spmm_kernel<NACC, Q, PW, MINB, IN_BF16, OUT_BF16>;
+  using C_ = Cfg<NACC, Q, PW, WPG, MINB, kIdxLead>;
+  auto kern = wcsr_spmm_kernel<NACC, Q, PW, WPG, MINB, IN_BF16, OUT_BF16>;
   static std::atomic<uint64_t> smem_set{0};  // per instantiation, one bit per device
   cudaError_t e = set_smem_limit_once(kern, C_::kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
@@ -720,13 +739,13 @@ cudaError_t launch_variant(const WcsrParams &p, cudaStream_t stream) {
                                            C_::kBN, stream);
 }
 
-template <int NACC, int Q, int PW, int MINB>
+template <int NACC, int Q, int PW, int WPG, int MINB>
 cudaError_t launch_dtypes(const WcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t s) {
   if (in_bf16)
-    return out_bf16 ? launch_variant<NACC, Q, PW, MINB, true, true>(p, s)
-                    : launch_variant<NACC, Q, PW, MINB, true, false>(p, s);
-  return out_bf16 ? launch_variant<NACC, Q, PW, MINB, false, true>(p, s)
-                  : launch_variant<NACC, Q, PW, MINB, false, false>(p, s);
+    return out_bf16 ? launch_variant<NACC, Q, PW, WPG, MINB, true, true>(p, s)
+                    : launch_variant<NACC, Q, PW, WPG, MINB, true, false>(p, s);
+  return out_bf16 ? launch_variant<NACC, Q, PW, WPG, MINB, false, true>(p, s)
+                  : launch_variant<NACC, Q, PW, WPG, MINB, false, false>(p, s);
 }
 
 // ------------------------------------------------------------ no-allocation variant
@@ -796,8 +815,8 @@ __global__ void __launch_bounds__(1024)
 
 template <int NACC, int Q, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_noalloc_variant(const WcsrParams &p, cudaStream_t stream) {
-  using C_ = Cfg<NACC, Q, 4, 1, 0>;
-  auto kern = wcsr_spmm_kernel<NACC, Q, 4, 1, IN_BF16, OUT_BF16, true>;
+  using C_ = Cfg<NACC, Q, 4, 1, 1, 0>;
+  auto kern = wcsr_spmm_kernel<NACC, Q, 4, 1, 1, IN_BF16, OUT_BF16, true>;
   static std::atomic<uint64_t> smem_set{0};  // per instantiation, one bit per device
   cudaError_t e = set_smem_limit_once(kern, C_::kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
@@ -883,10 +902,17 @@ constexpr bool kWideTiles = true;
 
 int wcsr_tile_cols(int64_t N) { return (N <= 128 || !kWideTiles) ? 128 : 256; }
 
+// Launch shapes, two CTAs per SM (one CTA per SM with more stages and
+// producers measured 35-70 % slower: the single MMA-issuing thread of a CTA
+// becomes the limit).  128-column items: five 18 KB stages, four producer
+// warps each copying whole items.  256-column items: three 34 KB stages,
+// three producer groups of two warps (each warp copies 32 of an item's 64
+// rows): 12 copying warps per SM instead of 6, 7 % faster on the uniform
+// matrix; at 128 columns the same split was 12 % slower.
 cudaError_t launch_wcsr(const WcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream) {
   if (p.n_stages == 0 || p.N == 0 || p.grid == 0) return cudaSuccess;
-  if (wcsr_tile_cols(p.N) == 128) return launch_dtypes<1, 5, 4, 2>(p, in_bf16, out_bf16, stream);
-  return launch_dtypes<2, 3, 3, 2>(p, in_bf16, out_bf16, stream);
+  if (wcsr_tile_cols(p.N) == 128) return launch_dtypes<1, 5, 4, 1, 2>(p, in_bf16, out_bf16, stream);
+  return launch_dtypes<2, 3, 6, 2, 2>(p, in_bf16, out_bf16, stream);
 }
 
 }  // namespace spmm
