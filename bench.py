@@ -40,18 +40,18 @@ sys.path.insert(0, ROOT)
 
 import spmm_workloads as W  # noqa: E402
 
-METRIC = "SpMM effective TFLOP/s (2*nnz*N/t), BCSR and WCSR"
+METRIC = "SpMM effective TFLOP/s (2·nnz·N/t) and % of roofline, BCSR and WCSR"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
 # valid only for the kernel source it was taken on (sha256 of the file).
 MEASURED_TRAFFIC = {
-    # bcsr_weight: 376 MB measured at N = 8192; B and C scale with N, A (13.6 MB)
-    # does not: 13.6 MB + 8 x 362.5 MB at N = 65536
-    "bcsr_kernel.cu": {"src_sha": "2acc16b6708d6524", "bytes_per_launch": 2.914e9},
-    # wcsr_uniform at its benchmark size
-    "wcsr_kernel.cu": {"src_sha": "4a2ab33295fb992a", "bytes_per_launch": 1.086e8},
+    # bcsr_weight: 114.5 MB read + 261.4 MB written at N = 8192; B and C scale
+    # with N, A (13.6 MB) does not: 13.6 MB + 8 x 362.3 MB at N = 65536
+    "bcsr_kernel.cu": {"src_sha": "6ca8a92fad3c6c13", "bytes_per_launch": 2.912e9},
+    # wcsr_uniform at its benchmark size: 100.2 MB read + 15.9 MB written
+    "wcsr_kernel.cu": {"src_sha": "218398c36b4bebd7", "bytes_per_launch": 1.162e8},
 }
 
 
@@ -483,11 +483,20 @@ def run_sweep(args):
                 ("bcsr_weight", lambda n: [W.bcsr_weight(n=n) if n else W.bcsr_weight()]),
                 ("bcsr_sweep", lambda n: [W.bcsr_sweep(s, k) for s in W.BCSR_SWEEP_SPARSITY for k in W.SWEEP_N]),
                 ("wcsr_sweep", lambda n: [W.wcsr_sweep(d, k) for d in W.WCSR_SWEEP_DENSITY for k in W.SWEEP_N])]
-    # an entry may end in _h64 (the WCSR matrix in 64-row windows with column
-    # padding 8, the paper's WCSR geometry) and/or _dyn (the WCSR dynamic
-    # schedule); bcsr_sweep_95_N256 or wcsr_sweep_0.1_N8 name one sweep point
-    def variant(ws, h64, dyn):
+    # an entry may end in _rcm (rows in reverse Cuthill-McKee order before the
+    # format is built; C comes out in that row order), _h64 (the WCSR matrix
+    # in 64-row windows with column padding 8, the paper's WCSR geometry)
+    # and/or _dyn (the WCSR dynamic schedule), in that order;
+    # bcsr_sweep_95_N256 or wcsr_sweep_0.1_N8 name one sweep point
+    def variant(ws, h64, dyn, rcm=False):
         for w in ws:
+            if rcm:
+                from sparse_dense_matrix_bcsr_gb300 import reorder
+                t0 = time.perf_counter()
+                perm = reorder.rcm_row_order(w.m, w.k, w.row_ptr, w.col_idx)
+                w.row_ptr, w.col_idx, w.vals = reorder.permute_rows(w.row_ptr, w.col_idx, w.vals, perm)
+                w.name += "_rcm"
+                w.meta["desc"] = w.describe() + f" (RCM rows, {time.perf_counter() - t0:.1f} s on the host)"
             if h64:
                 w.b_row, w.b_col = 64, 8
                 w.name += "_h64"
@@ -503,11 +512,13 @@ def run_sweep(args):
     for e, n in sel.items():
         if e == "linear_weight":
             continue
-        base, h64, dyn = e, False, False
+        base, h64, dyn, rcm = e, False, False, False
         if base.endswith("_dyn"):
             base, dyn = base[:-4], True
         if base.endswith("_h64"):
             base, h64 = base[:-4], True
+        if base.endswith("_rcm"):
+            base, rcm = base[:-4], True
         parts = base.split("_")
         if base in named:
             fn = (lambda b=named[base], n=n: b(n))
@@ -517,7 +528,7 @@ def run_sweep(args):
                 (lambda lvl=lvl, nn=nn: [W.wcsr_sweep(lvl, nn)])
         else:
             raise SystemExit(f"unknown configuration {e!r}")
-        cfgs.append((e, lambda fn=fn, h64=h64, dyn=dyn: variant(fn(), h64, dyn)))
+        cfgs.append((e, lambda fn=fn, h64=h64, dyn=dyn, rcm=rcm: variant(fn(), h64, dyn, rcm)))
     if "linear_weight" in sel:
         run_linear_sweep(args, peaks, stream, flush)
     for name, b in cfgs:
