@@ -304,8 +304,10 @@ spmm_status spmm_probe_l2_read(const void *buf, int64_t bytes, int32_t passes, v
  * Every call uses the same array, which keeps the previous call's contents
  * (each call rebuilds what it reads): calls whose work overlaps on the GPU
  * (other streams, other host threads) race and must be serialised by the
- * caller.  Asynchronous on `stream`; a bounded wait that runs out is not
- * reported here.
+ * caller.  Asynchronous on `stream`; a bounded wait that runs out, or a
+ * window_row_ptr that fails the device-side check (first entry 0, entries
+ * non-decreasing multiples of 16, last entry p_total), is reported by
+ * spmm_wcsr_noalloc_check, not here.
  * Errors: INVALID_ARG (null pointers, sizes), UNSUPPORTED (N % 8,
  * alignment, p_total % 16, the size limit, no sm_103 device), CUDA (launch).
  */
@@ -313,6 +315,17 @@ spmm_status spmm_wcsr_run_noalloc(const int64_t *window_row_ptr, const int32_t *
                                   const void *values, int64_t m, int64_t k, int64_t p_total,
                                   spmm_dtype in_t, spmm_dtype out_t, const void *B, void *C,
                                   int64_t N, void *stream);
+
+/*
+ * spmm_wcsr_noalloc_check -- waits for `stream`, then reads and clears the
+ * status word that spmm_wcsr_run_noalloc calls on the current device share
+ * (a call resets it when it starts, so it describes the last call):
+ * SPMM_OK; SPMM_ERR_DEVICE_CHECK when window_row_ptr failed the device-side
+ * check (no work was listed, C was left as it was); SPMM_ERR_TIMEOUT when a
+ * bounded wait ran out (C is incomplete).  Allocates nothing.
+ * Errors: CUDA (the copy or the synchronisation).
+ */
+spmm_status spmm_wcsr_noalloc_check(void *stream);
 
 /* spmm_status_str -- static English name of a status. */
 const char *spmm_status_str(spmm_status s);

@@ -49,7 +49,7 @@ EXPORTS = (
     "spmm_format_info", "spmm_export_format", "spmm_bcsr_convert", "spmm_wcsr_convert",
     "spmm_check", "spmm_set_max_ctas", "spmm_selftest_wait_timeout", "spmm_status_str",
     "spmm_last_error", "spmm_wcsr_run_noalloc", "spmm_run_linear", "spmm_set_schedule",
-    "spmm_probe_l2_read",
+    "spmm_probe_l2_read", "spmm_wcsr_noalloc_check",
 )
 
 
@@ -100,6 +100,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "spmm_set_schedule": [P, ctypes.c_int32],
         "spmm_selftest_wait_timeout": [I64, P, ctypes.POINTER(ctypes.c_int32)],
         "spmm_probe_l2_read": [P, I64, I32, P, P],
+        "spmm_wcsr_noalloc_check": [P],
         "spmm_wcsr_run_noalloc": [P, P, P, I64, I64, I64, I32, I32, P, P, I64, P],
     }
     for name, args in sig.items():
@@ -237,6 +238,12 @@ def spmm_selftest_wait_timeout(timeout_ns: int, stream: int = 0) -> int:
     _check(load_library().spmm_selftest_wait_timeout(timeout_ns, stream or None, ctypes.byref(out)),
            "spmm_selftest_wait_timeout")
     return out.value
+
+
+def spmm_wcsr_noalloc_check(stream: int = 0) -> int:
+    """Status of the last spmm_wcsr_run_noalloc call on the current device
+    (waits for `stream`): SPMM_OK, SPMM_ERR_DEVICE_CHECK or SPMM_ERR_TIMEOUT."""
+    return load_library().spmm_wcsr_noalloc_check(stream or None)
 
 
 def spmm_probe_l2_read(buf: int, nbytes: int, passes: int, sink: int, stream: int = 0) -> None:

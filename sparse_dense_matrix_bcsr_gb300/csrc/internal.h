@@ -166,6 +166,9 @@ constexpr int kNoallocMaxCtas = 256;
 // window_row_ptr into the static scratch, runs the WCSR kernel's no-allocation
 // variant and the partial-sum pass.  p carries the caller's arrays, B, C and
 // the sizes; the scratch pointers are filled in here.
+// Copies the no-allocation scratch's status word of the current device into
+// *word and clears it, after the work queued on `stream` (synchronises it).
+cudaError_t wcsr_noalloc_take_status(uint32_t *word, cudaStream_t stream);
 cudaError_t launch_wcsr_noalloc(WcsrParams p, const int64_t *window_row_ptr, int64_t n_windows, int num_sms,
                                 bool in_bf16, bool out_bf16, cudaStream_t stream);
 size_t wcsr_noalloc_scratch_bytes();

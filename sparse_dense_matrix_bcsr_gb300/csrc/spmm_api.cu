@@ -891,6 +891,16 @@ __global__ void __launch_bounds__(512) l2_read_kernel(const uint4 *__restrict__ 
 }  // namespace
 }  // namespace spmm
 
+extern "C" spmm_status spmm_wcsr_noalloc_check(void *stream) {
+  uint32_t word = 0;
+  cudaError_t e = spmm::wcsr_noalloc_take_status(&word, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "reading the no-allocation status word");
+  if (word & spmm::kDevIndex)
+    return fail(SPMM_ERR_DEVICE_CHECK, "window_row_ptr failed the device check; no work was listed");
+  if (word & spmm::kDevTimeout) return fail(SPMM_ERR_TIMEOUT, "a bounded wait ran out in the WCSR kernel");
+  return SPMM_OK;
+}
+
 extern "C" spmm_status spmm_probe_l2_read(const void *buf, int64_t bytes, int32_t passes, void *sink,
                                           void *stream) {
   if (!buf || !sink) return fail(SPMM_ERR_INVALID_ARG, "buf or sink is NULL");

@@ -840,34 +840,55 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes]
 
 size_t wcsr_noalloc_scratch_bytes() { return kNoallocScratchBytes; }
 
-cudaError_t launch_wcsr_noalloc(WcsrParams p, const int64_t *window_row_ptr, int64_t n_windows, int num_sms,
-                                bool in_bf16, bool out_bf16, cudaStream_t stream) {
-  // Device address of the scratch array, looked up once per device with
-  // that device current (in host code the array's name is only a stand-in).
+namespace {
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current (in host code the array's name is only
+// a stand-in).
+cudaError_t noalloc_base(uint8_t **base) {
   static std::mutex mu;
   static uint8_t *addr[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  uint8_t *base;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-      void *ptr = nullptr;
-      e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-      if (e != cudaSuccess) return e;
-      addr[dev] = static_cast<uint8_t *>(ptr);
-    }
-    base = addr[dev];
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<uint8_t *>(ptr);
   }
+  *base = addr[dev];
+  return cudaSuccess;
+}
+
+// The status word (bounded-wait timeouts, the stage-list check) in the
+// scratch's spare tail.
+constexpr size_t kNoallocStatusOff = kNoallocStageBytes + kNoallocWsBytes + kNoallocRecBytes + 8;
+}  // namespace
+
+cudaError_t wcsr_noalloc_take_status(uint32_t *word, cudaStream_t stream) {
+  uint8_t *base = nullptr;
+  cudaError_t e = noalloc_base(&base);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyAsync(word, base + kNoallocStatusOff, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(base + kNoallocStatusOff, 0, sizeof(uint32_t), stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  return e;
+}
+
+cudaError_t launch_wcsr_noalloc(WcsrParams p, const int64_t *window_row_ptr, int64_t n_windows, int num_sms,
+                                bool in_bf16, bool out_bf16, cudaStream_t stream) {
+  uint8_t *base = nullptr;
+  cudaError_t e = noalloc_base(&base);
+  if (e != cudaSuccess) return e;
   WcsrStage *stages = reinterpret_cast<WcsrStage *>(base);
   p.stages = stages;
   p.workspace = reinterpret_cast<float *>(base + kNoallocStageBytes);
   p.partials = reinterpret_cast<PartialRec *>(base + kNoallocStageBytes + kNoallocWsBytes);
   uint8_t *tail = base + kNoallocStageBytes + kNoallocWsBytes + kNoallocRecBytes;  // 256 spare bytes
   p.n_stages_dev = reinterpret_cast<int64_t *>(tail);
-  p.status = reinterpret_cast<uint32_t *>(tail + 8);  // bounded-wait timeouts (not reported by this entry point)
+  p.status = reinterpret_cast<uint32_t *>(base + kNoallocStatusOff);  // read by wcsr_noalloc_take_status
   p.grid = num_sms < kNoallocMaxCtas ? num_sms : kNoallocMaxCtas;
   p.dynamic = 0;
   wcsr_noalloc_stages_kernel<<<1, 1024, 0, stream>>>(window_row_ptr, n_windows, p.P_total, stages,

@@ -73,6 +73,7 @@ def test_noalloc_matches_handle_on_two_calls(S, name, out_t):
         S.spmm_wcsr_run_noalloc(d_ptr.data_ptr(), d_idx.data_ptr(), d_val.data_ptr(), m, k, len(idx),
                                 "bf16", out_t, dB.data_ptr(), C.data_ptr(), n, stream)
         torch.cuda.synchronize()
+        assert S.spmm_wcsr_noalloc_check(stream) == S.SPMM_OK
         got = C.double().cpu().numpy()
         assert not np.isnan(got).any(), f"call {call}: C not fully written"
         assert np.all(np.abs(got - C_orc) <= bound), f"call {call}: differs from the oracle beyond the bound"
@@ -110,11 +111,13 @@ def test_noalloc_turns_away_a_bad_window_row_ptr(S, defect):
     S.spmm_wcsr_run_noalloc(torch.from_numpy(bad).cuda().data_ptr(), d_idx.data_ptr(), d_val.data_ptr(), m, k,
                             len(idx), "bf16", "f32", dB.data_ptr(), C.data_ptr(), n, stream)
     torch.cuda.synchronize()
+    assert S.spmm_wcsr_noalloc_check(stream) == S.SPMM_ERR_DEVICE_CHECK
     assert bool((C == 7.0).all().item()), "C was written although window_row_ptr was rejected"
     d_ptr = torch.from_numpy(ptr).cuda()
     S.spmm_wcsr_run_noalloc(d_ptr.data_ptr(), d_idx.data_ptr(), d_val.data_ptr(), m, k, len(idx), "bf16", "f32",
                             dB.data_ptr(), C.data_ptr(), n, stream)
     torch.cuda.synchronize()
+    assert S.spmm_wcsr_noalloc_check(stream) == S.SPMM_OK
     C_orc, Sabs = oracle.spmm_csr(m, k, rp, ci, vals, oracle.BF16, B)
     assert np.all(np.abs(C.double().cpu().numpy() - C_orc) <= 4.0 * 2.0 ** -8 * Sabs + 1e-6)
 
