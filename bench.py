@@ -486,10 +486,15 @@ def run_sweep(args):
     # an entry may end in _rcm (rows in reverse Cuthill-McKee order before the
     # format is built; C comes out in that row order), _h64 (the WCSR matrix
     # in 64-row windows with column padding 8, the paper's WCSR geometry)
-    # and/or _dyn (the WCSR dynamic schedule), in that order;
+    # and/or _dyn (the WCSR dynamic schedule) or _split (the BCSR split
+    # schedule), in that order;
     # bcsr_sweep_95_N256 or wcsr_sweep_0.1_N8 name one sweep point
-    def variant(ws, h64, dyn, rcm=False):
+    def variant(ws, h64, dyn, rcm=False, split=False):
         for w in ws:
+            if split:
+                w.name += "_split"
+                w.meta["schedule"] = S.SPMM_SCHEDULE_SPLIT
+                w.meta["desc"] = w.describe() + " (split schedule)"
             if rcm:
                 from sparse_dense_matrix_bcsr_gb300 import reorder
                 t0 = time.perf_counter()
@@ -512,7 +517,9 @@ def run_sweep(args):
     for e, n in sel.items():
         if e == "linear_weight":
             continue
-        base, h64, dyn, rcm = e, False, False, False
+        base, h64, dyn, rcm, split = e, False, False, False, False
+        if base.endswith("_split"):
+            base, split = base[:-6], True
         if base.endswith("_dyn"):
             base, dyn = base[:-4], True
         if base.endswith("_h64"):
@@ -528,7 +535,7 @@ def run_sweep(args):
                 (lambda lvl=lvl, nn=nn: [W.wcsr_sweep(lvl, nn)])
         else:
             raise SystemExit(f"unknown configuration {e!r}")
-        cfgs.append((e, lambda fn=fn, h64=h64, dyn=dyn, rcm=rcm: variant(fn(), h64, dyn, rcm)))
+        cfgs.append((e, lambda fn=fn, h64=h64, dyn=dyn, rcm=rcm, split=split: variant(fn(), h64, dyn, rcm, split)))
     if "linear_weight" in sel:
         run_linear_sweep(args, peaks, stream, flush)
     for name, b in cfgs:

@@ -36,6 +36,9 @@ def full_check(m, k, n, rp, ci, vals, dt, out_dt, B, runs=1):
     (300, 200, 72, 0.6, "bf16", "f32"),     # ragged M, K, N < 128
     (640, 448, 264, 0.4, "bf16", "f32"),    # N spans two 256-wide tiles + tail
     (256, 1024, 8, 0.3, "bf16", "f32"),     # N = 8
+    (300, 200, 40, 0.6, "bf16", "f32"),     # ragged M, K and N
+    (20000, 448, 64, 0.5, "f16", "f32"),    # several tiles per CTA (the stage ring wraps)
+    (130, 130, 24, 0.5, "bf16", "bf16"),    # N < 64 with bf16 C
     (192, 320, 256, 1.0, "f16", "bf16"),    # dense blocks everywhere, bf16 C
     (130, 130, 136, 0.5, "bf16", "bf16"),   # partial last block row / column
 ])
