@@ -75,14 +75,16 @@ struct TileRec {
   int32_t br;     // block row
   int32_t nt;     // column tile
   int32_t flags;
-  int32_t pad_;
+  int32_t nblk;   // blocks in the stage (1 .. KB)
 };
 
 // BN columns per tile, Q pipeline stages, NBUF TMEM accumulators, the
 // epilogue writing each warp's share of a tile in PARTS column parts through
 // two alternating staging buffers, MINB CTAs per SM, PW producer warps (warp
 // w issues the stages s with s % PW == w; warps PW and PW+1..PW+4 are the MMA
-// issuer and the epilogue).
+// issuer and the epilogue), KB consecutive blocks of a block row per stage
+// (each with its own B tile; more MMA work per barrier handshake, whose fixed
+// cost bounds problems with few long block rows).
 //
 // Narrow tiles (BN = 128) use the plain MMA, M = 64 x N = 128: the
 // accumulator's rows 16s..16s+15 sit in TMEM lanes 32s..32s+15, so epilogue
@@ -92,7 +94,7 @@ struct TileRec {
 // columns 0..127 and in lanes 64..127 for columns 128..255, in 128 TMEM
 // columns, so warp s holds rows 32(s%2)..32(s%2)+31 x columns 128(s/2) ..
 // 128(s/2)+127 and stores 32-row x 64-byte boxes (64-byte swizzle).
-template <int BN, int Q, int NBUF, int PARTS, int MINB, int PW, bool OUT_BF16>
+template <int BN, int Q, int NBUF, int PARTS, int MINB, int PW, int KB, bool OUT_BF16>
 struct Cfg {
   static constexpr int kMmaWarp = PW;
   static constexpr int kEpiWarp0 = PW + 1;
@@ -102,7 +104,8 @@ struct Cfg {
   static constexpr int kNmma = BN < 256 ? BN : 256;           // N of one MMA
   static constexpr int kMmas = BN / kNmma;                    // MMAs per 16-deep k step
   static constexpr int kChunks = BN / 64;                     // 64-column chunks of the B tile
-  static constexpr int kStageBytes = kBlkBytes + kChunks * kChunkBytes;
+  static constexpr int kSubBytes = kBlkBytes + kChunks * kChunkBytes;   // one block and its B tile
+  static constexpr int kStageBytes = KB * kSubBytes;
   static constexpr int kAccCols = kWS ? BN / 2 : BN;          // TMEM columns of one accumulator
   static constexpr int kTmemCols = NBUF * kAccCols;
   static constexpr int kOutBytes = OUT_BF16 ? 2 : 4;
@@ -128,6 +131,7 @@ struct Cfg {
   // stage it owns; with PW <= Q the phase it waits for is never two phases
   // ahead of the barrier, so the parity test cannot pass early.
   static_assert(PW >= 1 && PW <= Q, "producer warps");
+  static_assert(KB == 1 || KB == 2, "blocks per stage");
   static_assert(BN % 128 == 0 && BN <= 256 && kNmma % 16 == 0 && kPartBoxes >= 1 && PARTS % 2 == 0 &&
                     kPartGroups % kBatch == 0, "tile shape");
 };
@@ -145,11 +149,11 @@ __device__ __forceinline__ void tile_coords(int64_t t, int n_block_rows, int n_c
   nt = static_cast<int>(g) * kGroupN + static_cast<int>(r % gsz);
 }
 
-template <int BN, int Q, int NBUF, int PARTS, int MINB, int PW, bool IN_BF16, bool OUT_BF16>
-__global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, OUT_BF16>::kThreads, MINB)
+template <int BN, int Q, int NBUF, int PARTS, int MINB, int PW, int KB, bool IN_BF16, bool OUT_BF16>
+__global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, KB, OUT_BF16>::kThreads, MINB)
     bcsr_spmm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const BcsrParams p) {
-  using C_ = Cfg<BN, Q, NBUF, PARTS, MINB, PW, OUT_BF16>;
+  using C_ = Cfg<BN, Q, NBUF, PARTS, MINB, PW, KB, OUT_BF16>;
   constexpr int kMmaWarp = C_::kMmaWarp;
   constexpr int kEpiWarp0 = C_::kEpiWarp0;
   extern __shared__ uint8_t smem_raw[];
@@ -225,11 +229,12 @@ __global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, OUT_BF16>::k
       }
     };
     // One stage: its tile record (released to the MMA thread by the arrive)
-    // and, unless the block row is empty, the TMA loads of block j and of the
-    // 64 rows of B it multiplies (block column bcol) for column tile nt.
-    auto issue = [&](int br, int nt, int64_t j, int32_t bcol, int32_t flags) {
+    // and, unless the block row is empty, the TMA loads of blocks j .. j+nblk-1
+    // and of the 64 rows of B each multiplies (block columns bcol0, bcol1) for
+    // column tile nt.
+    auto issue = [&](int br, int nt, int64_t j, int32_t bcol0, int32_t bcol1, int nblk, int32_t flags) {
       if (lane == 0 && mine()) {
-        tile_rec[stage] = TileRec{br, nt, flags, 0};
+        tile_rec[stage] = TileRec{br, nt, flags, nblk};
         const uint32_t fb = full0 + 8 * stage;
         if (flags & kRecEmpty) {
           mbar_arrive(fb);
@@ -237,10 +242,13 @@ __global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, OUT_BF16>::k
           const int n0 = nt * C_::kBN;
           const int nch = min(C_::kChunks, (p.N - n0 + 63) / 64);
           const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
-          mbar_arrive_expect_tx(fb, kBlkBytes + nch * kChunkBytes);
-          tma_load_2d(st, &tmA, fb, 0, static_cast<int32_t>(j * kBlk));
-          for (int c = 0; c < nch; ++c)
-            tma_load_2d(st + kBlkBytes + c * kChunkBytes, &tmB, fb, n0 + c * 64, bcol * kBlk);
+          mbar_arrive_expect_tx(fb, nblk * (kBlkBytes + nch * kChunkBytes));
+          for (int b = 0; b < nblk; ++b) {
+            const uint32_t sb = st + b * C_::kSubBytes;
+            tma_load_2d(sb, &tmA, fb, 0, static_cast<int32_t>((j + b) * kBlk));
+            for (int c = 0; c < nch; ++c)
+              tma_load_2d(sb + kBlkBytes + c * kChunkBytes, &tmB, fb, n0 + c * 64, (b ? bcol1 : bcol0) * kBlk);
+          }
         }
       }
       advance();
@@ -304,7 +312,7 @@ __global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, OUT_BF16>::k
         const int32_t flags = (tfirst || f == f0 ? kRecFirst : 0) | (tlast || f == f1 - 1 ? kRecLast : 0) |
                               (tfirst ? kRecTileFirst : 0) | (tlast ? kRecTileLast : 0) | (f == f0 ? kRecAtF0 : 0) |
                               (empty ? kRecEmpty : 0);
-        issue(br, g * kGroupN + i, jb + j, bcol, flags);
+        issue(br, g * kGroupN + i, jb + j, bcol, 0, 1, flags);
         if (++j == len) {  // next tile
           j = 0;
           if (++i == gsz) {
@@ -344,20 +352,22 @@ __global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, OUT_BF16>::k
         if (jb == je) {
           ok = claim();
           if (!ok) break;
-          issue(br, nt, 0, 0, kRecFirst | kRecLast | kRecWhole | kRecEmpty);
+          issue(br, nt, 0, 0, 0, 1, kRecFirst | kRecLast | kRecWhole | kRecEmpty);
         }
         for (int64_t jbase = jb; jbase < je && ok; jbase += 32) {
           // The warp loads the next 32 block-column indices at once.
           const int64_t jl = jbase + lane;
           const int32_t my_col = jl < je ? p.block_col_idx[jl] : 0;
           const int cnt = (je - jbase) < 32 ? static_cast<int>(je - jbase) : 32;
-          for (int i = 0; i < cnt; ++i) {
-            const int32_t bcol = __shfl_sync(0xffffffffu, my_col, i);
+          for (int i = 0; i < cnt; i += KB) {  // KB divides 32: a stage never spans two loads
+            const int32_t bcol0 = __shfl_sync(0xffffffffu, my_col, i);
+            const int32_t bcol1 = __shfl_sync(0xffffffffu, my_col, (i + 1) & 31);
+            const int nb = min(KB, cnt - i);
             ok = claim();
             if (!ok) break;
             const int64_t j = jbase + i;
-            issue(br, nt, j, bcol,
-                  (j == jb ? kRecFirst | kRecTileFirst : 0) | (j == je - 1 ? kRecLast | kRecTileLast : 0));
+            issue(br, nt, j, bcol0, bcol1, nb,
+                  (j == jb ? kRecFirst | kRecTileFirst : 0) | (j + nb - 1 == je - 1 ? kRecLast | kRecTileLast : 0));
           }
         }
         br = br_n;
@@ -419,22 +429,28 @@ __global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, OUT_BF16>::k
         if (!(rec.flags & kRecEmpty)) {
           tc_fence_after_sync();
           const int nmma = min(C_::kMmas, (p.N - rec.nt * BN + C_::kNmma - 1) / C_::kNmma);
-          const uint32_t a_blk = smem_addr(smem + stage * C_::kStageBytes);  // block: MMA operand A (K-major)
-          const uint32_t b_til = a_blk + kBlkBytes;                          // B tile: MMA operand B (MN-major)
           const uint32_t acc = tmem + buf * C_::kAccCols;
           const bool first = (rec.flags & kRecFirst) != 0;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = smem_desc_sw128(a_blk + kk * 32, 16, 1024);
+          for (int b = 0; b < KB; ++b) {
+            if (b < rec.nblk) {
+              const uint32_t a_blk = smem_addr(smem + stage * C_::kStageBytes + b * C_::kSubBytes);  // block: A, K-major
+              const uint32_t b_til = a_blk + kBlkBytes;                                          // B tile: MN-major
 #pragma unroll
-            for (int m = 0; m < C_::kMmas; ++m) {
-              if (m < nmma) {
-                const uint64_t bdesc = smem_desc_sw128(b_til + m * (C_::kNmma / 64) * kChunkBytes + kk * 2048,
-                                                       kChunkBytes, 1024);
-                if constexpr (C_::kWS)
-                  umma_ws_f16(acc, adesc, bdesc, idesc, (first && kk == 0) ? 0u : 1u);
-                else
-                  umma_f16(acc + m * C_::kNmma, adesc, bdesc, idesc, (first && kk == 0) ? 0u : 1u);
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t adesc = smem_desc_sw128(a_blk + kk * 32, 16, 1024);
+                const uint32_t acc_in = (first && b == 0 && kk == 0) ? 0u : 1u;  // the tile's first step overwrites
+#pragma unroll
+                for (int m = 0; m < C_::kMmas; ++m) {
+                  if (m < nmma) {
+                    const uint64_t bdesc = smem_desc_sw128(b_til + m * (C_::kNmma / 64) * kChunkBytes + kk * 2048,
+                                                           kChunkBytes, 1024);
+                    if constexpr (C_::kWS)
+                      umma_ws_f16(acc, adesc, bdesc, idesc, acc_in);
+                    else
+                      umma_f16(acc + m * C_::kNmma, adesc, bdesc, idesc, acc_in);
+                  }
+                }
               }
             }
           }
@@ -629,11 +645,11 @@ __global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, OUT_BF16>::k
   }
 }
 
-template <int BN, int Q, int NBUF, int PARTS, int MINB, int PW, bool IN_BF16, bool OUT_BF16>
+template <int BN, int Q, int NBUF, int PARTS, int MINB, int PW, int KB, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_variant(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC,
                            const BcsrParams &p, cudaStream_t stream) {
-  using C_ = Cfg<BN, Q, NBUF, PARTS, MINB, PW, OUT_BF16>;
-  auto kern = bcsr_spmm_kernel<BN, Q, NBUF, PARTS, MINB, PW, IN_BF16, OUT_BF16>;
+  using C_ = Cfg<BN, Q, NBUF, PARTS, MINB, PW, KB, OUT_BF16>;
+  auto kern = bcsr_spmm_kernel<BN, Q, NBUF, PARTS, MINB, PW, KB, IN_BF16, OUT_BF16>;
   static std::atomic<uint64_t> smem_set{0};  // per instantiation, one bit per device
   cudaError_t e = set_smem_limit_once(kern, C_::kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
@@ -652,11 +668,11 @@ cudaError_t launch_variant(const CUtensorMap &tmA, const CUtensorMap &tmB, const
                                              static_cast<int32_t>(grid), BN, stream);
 }
 
-template <int BN, int Q, int NBUF, int PARTS, int MINB, int PW, bool OUT_BF16>
+template <int BN, int Q, int NBUF, int PARTS, int MINB, int PW, int KB, bool OUT_BF16>
 cudaError_t launch_in(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmC, const BcsrParams &p,
                       bool in_bf16, cudaStream_t s) {
-  return in_bf16 ? launch_variant<BN, Q, NBUF, PARTS, MINB, PW, true, OUT_BF16>(tmA, tmB, tmC, p, s)
-                 : launch_variant<BN, Q, NBUF, PARTS, MINB, PW, false, OUT_BF16>(tmA, tmB, tmC, p, s);
+  return in_bf16 ? launch_variant<BN, Q, NBUF, PARTS, MINB, PW, KB, true, OUT_BF16>(tmA, tmB, tmC, p, s)
+                 : launch_variant<BN, Q, NBUF, PARTS, MINB, PW, KB, false, OUT_BF16>(tmA, tmB, tmC, p, s);
 }
 
 }  // namespace
@@ -667,27 +683,30 @@ cudaError_t launch_bcsr(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
                         const BcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream) {
   if (p.n_block_rows == 0 || p.N == 0) return cudaSuccess;
   // N <= 128: 128-column tiles (one plain MMA of N = 128 per k step), two
-  // accumulators; one CTA per SM with six stages, or, on the split schedule,
-  // two CTAs per SM with three.  Wider (bcsr_wide_tiles): 256-column tiles,
-  // one weight-stationary MMA of N = 256 per k step, two accumulators of 128
-  // TMEM columns; with at least two tiles per SM (or on the split schedule)
-  // two CTAs share each SM (two stages each), so one CTA's barrier handshakes
-  // overlap the other's MMAs and loads; with fewer tiles one CTA per SM runs
-  // four stages.  Epilogue parts are one 32-row x 64-byte store box (32 bf16
-  // or 16 fp32 columns).
+  // accumulators; one CTA per SM with four stages of two blocks each (the
+  // MMA thread's fixed cost per stage, ~600 cycles besides the MMAs, bounds
+  // these shapes; two blocks per stage cut the 8192^2 sweeps by 20-24 %), or,
+  // on the split schedule, two CTAs per SM with three one-block stages.
+  // Wider (bcsr_wide_tiles): 256-column tiles, one weight-stationary MMA of
+  // N = 256 per k step, two accumulators of 128 TMEM columns; with at least
+  // two tiles per SM (or on the split schedule) two CTAs share each SM (two
+  // stages each), so one CTA's barrier handshakes overlap the other's MMAs
+  // and loads; with fewer tiles one CTA per SM runs four stages (two blocks
+  // per stage measured no faster there).  Epilogue parts are one 32-row x
+  // 64-byte store box (32 bf16 or 16 fp32 columns).
   if (!bcsr_wide_tiles(p.N)) {
     if (p.split_grid > 0)
-      return out_bf16 ? launch_in<128, 3, 2, 2, 2, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
-                      : launch_in<128, 3, 2, 2, 2, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
-    return out_bf16 ? launch_in<128, 6, 2, 2, 1, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
-                    : launch_in<128, 6, 2, 2, 1, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
+      return out_bf16 ? launch_in<128, 3, 2, 2, 2, 1, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                      : launch_in<128, 3, 2, 2, 2, 1, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
+    return out_bf16 ? launch_in<128, 4, 2, 2, 1, 1, 2, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                    : launch_in<128, 4, 2, 2, 1, 1, 2, false>(tmA, tmB, tmC, p, in_bf16, stream);
   }
   const int64_t tiles = static_cast<int64_t>(p.n_block_rows) * ((p.N + 255) / 256);
   if (tiles < 2ll * p.num_sms && p.split_grid == 0)
-    return out_bf16 ? launch_in<256, 4, 2, 4, 1, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
-                    : launch_in<256, 4, 2, 8, 1, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
-  return out_bf16 ? launch_in<256, 2, 2, 4, 2, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
-                  : launch_in<256, 2, 2, 8, 2, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
+    return out_bf16 ? launch_in<256, 4, 2, 4, 1, 1, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                    : launch_in<256, 4, 2, 8, 1, 1, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
+  return out_bf16 ? launch_in<256, 2, 2, 4, 2, 1, 1, true>(tmA, tmB, tmC, p, in_bf16, stream)
+                  : launch_in<256, 2, 2, 8, 2, 1, 1, false>(tmA, tmB, tmC, p, in_bf16, stream);
 }
 
 }  // namespace spmm
