@@ -460,6 +460,28 @@ def run_reference(args, rank, world):
 
 
 # ---------------------------------------------------------------- sweep
+SWEEP_SUFFIXES = ("_split", "_dyn", "_h64", "_rcm")  # removed from the end in this order
+
+
+def parse_config_entry(e):
+    """A --sweep entry -> (base configuration, variant flags, sweep point).
+    The variant suffixes (see SWEEP_SUFFIXES) may follow a name in the order
+    _rcm, _h64, _dyn, _split; the flags dict holds those present (without the
+    underscore).  A single sweep point such as bcsr_sweep_95_N256 or
+    wcsr_sweep_0.1_N8 gives point = (format, level, N), else point is None."""
+    flags = {}
+    base = e
+    for suf in SWEEP_SUFFIXES:
+        if base.endswith(suf):
+            base = base[:-len(suf)]
+            flags[suf[1:]] = True
+    parts = base.split("_")
+    point = None
+    if len(parts) == 4 and parts[0] in ("bcsr", "wcsr") and parts[1] == "sweep" and parts[3].startswith("N"):
+        point = (parts[0], float(parts[2]), int(parts[3][1:]))
+    return base, flags, point
+
+
 def run_sweep(args):
     """One JSON line per benchmark configuration on this GPU (ours only)."""
     import torch
@@ -517,21 +539,13 @@ def run_sweep(args):
     for e, n in sel.items():
         if e == "linear_weight":
             continue
-        base, h64, dyn, rcm, split = e, False, False, False, False
-        if base.endswith("_split"):
-            base, split = base[:-6], True
-        if base.endswith("_dyn"):
-            base, dyn = base[:-4], True
-        if base.endswith("_h64"):
-            base, h64 = base[:-4], True
-        if base.endswith("_rcm"):
-            base, rcm = base[:-4], True
-        parts = base.split("_")
+        base, flags, point = parse_config_entry(e)
+        h64, dyn, rcm, split = (flags.get(k, False) for k in ("h64", "dyn", "rcm", "split"))
         if base in named:
             fn = (lambda b=named[base], n=n: b(n))
-        elif len(parts) == 4 and parts[0] in ("bcsr", "wcsr") and parts[1] == "sweep" and parts[3].startswith("N"):
-            lvl, nn = float(parts[2]), int(parts[3][1:])
-            fn = (lambda lvl=lvl, nn=nn: [W.bcsr_sweep(int(lvl), nn)]) if parts[0] == "bcsr" else \
+        elif point is not None:
+            fmt, lvl, nn = point
+            fn = (lambda lvl=lvl, nn=nn: [W.bcsr_sweep(int(lvl), nn)]) if fmt == "bcsr" else \
                 (lambda lvl=lvl, nn=nn: [W.wcsr_sweep(lvl, nn)])
         else:
             raise SystemExit(f"unknown configuration {e!r}")

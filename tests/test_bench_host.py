@@ -76,3 +76,16 @@ def test_gather_model_counts_one_b_row_per_packed_column():
     assert bench.gather_model(_W, {"n_units": 1000}) == 2.0 * 1000 * 256
     _W.fmt = "bcsr"
     assert bench.gather_model(_W, {"n_units": 1000}) == 0.0
+
+
+@pytest.mark.parametrize("entry,base,flags,point", [
+    ("wcsr_uniform", "wcsr_uniform", {}, None),
+    ("wcsr_irregular_rcm_dyn", "wcsr_irregular", {"rcm": True, "dyn": True}, None),
+    ("wcsr_uniform_h64", "wcsr_uniform", {"h64": True}, None),
+    ("bcsr_sweep_95_N256_split", "bcsr_sweep_95_N256", {"split": True}, ("bcsr", 95.0, 256)),
+    ("wcsr_sweep_0.1_N8_h64", "wcsr_sweep_0.1_N8", {"h64": True}, ("wcsr", 0.1, 8)),
+    ("wcsr_sweep_2.0_N256_rcm", "wcsr_sweep_2.0_N256", {"rcm": True}, ("wcsr", 2.0, 256)),
+])
+def test_sweep_entry_parsing(entry, base, flags, point):
+    b, f, pt = bench.parse_config_entry(entry)
+    assert (b, f, pt) == (base, flags, point)
