@@ -47,11 +47,11 @@ L2_FLUSH_BYTES = 256 << 20
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
 # valid only for the kernel source it was taken on (sha256 of the file).
 MEASURED_TRAFFIC = {
-    # bcsr_weight: 114.5 MB read + 261.4 MB written at N = 8192; B and C scale
-    # with N, A (13.6 MB) does not: 13.6 MB + 8 x 362.3 MB at N = 65536
-    "bcsr_kernel.cu": {"src_sha": "6ca8a92fad3c6c13", "bytes_per_launch": 2.912e9},
-    # wcsr_uniform at its benchmark size: 100.2 MB read + 15.9 MB written
-    "wcsr_kernel.cu": {"src_sha": "218398c36b4bebd7", "bytes_per_launch": 1.162e8},
+    # bcsr_weight: 114.8 MB read + 261.4 MB written at N = 8192; B and C scale
+    # with N, A (13.6 MB) does not: 13.6 MB + 8 x 362.5 MB at N = 65536
+    "bcsr_kernel.cu": {"src_sha": "19cde5845824cb2f", "bytes_per_launch": 2.914e9},
+    # wcsr_uniform at its benchmark size: 100.3 MB read + 16.4 MB written
+    "wcsr_kernel.cu": {"src_sha": "0733d8a78e7dd0d8", "bytes_per_launch": 1.167e8},
 }
 
 
