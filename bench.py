@@ -190,6 +190,26 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- multi-rank host logic
+def host_link_rates(stream, dev, nbytes=1 << 30):
+    """The host link's own copy rates, the ceiling of the end-to-end figure:
+    one 1 GiB copy each way between pinned host memory and the device on the
+    benchmark's stream, after one untimed copy, timed with CUDA events."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=f"cuda:{dev}")
+    out = {}
+    for name, dst, src in (("h2d_gbs", d, h), ("d2h_gbs", h, d)):
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+        stream.synchronize()
+        out[name] = round(nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+    return out
+
+
 def max_over_ranks(x: float, world: int) -> float:
     """The largest of the ranks' values of x (all-reduce MAX over the default
     process group; a GPU tensor under NCCL, a host tensor under gloo)."""
@@ -348,7 +368,7 @@ def run_ours(args, rank, world):
         e2e = {"value": round(whole_job_tflops(eff_per_step, e2e_steps, world, t_e2e * 1e3), 4), "unit": UNIT,
                "h2d_bytes_per_step": int(sum(hb.numel() * 2 for hb, _ in hosts)),
                "d2h_bytes_per_step": int(sum(hc.numel() * hc.element_size() for _, hc in hosts)),
-               "steps": e2e_steps}
+               "steps": e2e_steps, "host_link": host_link_rates(stream, dev)}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
