@@ -214,9 +214,11 @@ spmm_status spmm_check(spmm_handle h, void *stream);
 
 /*
  * spmm_set_max_ctas -- cap the number of persistent CTAs a run launches
- * (ctas = 0, the default: two CTAs per SM for WCSR; for BCSR one per SM,
- * or two per SM when N > 128 and there are at least two 256-column tiles per
- * SM; WCSR caps ctas at two per SM).  Both kernels give each CTA an equal
+ * (ctas = 0, the default: two CTAs per SM for WCSR with 16-row windows, one
+ * with 64-row windows; for BCSR one per SM, or two per SM when N > 128 and
+ * there are at least two 256-column tiles per SM; WCSR caps ctas at two per
+ * SM).  Under the WCSR dynamic schedule the cap sets the CTAs that fit, and
+ * the grid holds about four chunks per such CTA.  Both kernels give each CTA an equal
  * share of the work (BCSR: whole block-row x column tiles; WCSR: equal
  * numbers of 64-column stages), so the cap changes where WCSR windows are cut
  * between CTAs (their partial sums are added by a second kernel in a fixed

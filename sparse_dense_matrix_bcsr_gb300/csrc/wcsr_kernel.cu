@@ -907,11 +907,8 @@ cudaError_t launch_wcsr_noalloc(WcsrParams p, const int64_t *window_row_ptr, int
                   : launch_noalloc_variant<2, 5, false, false>(p, stream);
 }
 
-// Two CTAs per SM, each with two producer warps: one CTA's barrier
-// handshakes and MMA issue stalls overlap the other's work.  Records are
-// fetched one item of the warp ahead, which leaves room for three stages per
-// CTA at N > 128 (15 % faster on a 1 %-dense 16384^2 matrix than two stages
-// with a lead of two).
+// Two CTAs per SM at every N (see launch_wcsr for their shapes): one CTA's
+// barrier handshakes and MMA issue stalls overlap the other's work.
 int wcsr_ctas_per_sm(int64_t N) {
   (void)N;
   return 2;
