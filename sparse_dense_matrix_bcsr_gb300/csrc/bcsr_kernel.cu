@@ -431,20 +431,23 @@ __global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, KB, OUT_BF16
           const int nmma = min(C_::kMmas, (p.N - rec.nt * BN + C_::kNmma - 1) / C_::kNmma);
           const uint32_t acc = tmem + buf * C_::kAccCols;
           const bool first = (rec.flags & kRecFirst) != 0;
+          // Descriptors of the stage's first block; every other operand is a
+          // fixed byte offset from them (smem_desc_add).
+          const uint32_t st0 = smem_addr(smem + stage * C_::kStageBytes);
+          const uint64_t adesc0 = smem_desc_sw128(st0, 16, 1024);                    // block: A, K-major
+          const uint64_t bdesc0 = smem_desc_sw128(st0 + kBlkBytes, kChunkBytes, 1024);  // B tile: MN-major
 #pragma unroll
           for (int b = 0; b < KB; ++b) {
             if (b < rec.nblk) {
-              const uint32_t a_blk = smem_addr(smem + stage * C_::kStageBytes + b * C_::kSubBytes);  // block: A, K-major
-              const uint32_t b_til = a_blk + kBlkBytes;                                          // B tile: MN-major
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t adesc = smem_desc_sw128(a_blk + kk * 32, 16, 1024);
+                const uint64_t adesc = smem_desc_add(adesc0, b * C_::kSubBytes + kk * 32);
                 const uint32_t acc_in = (first && b == 0 && kk == 0) ? 0u : 1u;  // the tile's first step overwrites
 #pragma unroll
                 for (int m = 0; m < C_::kMmas; ++m) {
                   if (m < nmma) {
-                    const uint64_t bdesc = smem_desc_sw128(b_til + m * (C_::kNmma / 64) * kChunkBytes + kk * 2048,
-                                                           kChunkBytes, 1024);
+                    const uint64_t bdesc = smem_desc_add(
+                        bdesc0, b * C_::kSubBytes + m * (C_::kNmma / 64) * kChunkBytes + kk * 2048);
                     if constexpr (C_::kWS)
                       umma_ws_f16(acc, adesc, bdesc, idesc, acc_in);
                     else

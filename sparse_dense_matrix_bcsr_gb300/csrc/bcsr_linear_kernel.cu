@@ -218,14 +218,15 @@ __global__ void __launch_bounds__(kThreads, 2)
           const uint32_t acc = tmem + buf * kAccCols;
           const bool first = (rec.flags & kRecFirst) != 0;
           // half h: rows 128h .. 128h + 127 of the tile
+          const uint64_t bdesc0 = smem_desc_sw128(blk, 16, 1024);
+          const uint64_t adesc0 = smem_desc_sw128(xt, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(blk + kk * 32, 16, 1024);
+            const uint64_t bdesc = smem_desc_add(bdesc0, kk * 32);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint64_t adesc = smem_desc_sw128(xt + h * (kXBytes / 2) + kk * 32, 16, 1024);
-              umma_f16(acc + h * kBlk, adesc, bdesc, idesc, (first && kk == 0) ? 0u : 1u);
-            }
+            for (int h = 0; h < 2; ++h)
+              umma_f16(acc + h * kBlk, smem_desc_add(adesc0, h * (kXBytes / 2) + kk * 32), bdesc, idesc,
+                       (first && kk == 0) ? 0u : 1u);
           }
         }
         umma_commit(empty0 + 8 * stage);

@@ -290,6 +290,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The descriptor of the same layout `bytes` further on in shared memory
+// (bytes a multiple of 16): the start-address field (address / 16, bits
+// 0..13) grows by bytes / 16.  Shared-memory addresses stay below 256 KB, so
+// the field cannot carry into the next one.
+__device__ __forceinline__ uint64_t smem_desc_add(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
+}
+
 // Instruction descriptor for tcgen05.mma kind::f16 with fp32 accumulation.
 //   ab_bf16: inputs are bf16 (else fp16); a_mn_major / b_mn_major: operand
 //   major-ness (0 = K-major); m, n: MMA shape.

@@ -328,10 +328,13 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
         const uint32_t vals = smem_addr(smem + stage * kStageBytes);  // M operand (K-major)
         const uint32_t gath = vals + kValBytes;                       // N operand (MN-major)
         const uint32_t acc = tmem + buf * kAccCols;
-        for (int kk = 0; kk < ksteps; ++kk)
-          umma_ws_f16(acc, smem_desc_sw128(vals + kk * 32, 16, 1024),
-                      smem_desc_sw128(gath + kk * 2048, kChunkBytes, 1024), idesc,
-                      (ksteps_done + kk) > 0 ? 1u : 0u);
+        const uint64_t vdesc0 = smem_desc_sw128(vals, 16, 1024);
+        const uint64_t gdesc0 = smem_desc_sw128(gath, kChunkBytes, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kKC / 16; ++kk)
+          if (kk < ksteps)
+            umma_ws_f16(acc, smem_desc_add(vdesc0, kk * 32), smem_desc_add(gdesc0, kk * 2048), idesc,
+                        (ksteps_done + kk) > 0 ? 1u : 0u);
         umma_commit(empty0 + 8 * stage);
       }
       ksteps_done += ksteps;

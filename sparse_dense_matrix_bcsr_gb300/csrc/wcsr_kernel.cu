@@ -605,13 +605,19 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
           const uint32_t vals = gath + C_::kGatherBytes;                     // MMA operand B (K-major)
           const int nacc = min(NACC, (p.N - rec.tile * C_::kBN + 127) / 128);
           const uint32_t acc = tmem + buf * C_::kAccCols;
-          for (int kk = 0; kk < ksteps; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(vals + kk * 32, 16, 1024);
+          // Descriptors of k step 0; a step adds a fixed byte offset to the
+          // start-address field (smem_desc_add), which stays in range.
+          const uint64_t bdesc0 = smem_desc_sw128(vals, 16, 1024);
+          const uint64_t adesc0 = smem_desc_sw128(gath, kChunkBytes, 1024);
 #pragma unroll
-            for (int a = 0; a < NACC; ++a) {
-              if (a < nacc) {
-                const uint64_t adesc = smem_desc_sw128(gath + a * 2 * kChunkBytes + kk * 2048, kChunkBytes, 1024);
-                umma_f16(acc + a * kH, adesc, bdesc, idesc, (ksteps_done + kk) > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kKC / 16; ++kk) {
+            if (kk < ksteps) {
+              const uint64_t bdesc = smem_desc_add(bdesc0, kk * 32);
+#pragma unroll
+              for (int a = 0; a < NACC; ++a) {
+                if (a < nacc)
+                  umma_f16(acc + a * kH, smem_desc_add(adesc0, a * 2 * kChunkBytes + kk * 2048), bdesc, idesc,
+                           (ksteps_done + kk) > 0 ? 1u : 0u);
               }
             }
           }
