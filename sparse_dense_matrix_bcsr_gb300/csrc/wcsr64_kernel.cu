@@ -25,12 +25,13 @@
 // partial sums (64 x 256) for split_reduce_kernel.
 //
 // PW + 5 warps (see kLaunch* for the launch shape):
-//   warps 0..PW-1  producers: warp w owns the work items w, w + PW, ...; it
-//                  gathers an item's 64 rows of B with 16-byte cp.async (one
+//   warps 0..PW-1  producers in groups of WPG: group g owns the work items
+//                  g, g + PW/WPG, ...; each warp of the group gathers its
+//                  share of an item's 64 rows of B with 16-byte cp.async (one
 //                  512-byte row per instruction at full width, live columns
-//                  only when N is narrower), after fetching its index record
-//                  ahead into a per-warp ring and its value tile into the
-//                  stage (TMA bulk copies)
+//                  only when N is narrower), after fetching the index record
+//                  ahead into a per-warp ring; the group's first warp has the
+//                  value tile copied into the stage (TMA bulk copy)
 //   warp PW        TMEM allocator and MMA issuer
 //   warps PW+1..   epilogue (warp w reads TMEM sub-partition w % 4)
 #include <cuda_bf16.h>
@@ -54,19 +55,22 @@ constexpr int kChunkBytes = kKC * 128;                 // 64 gathered rows x 64 
 constexpr int kGatherBytes = 4 * kChunkBytes;          // 32 KB
 constexpr int kStageBytes = kValBytes + kGatherBytes;  // 40 KB
 constexpr int kEpiWarps = 4;
-constexpr int kIdxLead = 4;
 constexpr int kAccCols = kBN / 2;
 constexpr int kNbuf = 2;
 constexpr int kTmemCols = kNbuf * kAccCols;
 constexpr int kBoxBytes = 2048;                         // a store box: 32 rows x 64 bytes
 constexpr int kMiscBytes = 1024;
 
-// Q stages, PW producer warps (each gathers 64 / PW rows of every stage),
-// MINB CTAs per SM.
-template <int Q, int PW, int MINB, bool OUT_BF16>
+// Q stages, PW producer warps in groups of WPG (the warps of a group copy
+// disjoint row ranges of the same items: a warp's cp.async issue rate is
+// limited, so more copying warps gather faster), MINB CTAs per SM.  Each
+// producer warp fetches its items' index records kILead of its items ahead.
+template <int Q, int PW, int WPG, int MINB, bool OUT_BF16>
 struct Cfg {
   static constexpr int kQ = Q;
   static constexpr int kPW = PW;
+  static constexpr int kG = PW / WPG;                   // producer groups
+  static constexpr int kILead = WPG > 1 ? 2 : 4;
   static constexpr int kMmaWarp = PW;
   static constexpr int kEpiWarp0 = PW + 1;
   static constexpr int kThreads = 32 * (PW + 1 + kEpiWarps);
@@ -75,15 +79,16 @@ struct Cfg {
   static constexpr int kParts = OUT_BF16 ? 4 : 8;       // the warp's 128 columns in parts of one box
   static constexpr int kPartCols = 128 / kParts;
   static constexpr int kStaging = kEpiWarps * 2 * kBoxBytes;
-  static constexpr int kIdxRingBytes = (PW * kIdxLead * kMetaBytes + 1023) / 1024 * 1024;
+  static constexpr int kIdxRingBytes = (PW * kILead * kMetaBytes + 1023) / 1024 * 1024;
   static constexpr int kSmemBytes = Q * kStageBytes + kStaging + kIdxRingBytes + kMiscBytes + 1024;
   static_assert(kPartCols == kBoxCols, "one store box per part");
   static_assert(kSmemBytes <= 227 * 1024 && MINB * (kSmemBytes + 1024) <= 228 * 1024, "shared memory");
   static_assert(MINB * kTmemCols <= 512, "TMEM");
   // a warp waits for its item's stage with a parity wait on the MMA commit of
   // item it - Q; unambiguous only if the commit of it - 2Q was already seen,
-  // which the warp's previous wait (item it - PW) guarantees when PW <= Q
-  static_assert(PW <= Q, "more producer warps than stages");
+  // which the warp's previous wait (item it - kG) guarantees when kG <= Q
+  static_assert(PW % WPG == 0 && (WPG == 1 || WPG == 2), "producer groups");
+  static_assert(kG <= Q, "more producer groups than stages");
 };
 
 struct StageRec {  // producer -> MMA
@@ -101,10 +106,11 @@ struct SegRec {    // MMA -> epilogue
   int32_t pad_[3];
 };
 
-template <int Q, int PW, int MINB, bool IN_BF16, bool OUT_BF16>
+template <int Q, int PW, int WPG, int MINB, bool IN_BF16, bool OUT_BF16>
 __global__ void __launch_bounds__(32 * (PW + 5), MINB)
     wcsr64_spmm_kernel(const __grid_constant__ CUtensorMap tmC, const WcsrParams p) {
-  using E = Cfg<Q, PW, MINB, OUT_BF16>;
+  using E = Cfg<Q, PW, WPG, MINB, OUT_BF16>;
+  constexpr int kIdxLead = E::kILead;
   constexpr int kQ = E::kQ;
   constexpr int kPW = E::kPW;
   constexpr int kMmaWarp = E::kMmaWarp;
@@ -139,9 +145,9 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < kQ; ++q) {
-      // the owning warp's 32 cp.async lane arrivals + its lane 0's arrive
-      // (stage record, value tile bytes)
-      mbar_init(full0 + 8 * q, 33);
+      // 32 cp.async lane arrivals of each warp of the owning group + the
+      // group's first warp's lane 0 arrive (stage record, value tile bytes)
+      mbar_init(full0 + 8 * q, 1 + 32 * WPG);
       mbar_init(empty0 + 8 * q, 1);
     }
     for (int b = 0; b < kNbuf; ++b) {
@@ -167,7 +173,9 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
 
   if (warp < kPW) {
     // ------------------------------------------------------------ producers
-    // Warp w owns the work items w, w + PW, ... of the CTA's share.  It
+    // Group g (warps g*WPG .. g*WPG+WPG-1) owns the work items g, g + kG, ...
+    // of the CTA's share; each of its warps copies rows [rbeg, rend) of them.
+    // Each warp
     // fetches the index record of its item j (272 bytes) kIdxLead of its items
     // ahead into slot j % kIdxLead of its ring, reads the item's indices from
     // there, waits for the item's stage to be free, has the value tile copied
@@ -177,17 +185,20 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
     // are the producer warps' items: PW <= Q keeps them all busy and the
     // parity waits unambiguous.
     const uint16_t *Bp = reinterpret_cast<const uint16_t *>(p.B);
+    constexpr int kG = E::kG;
+    const int grp = warp / WPG, sub = warp % WPG;
+    const int rbeg = sub * (64 / WPG), rend = rbeg + 64 / WPG;
     const uint8_t *pack = reinterpret_cast<const uint8_t *>(p.stage_pack);
     uint8_t *ring = iring + warp * kIdxLead * kMetaBytes;
     const uint32_t ifull_w = ifull0 + 8 * (warp * kIdxLead);
     auto fetch_idx = [&](int64_t j) {
-      const int64_t fj = f0 + warp + j * kPW;
+      const int64_t fj = f0 + grp + j * kG;
       if (fj < f1 && lane == 0) {
         const uint32_t slot = static_cast<uint32_t>(j % kIdxLead);
         const uint8_t *src = pack + (fj % n_stages) * kPackBytes;
         mbar_arrive_expect_tx(ifull_w + 8 * slot, kMetaBytes);
         tma_bulk_load(smem_addr(ring + slot * kMetaBytes), src + kIdxOff, kMetaBytes, ifull_w + 8 * slot);
-        prefetch_l2_bulk(src, kValBytes);
+        if (sub == 0) prefetch_l2_bulk(src, kValBytes);
       }
     };
     // The item's 64 rows of B -> the stage's gather area: one B row per
@@ -196,12 +207,13 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
     // zero-filled.  lo / hi hold the indices of rows lane and 32 + lane.
     auto gather = [&](uint32_t st, int n0, int ncols, int32_t lo, int32_t hi) {
       const int live_units = (min(kBN, p.N - n0) + 7) >> 3;  // 1 .. 32
+      const int rlim = min(ncols, rend);
       const uint32_t dst = st + kValBytes;
       if (live_units == 32) {
         const int n = n0 + lane * 8;
         const uint32_t dst_col = (lane >> 3) * kChunkBytes;
         const uint32_t uu = static_cast<uint32_t>(lane & 7);
-        for (int r0 = 0; r0 < ncols; r0 += 16) {
+        for (int r0 = rbeg; r0 < rlim; r0 += 16) {
           const int32_t src = r0 < 32 ? lo : hi;
           int32_t col[16];
 #pragma unroll
@@ -220,14 +232,15 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
       }
       const int sh = 32 - __clz(live_units - 1);
       const int rsh = 5 - sh;
-      const int ninst = (ncols + (1 << rsh) - 1) >> rsh;
+      const int i_beg = rbeg >> rsh;  // instructions holding rows [rbeg, rlim)
+      const int i_end = (rlim + (1 << rsh) - 1) >> rsh;
       const int r_lane = lane >> sh;
       const int u = lane & ((1 << sh) - 1);
       const int n = n0 + u * 8;
       const bool u_live = n < p.N;
       const uint32_t dst_u = (u >> 3) * kChunkBytes;
       const uint32_t uu = static_cast<uint32_t>(u & 7);
-      for (int i0 = 0; i0 < ninst; i0 += 16) {
+      for (int i0 = i_beg; i0 < i_end; i0 += 16) {
         int32_t col[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -237,7 +250,7 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int r = ((i0 + j) << rsh) + r_lane;
-          if (i0 + j < ninst && u_live && r < ncols) {
+          if (i0 + j < i_end && u_live && r >= rbeg && r < rlim) {
             const bool live = col[j] >= 0;
             cp_async_16(dst + dst_u + r * 128 + ((uu ^ static_cast<uint32_t>(r & 7)) << 4),
                         live ? static_cast<const void *>(Bp + static_cast<int64_t>(col[j]) * p.N + n)
@@ -252,7 +265,7 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
     bool ok = true;
     int64_t consumed = 0;  // own items whose indices were read; fetches of the next kIdxLead are in flight
     for (int64_t j = 0;; ++j) {
-      const int64_t f = f0 + warp + j * kPW;
+      const int64_t f = f0 + grp + j * kG;
       if (f >= f1) break;
       const uint32_t islot = static_cast<uint32_t>(j % kIdxLead);
       ok = mbar_wait_warp(ifull_w + 8 * islot, static_cast<uint32_t>((j / kIdxLead) & 1), p.wait_limit_ns);
@@ -275,7 +288,7 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
       const int tile = static_cast<int>(f / n_stages);
       const uint32_t st = smem_addr(smem + stage * kStageBytes);
       const uint32_t fb = full0 + 8 * stage;
-      if (lane == 0) {
+      if (lane == 0 && sub == 0) {
         stage_rec[stage] = StageRec{d.x, d.y, d.z, tile};  // released by this arrive
         mbar_arrive_expect_tx(fb, kValBytes);
         tma_bulk_load(st, pack + (f % n_stages) * kPackBytes, kValBytes, fb);
@@ -287,7 +300,7 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
     if (!ok && lane == 0) {
       atomicOr(p.status, kDevTimeout);
       *abort_flag = 1;
-      for (int64_t i = consumed; i < consumed + kIdxLead && f0 + warp + i * kPW < f1; ++i)
+      for (int64_t i = consumed; i < consumed + kIdxLead && f0 + grp + i * kG < f1; ++i)
         mbar_wait(ifull_w + 8 * (i % kIdxLead), static_cast<uint32_t>((i / kIdxLead) & 1), 1000000ull);
     }
   } else if (warp == kMmaWarp) {
@@ -497,10 +510,10 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
   }
 }
 
-template <int Q, int PW, int MINB, bool IN_BF16, bool OUT_BF16>
+template <int Q, int PW, int WPG, int MINB, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_variant(const CUtensorMap &tmC, const WcsrParams &p, cudaStream_t stream) {
-  using E = Cfg<Q, PW, MINB, OUT_BF16>;
-  auto kern = wcsr64_spmm_kernel<Q, PW, MINB, IN_BF16, OUT_BF16>;
+  using E = Cfg<Q, PW, WPG, MINB, OUT_BF16>;
+  auto kern = wcsr64_spmm_kernel<Q, PW, WPG, MINB, IN_BF16, OUT_BF16>;
   static std::atomic<uint64_t> smem_set{0};
   cudaError_t e = set_smem_limit_once(kern, E::kSmemBytes, smem_set);
   if (e != cudaSuccess) return e;
@@ -513,20 +526,21 @@ cudaError_t launch_variant(const CUtensorMap &tmC, const WcsrParams &p, cudaStre
 
 }  // namespace
 
-// Launch shape: kLaunchQ stages, kLaunchPW producer warps, kLaunchMinB CTAs per SM.
-constexpr int kLaunchQ = 5, kLaunchPW = 5, kLaunchMinB = 1;
+// Launch shape: kLaunchQ stages, kLaunchPW producer warps in groups of
+// kLaunchWPG, kLaunchMinB CTAs per SM.
+constexpr int kLaunchQ = 5, kLaunchPW = 10, kLaunchWPG = 2, kLaunchMinB = 1;
 
 int wcsr64_ctas_per_sm() { return kLaunchMinB; }
 
 cudaError_t launch_wcsr64(const CUtensorMap &tmC, const WcsrParams &p, bool in_bf16, bool out_bf16,
                           cudaStream_t stream) {
   if (p.n_stages == 0 || p.N == 0 || p.grid == 0) return cudaSuccess;
-  constexpr int Q = kLaunchQ, PW = kLaunchPW, MB = kLaunchMinB;
+  constexpr int Q = kLaunchQ, PW = kLaunchPW, G = kLaunchWPG, MB = kLaunchMinB;
   if (in_bf16)
-    return out_bf16 ? launch_variant<Q, PW, MB, true, true>(tmC, p, stream)
-                    : launch_variant<Q, PW, MB, true, false>(tmC, p, stream);
-  return out_bf16 ? launch_variant<Q, PW, MB, false, true>(tmC, p, stream)
-                  : launch_variant<Q, PW, MB, false, false>(tmC, p, stream);
+    return out_bf16 ? launch_variant<Q, PW, G, MB, true, true>(tmC, p, stream)
+                    : launch_variant<Q, PW, G, MB, true, false>(tmC, p, stream);
+  return out_bf16 ? launch_variant<Q, PW, G, MB, false, true>(tmC, p, stream)
+                  : launch_variant<Q, PW, G, MB, false, false>(tmC, p, stream);
 }
 
 }  // namespace spmm
