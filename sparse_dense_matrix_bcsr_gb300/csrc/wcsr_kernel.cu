@@ -928,14 +928,14 @@ int wcsr_tile_cols(int64_t N) { return (N <= 128 || !kWideTiles) ? 128 : 256; }
 
 // Launch shapes, two CTAs per SM (one CTA per SM with more stages and
 // producers measured 35-70 % slower: the single MMA-issuing thread of a CTA
-// becomes the limit).  128-column items: five 18 KB stages, four producer
-// warps each copying whole items.  256-column items: three 34 KB stages,
-// three producer groups of two warps (each warp copies 32 of an item's 64
-// rows): 12 copying warps per SM instead of 6, 7 % faster on the uniform
-// matrix; at 128 columns the same split was 12 % slower.
+// becomes the limit).  128-column items: five 18 KB stages, five producer
+// warps each copying whole items (7-10 % faster than four; eight warps in
+// groups of two were slower).  256-column items: three 34 KB stages, three
+// producer groups of two warps (each warp copies 32 of an item's 64 rows):
+// 12 copying warps per SM instead of 6, 7 % faster on the uniform matrix.
 cudaError_t launch_wcsr(const WcsrParams &p, bool in_bf16, bool out_bf16, cudaStream_t stream) {
   if (p.n_stages == 0 || p.N == 0 || p.grid == 0) return cudaSuccess;
-  if (wcsr_tile_cols(p.N) == 128) return launch_dtypes<1, 5, 4, 1, 2>(p, in_bf16, out_bf16, stream);
+  if (wcsr_tile_cols(p.N) == 128) return launch_dtypes<1, 5, 5, 1, 2>(p, in_bf16, out_bf16, stream);
   return launch_dtypes<2, 3, 6, 2, 2>(p, in_bf16, out_bf16, stream);
 }
 
