@@ -124,6 +124,31 @@ constexpr int wcsr_pack_desc_off(int h) { return h * 64 * 2 + 256; }
 constexpr int wcsr_pack_bytes(int h) { return h * 64 * 2 + 256 + 16; }
 static_assert(wcsr_pack_bytes(16) == kWcsrPackBytes && wcsr_pack_bytes(64) % 16 == 0, "record layout");
 
+#ifdef __CUDACC__
+// Work item f of a WCSR grid is (column tile f / n_stages, stage record
+// f % n_stages).  A producer walks its items in small increasing steps, so
+// the cursor follows them with additions and divides only when f jumps (a
+// 64-bit division is a long instruction sequence on the GPU).
+struct ItemCursor {
+  int64_t f = -1;  // current item
+  int64_t s = 0;   // its stage record
+  int tile = 0;    // its column tile
+  __device__ __forceinline__ void to(int64_t nf, int64_t n_stages) {
+    if (f < 0 || nf < f || nf - f > n_stages) {
+      tile = static_cast<int>(nf / n_stages);
+      s = nf - static_cast<int64_t>(tile) * n_stages;
+    } else {
+      s += nf - f;
+      while (s >= n_stages) {
+        s -= n_stages;
+        ++tile;
+      }
+    }
+    f = nf;
+  }
+};
+#endif
+
 struct WcsrParams {
   const WcsrStage *stages;       // device, n_stages (the no-allocation variant's stage list)
   const void *stage_pack;        // device, n_stages x kWcsrPackBytes (the allocating entry points)

@@ -191,11 +191,13 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
     const uint8_t *pack = reinterpret_cast<const uint8_t *>(p.stage_pack);
     uint8_t *ring = iring + warp * kIdxLead * kMetaBytes;
     const uint32_t ifull_w = ifull0 + 8 * (warp * kIdxLead);
+    ItemCursor fcur, icur;  // the items fetched and the items copied
     auto fetch_idx = [&](int64_t j) {
       const int64_t fj = f0 + grp + j * kG;
+      if (fj < f1) fcur.to(fj, n_stages);
       if (fj < f1 && lane == 0) {
         const uint32_t slot = static_cast<uint32_t>(j % kIdxLead);
-        const uint8_t *src = pack + (fj % n_stages) * kPackBytes;
+        const uint8_t *src = pack + fcur.s * kPackBytes;
         mbar_arrive_expect_tx(ifull_w + 8 * slot, kMetaBytes);
         tma_bulk_load(smem_addr(ring + slot * kMetaBytes), src + kIdxOff, kMetaBytes, ifull_w + 8 * slot);
         if (sub == 0) prefetch_l2_bulk(src, kValBytes);
@@ -279,19 +281,20 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
       __syncwarp();
       fetch_idx(j + kIdxLead);
       consumed = j + 1;
+      icur.to(f, n_stages);
+      const int tile = icur.tile;
       const int64_t it = f - f0;
       const uint32_t stage = static_cast<uint32_t>(it % kQ);
       const uint32_t phase = static_cast<uint32_t>((it / kQ) & 1);
       ok = mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns);
       ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
       if (!ok) break;
-      const int tile = static_cast<int>(f / n_stages);
       const uint32_t st = smem_addr(smem + stage * kStageBytes);
       const uint32_t fb = full0 + 8 * stage;
       if (lane == 0 && sub == 0) {
         stage_rec[stage] = StageRec{d.x, d.y, d.z, tile};  // released by this arrive
         mbar_arrive_expect_tx(fb, kValBytes);
-        tma_bulk_load(st, pack + (f % n_stages) * kPackBytes, kValBytes, fb);
+        tma_bulk_load(st, pack + icur.s * kPackBytes, kValBytes, fb);
       }
       gather(st, tile * kBN, d.x, lo, hi);
       cp_async_arrive_noinc(fb);

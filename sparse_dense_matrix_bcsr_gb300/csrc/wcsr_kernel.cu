@@ -146,7 +146,8 @@ struct SegRec {     // MMA -> epilogue, one per accumulator buffer
 // read from device memory (the stage list is built on the device), CTAs
 // beyond the number of work items leave at once, and column indices are read
 // from window_col_idx at each stage's first packed column.
-template <int NACC, int Q, int PW, int WPG, int MINB, bool IN_BF16, bool OUT_BF16, bool NOALLOC = false>
+template <int NACC, int Q, int PW, int WPG, int MINB, bool IN_BF16, bool OUT_BF16, bool NOALLOC = false,
+          bool DYN = false>
 __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
     wcsr_spmm_kernel(const WcsrParams p) {
   constexpr int kILead = NOALLOC ? 0 : kIdxLead;
@@ -424,7 +425,9 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         int64_t lbase, len, g0;  // first CTA-local item, items, first work item
         int32_t id;
       };
-      Chunk kn[4] = {};
+      // the last four chunks learned (the static schedule has one)
+      constexpr int kKn = DYN ? 4 : 1;
+      Chunk kn[kKn] = {};
       int nk = 0;               // chunks learned
       bool no_more = false;     // the chunk after the last learned one does not exist
       int64_t l_end = 0;        // CTA-local items in all (once no_more)
@@ -435,7 +438,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         int32_t id = -1;
         if (nk == 0) {
           id = static_cast<int32_t>(blockIdx.x);
-        } else if (p.dynamic) {
+        } else if (DYN) {
           const uint32_t sl = static_cast<uint32_t>((nk - 1) % kRespSlots);
           bool r = mbar_wait_warp(respb0 + 8 * sl, static_cast<uint32_t>(((nk - 1) / kRespSlots) & 1),
                                   p.wait_limit_ns);
@@ -446,7 +449,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
           ++n_read;
           id = got ? static_cast<int32_t>(x) : -1;
         }
-        const int64_t lb = nk ? kn[(nk - 1) & 3].lbase + kn[(nk - 1) & 3].len : 0;
+        const int64_t lb = nk ? kn[(nk - 1) & (kKn - 1)].lbase + kn[(nk - 1) & (kKn - 1)].len : 0;
         if (id < 0) {
           no_more = true;
           l_end = lb;
@@ -457,8 +460,8 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         c.g0 = total * id / n_chunks;
         c.len = total * (id + 1) / n_chunks - c.g0;
         c.lbase = lb;
-        kn[nk & 3] = c;
-        if (p.dynamic && warp == 0) {
+        kn[nk & (kKn - 1)] = c;
+        if (DYN && warp == 0) {
           if (lane == 0) {
             const uint32_t sl = static_cast<uint32_t>(nk % kRespSlots);
             mbar_arrive_expect_tx(respb0 + 8 * sl, 16);
@@ -473,22 +476,23 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
       // needed): its ordinal, -1 past the last item, -2 when a wait ran out.
       auto locate = [&](int64_t it) -> int {
         while (true) {
-          for (int q = nk > 4 ? nk - 4 : 0; q < nk; ++q)
-            if (it >= kn[q & 3].lbase && it < kn[q & 3].lbase + kn[q & 3].len) return q;
+          for (int q = nk > kKn ? nk - kKn : 0; q < nk; ++q)
+            if (it >= kn[q & (kKn - 1)].lbase && it < kn[q & (kKn - 1)].lbase + kn[q & (kKn - 1)].len) return q;
           if (no_more) return -1;
           if (!learn_next()) return -2;
         }
       };
       int64_t n_fetched = 0;  // own items whose index records were requested (a prefix)
+      ItemCursor fcur, icur;  // the items fetched and the items copied
       auto fetch_idx = [&](int64_t j) -> bool {
         const int q = locate(grp + G * j);
         if (q == -2) return false;
         if (q >= 0) {
-          const Chunk &c = kn[q & 3];
-          const int64_t fj = c.g0 + (grp + G * j - c.lbase);
+          const Chunk &c = kn[q & (kKn - 1)];
+          fcur.to(c.g0 + (grp + G * j - c.lbase), n_stages);
           if (lane == 0) {
             const uint32_t slot = static_cast<uint32_t>(j % kILead);
-            const uint8_t *src = pack + (fj % n_stages) * kWcsrPackBytes;
+            const uint8_t *src = pack + fcur.s * kWcsrPackBytes;
             mbar_arrive_expect_tx(ifull_w + 8 * slot, kMetaBytes);
             tma_bulk_load(smem_addr(ring + slot * kMetaBytes), src + kWcsrPackIdxOff, kMetaBytes,
                           ifull_w + 8 * slot);
@@ -506,7 +510,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         const int q = locate(it);
         if (q == -2) ok = false;
         if (q < 0) break;
-        const Chunk c = kn[q & 3];
+        const Chunk c = kn[q & (kKn - 1)];
         const int64_t f = c.g0 + (it - c.lbase);
         const uint32_t islot = static_cast<uint32_t>(j % kILead);
         ok = mbar_wait_warp(ifull_w + 8 * islot, static_cast<uint32_t>((j / kILead) & 1), p.wait_limit_ns);
@@ -521,13 +525,14 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         consumed = j + 1;
         ok = fetch_idx(j + kILead);
         if (!ok) break;
+        icur.to(f, n_stages);
+        const int tile = icur.tile;
         const uint32_t stage = static_cast<uint32_t>(it % Q);
         const uint32_t phase = static_cast<uint32_t>((it / Q) & 1);
         // the stage is free once the MMAs of item it - Q are complete
         ok = mbar_wait_warp(empty0 + 8 * stage, phase ^ 1u, p.wait_limit_ns);
         ok = __shfl_sync(0xffffffffu, ok && !*abort_flag, 0);
         if (!ok) break;
-        const int tile = static_cast<int>(f / n_stages);
         const uint32_t st = smem_addr(smem + stage * C_::kStageBytes);
         const uint32_t fb = full0 + 8 * stage;
         if (lane == 0 && sub == 0) {
@@ -538,7 +543,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
           const int32_t fl = d.y | (it == c.lbase ? kRecChunkFirst : 0) | (it == c.lbase + c.len - 1 ? kRecChunkLast : 0);
           stage_rec[stage] = StageRec{d.x, fl, d.z, tile, c.id, {0, 0, 0}};  // released by this arrive
           mbar_arrive_expect_tx(fb, kValBytes);
-          tma_bulk_load(st + C_::kGatherBytes, pack + (f % n_stages) * kWcsrPackBytes + kWcsrPackValOff, kValBytes,
+          tma_bulk_load(st + C_::kGatherBytes, pack + icur.s * kWcsrPackBytes + kWcsrPackValOff, kValBytes,
                         fb);
         }
         gather(st, tile * C_::kBN, d.x, lo, hi);
@@ -734,9 +739,10 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
 template <int NACC, int Q, int PW, int WPG, int MINB, bool IN_BF16, bool OUT_BF16>
 cudaError_t launch_variant(const WcsrParams &p, cudaStream_t stream) {
   using C_ = Cfg<NACC, Q, PW, WPG, MINB, kIdxLead>;
-  auto kern = wcsr_spmm_kernel<NACC, Q, PW, WPG, MINB, IN_BF16, OUT_BF16>;
-  static std::atomic<uint64_t> smem_set{0};  // per instantiation, one bit per device
-  cudaError_t e = set_smem_limit_once(kern, C_::kSmemBytes, smem_set);
+  auto kern = p.dynamic ? wcsr_spmm_kernel<NACC, Q, PW, WPG, MINB, IN_BF16, OUT_BF16, false, true>
+                        : wcsr_spmm_kernel<NACC, Q, PW, WPG, MINB, IN_BF16, OUT_BF16, false, false>;
+  static std::atomic<uint64_t> smem_set[2];  // per instantiation, one bit per device
+  cudaError_t e = set_smem_limit_once(kern, C_::kSmemBytes, smem_set[p.dynamic ? 1 : 0]);
   if (e != cudaSuccess) return e;
   kern<<<p.grid, C_::kThreads, C_::kSmemBytes, stream>>>(p);
   e = cudaGetLastError();
