@@ -33,6 +33,9 @@ def full_check(m, k, n, rp, ci, vals, dt, out_dt, B, max_ctas=None, runs=1):
     (333, 777, 72, 0.03, "f16", "f32"),       # ragged window, N < 128
     (256, 2048, 264, 0.02, "bf16", "bf16"),   # two column tiles + tail, bf16 C
     (64, 64, 8, 0.2, "bf16", "f32"),          # N = 8
+    (333, 777, 40, 0.03, "f16", "f32"),       # N <= 64, ragged window
+    (1000, 3000, 64, 0.01, "bf16", "bf16"),   # N = 64, bf16 C
+    (700, 4000, 24, 0.02, "bf16", "f32"),     # N = 24: partial 16-byte units
 ])
 def test_wcsr_parity_small(m, k, n, d, dt, out_dt):
     rng = np.random.default_rng(m + 17 * n)
@@ -42,7 +45,7 @@ def test_wcsr_parity_small(m, k, n, d, dt, out_dt):
 
 
 @pytest.mark.parametrize("ctas,n,out_dt", [(3, 256, "f32"), (7, 128, "f32"), (13, 72, "f32"), (5, 520, "f32"),
-                                          (6, 264, "bf16")])
+                                          (6, 264, "bf16"), (7, 64, "f32"), (11, 40, "bf16"), (4, 8, "f32")])
 def test_wcsr_windows_cut_between_ctas(ctas, n, out_dt):
     """Few persistent CTAs: long windows are cut between CTAs and finished by
     the second kernel; the result must match and be bitwise reproducible."""
@@ -56,10 +59,11 @@ def test_wcsr_windows_cut_between_ctas(ctas, n, out_dt):
     assert np.array_equal(outs[0], outs[1])
 
 
-def test_wcsr_window_spanning_many_ctas():
+@pytest.mark.parametrize("n", [136, 48])
+def test_wcsr_window_spanning_many_ctas(n):
     """One window much longer than a CTA's share: its partials span several CTAs."""
     rng = np.random.default_rng(17)
-    m, k, n = 48, 6000, 136
+    m, k = 48, 6000
     rp = np.zeros(m + 1, np.int64)
     cols = [np.sort(rng.choice(k, 3000 if i == 20 else 3, replace=False)) for i in range(m)]
     rp[1:] = np.cumsum([len(c) for c in cols])
@@ -88,9 +92,10 @@ def test_wcsr_empty_windows_and_identity():
     assert np.array_equal(outs[0], ref)
 
 
-def test_wcsr_one_nonzero_per_row_exact():
+@pytest.mark.parametrize("n", [136, 56])
+def test_wcsr_one_nonzero_per_row_exact(n):
     rng = np.random.default_rng(9)
-    m, k, n = 257, 900, 136
+    m, k = 257, 900
     rp = np.arange(m + 1, dtype=np.int64)
     ci = rng.integers(0, k, m).astype(np.int32)
     vals = W.draw_values(rng, m, "u1", "f16")
@@ -228,7 +233,7 @@ def test_wcsr_dynamic_schedule_takes_over_chunks():
     assert np.array_equal(outs[0], outs[1])
 
 
-@pytest.mark.parametrize("ctas,n,out_dt", [(3, 256, "f32"), (5, 72, "bf16"), (2, 520, "f32")])
+@pytest.mark.parametrize("ctas,n,out_dt", [(3, 256, "f32"), (5, 72, "bf16"), (2, 520, "f32"), (4, 40, "f32")])
 def test_wcsr_dynamic_schedule_few_chunks(ctas, n, out_dt):
     """Dynamic schedule with a CTA cap: a handful of chunks (all resident at
     once, so every cancellation request finds nothing left), long windows cut
