@@ -18,7 +18,7 @@ collective on the data path); the reported time is the max over ranks.
 
 --impl reference times the CPU oracle (fp64, OpenMP) on the host cores on a
 bounded sample of the same workload per step.
---sweep prints one line per benchmark configuration (not the driver line);
+--sweep prints one line per benchmark configuration (instead of the step line);
 --sweep bcsr_weight:8192 runs one configuration at another dense width N.
 """
 from __future__ import annotations
