@@ -483,16 +483,27 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         }
       };
       int64_t n_fetched = 0;  // own items whose index records were requested (a prefix)
+      // The stage record of work item f is f % n_stages, its column tile
+      // f / n_stages: followed by cursors on the static schedule (one chunk,
+      // items in steps of G), divided out under the dynamic one (whose
+      // chunk table already takes the registers).
       ItemCursor fcur, icur;  // the items fetched and the items copied
       auto fetch_idx = [&](int64_t j) -> bool {
         const int q = locate(grp + G * j);
         if (q == -2) return false;
         if (q >= 0) {
           const Chunk &c = kn[q & (kKn - 1)];
-          fcur.to(c.g0 + (grp + G * j - c.lbase), n_stages);
+          const int64_t fj = c.g0 + (grp + G * j - c.lbase);
+          int64_t fs;
+          if constexpr (DYN) {
+            fs = fj % n_stages;
+          } else {
+            fcur.to(fj, n_stages);
+            fs = fcur.s;
+          }
           if (lane == 0) {
             const uint32_t slot = static_cast<uint32_t>(j % kILead);
-            const uint8_t *src = pack + fcur.s * kWcsrPackBytes;
+            const uint8_t *src = pack + fs * kWcsrPackBytes;
             mbar_arrive_expect_tx(ifull_w + 8 * slot, kMetaBytes);
             tma_bulk_load(smem_addr(ring + slot * kMetaBytes), src + kWcsrPackIdxOff, kMetaBytes,
                           ifull_w + 8 * slot);
@@ -525,8 +536,16 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
         consumed = j + 1;
         ok = fetch_idx(j + kILead);
         if (!ok) break;
-        icur.to(f, n_stages);
-        const int tile = icur.tile;
+        int tile;
+        int64_t fsi;
+        if constexpr (DYN) {
+          tile = static_cast<int>(f / n_stages);
+          fsi = f - static_cast<int64_t>(tile) * n_stages;
+        } else {
+          icur.to(f, n_stages);
+          tile = icur.tile;
+          fsi = icur.s;
+        }
         const uint32_t stage = static_cast<uint32_t>(it % Q);
         const uint32_t phase = static_cast<uint32_t>((it / Q) & 1);
         // the stage is free once the MMAs of item it - Q are complete
@@ -543,7 +562,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
           const int32_t fl = d.y | (it == c.lbase ? kRecChunkFirst : 0) | (it == c.lbase + c.len - 1 ? kRecChunkLast : 0);
           stage_rec[stage] = StageRec{d.x, fl, d.z, tile, c.id, {0, 0, 0}};  // released by this arrive
           mbar_arrive_expect_tx(fb, kValBytes);
-          tma_bulk_load(st + C_::kGatherBytes, pack + icur.s * kWcsrPackBytes + kWcsrPackValOff, kValBytes,
+          tma_bulk_load(st + C_::kGatherBytes, pack + fsi * kWcsrPackBytes + kWcsrPackValOff, kValBytes,
                         fb);
         }
         gather(st, tile * C_::kBN, d.x, lo, hi);
