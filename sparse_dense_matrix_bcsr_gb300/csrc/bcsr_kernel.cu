@@ -489,6 +489,7 @@ __global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, KB, OUT_BF16
         }
       }
     }
+    grid_launch_dependents();  // every MMA is issued: the next kernel may be scheduled
   } else {
     // ------------------------------------------------------------ epilogue
     // Warp w reads TMEM sub-partition s = w % 4; lane t holds one row of C

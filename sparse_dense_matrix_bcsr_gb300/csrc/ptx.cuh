@@ -94,6 +94,18 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, ui
   }
 }
 
+// ---------------------------------------------------------------- dependent launches
+// A kernel launched with programmatic stream serialization may start before
+// the kernel ahead of it in the stream has finished: it waits here until that
+// kernel has completed and its memory writes are visible (a no-op for a
+// kernel launched without the attribute).  The kernel ahead lets its
+// dependents be scheduled once every one of its CTAs has executed
+// launch_dependents or exited.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace spmm {
 
@@ -39,6 +40,7 @@ __global__ void __launch_bounds__(256)
   static_assert(ROWS % RPB == 0, "row chunks");
   extern __shared__ int32_t contrib[];  // [grid]
   __shared__ int32_t n_contrib;
+  grid_dependency_wait();  // the first pass has finished and its partials are visible
   const int slot = blockIdx.x;
   const PartialRec rec = partials[slot];
   if (rec.group < 0 || !(rec.flags & kStageFirst) || (rec.flags & kStageLast)) return;
@@ -96,9 +98,21 @@ inline cudaError_t launch_split_reduce(const PartialRec *partials, const float *
                                        int32_t ws_ld, void *C, int32_t M, int32_t N, int32_t grid, int32_t bn,
                                        cudaStream_t stream) {
   constexpr int kRpb = 8;
-  split_reduce_kernel<ROWS, kRpb, OUT_BF16><<<dim3(2 * grid, ROWS / kRpb), 256, grid * sizeof(int32_t), stream>>>(
-      partials, ws, slot_floats, ws_ld, C, M, N, grid, bn);
-  return cudaGetLastError();
+  // Launched as a programmatic dependent of the first pass: its launch
+  // overlaps the first pass's last tiles, and grid_dependency_wait holds its
+  // blocks until the first pass has completed.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * grid, ROWS / kRpb);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = grid * sizeof(int32_t);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, split_reduce_kernel<ROWS, kRpb, OUT_BF16>, partials, ws, slot_floats, ws_ld, C,
+                            M, N, grid, bn);
 }
 
 }  // namespace spmm

@@ -396,6 +396,7 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
           mbar_arrive(accf0 + 8 * b);
         }
     }
+    grid_launch_dependents();  // every MMA is issued: the reduce pass may be scheduled
   } else {
     // ------------------------------------------------------------ epilogue
     // Warp w reads sub-partition sp = w % 4: rows 32 (sp % 2) + lane of the

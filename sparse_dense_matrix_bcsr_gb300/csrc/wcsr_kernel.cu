@@ -688,6 +688,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
       }
     }
     __syncwarp();
+    grid_launch_dependents();  // every MMA is issued: the reduce pass may be scheduled
   } else {
     // ------------------------------------------------------------ epilogue
     const int sp = warp & 3;
