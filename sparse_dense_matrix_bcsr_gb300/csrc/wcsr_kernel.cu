@@ -633,15 +633,29 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
           // start-address field (smem_desc_add), which stays in range.
           const uint64_t bdesc0 = smem_desc_sw128(vals, 16, 1024);
           const uint64_t adesc0 = smem_desc_sw128(gath, kChunkBytes, 1024);
+          if (ksteps == kKC / 16 && nacc == NACC) {
+            // a full item (the common case): the MMAs without per-step tests,
+            // which measured ~20 % cheaper to issue
+            const uint32_t acc_in0 = ksteps_done > 0 ? 1u : 0u;
 #pragma unroll
-          for (int kk = 0; kk < kKC / 16; ++kk) {
-            if (kk < ksteps) {
+            for (int kk = 0; kk < kKC / 16; ++kk) {
               const uint64_t bdesc = smem_desc_add(bdesc0, kk * 32);
 #pragma unroll
-              for (int a = 0; a < NACC; ++a) {
-                if (a < nacc)
-                  umma_f16(acc + a * kH, smem_desc_add(adesc0, a * 2 * kChunkBytes + kk * 2048), bdesc, idesc,
-                           (ksteps_done + kk) > 0 ? 1u : 0u);
+              for (int a = 0; a < NACC; ++a)
+                umma_f16(acc + a * kH, smem_desc_add(adesc0, a * 2 * kChunkBytes + kk * 2048), bdesc, idesc,
+                         kk > 0 ? 1u : acc_in0);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < kKC / 16; ++kk) {
+              if (kk < ksteps) {
+                const uint64_t bdesc = smem_desc_add(bdesc0, kk * 32);
+#pragma unroll
+                for (int a = 0; a < NACC; ++a) {
+                  if (a < nacc)
+                    umma_f16(acc + a * kH, smem_desc_add(adesc0, a * 2 * kChunkBytes + kk * 2048), bdesc, idesc,
+                             (ksteps_done + kk) > 0 ? 1u : 0u);
+                }
               }
             }
           }
