@@ -346,11 +346,19 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
         const uint32_t acc = tmem + buf * kAccCols;
         const uint64_t vdesc0 = smem_desc_sw128(vals, 16, 1024);
         const uint64_t gdesc0 = smem_desc_sw128(gath, kChunkBytes, 1024);
+        if (ksteps == kKC / 16) {  // a full item: no per-step tests (cheaper to issue)
+          const uint32_t acc_in0 = ksteps_done > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < kKC / 16; ++kk)
-          if (kk < ksteps)
+          for (int kk = 0; kk < kKC / 16; ++kk)
             umma_ws_f16(acc, smem_desc_add(vdesc0, kk * 32), smem_desc_add(gdesc0, kk * 2048), idesc,
-                        (ksteps_done + kk) > 0 ? 1u : 0u);
+                        kk > 0 ? 1u : acc_in0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kKC / 16; ++kk)
+            if (kk < ksteps)
+              umma_ws_f16(acc, smem_desc_add(vdesc0, kk * 32), smem_desc_add(gdesc0, kk * 2048), idesc,
+                          (ksteps_done + kk) > 0 ? 1u : 0u);
+        }
         umma_commit(empty0 + 8 * stage);
       }
       ksteps_done += ksteps;
