@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, KB, OUT_BF16
         }
         break;
       }
-      if (leader) {
+      {  // converged: one elected lane issues each MMA and commit
         if (!(rec.flags & kRecEmpty)) {
           tc_fence_after_sync();
           const int nmma = min(C_::kMmas, (p.N - rec.nt * BN + C_::kNmma - 1) / C_::kNmma);
@@ -449,22 +449,24 @@ __global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, KB, OUT_BF16
                     const uint64_t bdesc = smem_desc_add(
                         bdesc0, b * C_::kSubBytes + m * (C_::kNmma / 64) * kChunkBytes + kk * 2048);
                     if constexpr (C_::kWS)
-                      umma_ws_f16(acc, adesc, bdesc, idesc, acc_in);
+                      umma_ws_f16_elect(acc, adesc, bdesc, idesc, acc_in);
                     else
-                      umma_f16(acc + m * C_::kNmma, adesc, bdesc, idesc, acc_in);
+                      umma_f16_elect(acc + m * C_::kNmma, adesc, bdesc, idesc, acc_in);
                   }
                 }
               }
             }
           }
         }
-        umma_commit(empty0 + 8 * stage);  // frees the stage once these MMAs have read it
+        umma_commit_elect(empty0 + 8 * stage);  // frees the stage once these MMAs have read it
         if (rec.flags & kRecLast) {
-          acc_rec[buf].br = rec.br;
-          acc_rec[buf].nt = rec.nt;
-          acc_rec[buf].flags = (rec.flags & (kRecEmpty | kRecTileLast)) | seg_flags;
-          mbar_arrive(accf0 + 8 * buf);  // releases the record
-          umma_commit(accf0 + 8 * buf);  // arrives when the tile's MMAs are done
+          if (leader) {
+            acc_rec[buf].br = rec.br;
+            acc_rec[buf].nt = rec.nt;
+            acc_rec[buf].flags = (rec.flags & (kRecEmpty | kRecTileLast)) | seg_flags;
+            mbar_arrive(accf0 + 8 * buf);  // releases the record
+          }
+          umma_commit_elect(accf0 + 8 * buf);  // arrives when the tile's MMAs are done
         }
       }
       if (rec.flags & kRecLast) ++tcount;

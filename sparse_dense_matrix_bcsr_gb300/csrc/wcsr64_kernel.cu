@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
         s_at_f0 = f == f0;
       }
       const int ksteps = rec.ncols / 16;
-      if (leader) {
+      {  // converged: one elected lane issues each MMA and commit
         fence_proxy_async_smem();  // the stage's cp.async writes -> async-proxy MMA reads
         tc_fence_after_sync();
         const uint32_t vals = smem_addr(smem + stage * kStageBytes);  // M operand (K-major)
@@ -350,16 +350,16 @@ __global__ void __launch_bounds__(32 * (PW + 5), MINB)
           const uint32_t acc_in0 = ksteps_done > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < kKC / 16; ++kk)
-            umma_ws_f16(acc, smem_desc_add(vdesc0, kk * 32), smem_desc_add(gdesc0, kk * 2048), idesc,
+            umma_ws_f16_elect(acc, smem_desc_add(vdesc0, kk * 32), smem_desc_add(gdesc0, kk * 2048), idesc,
                         kk > 0 ? 1u : acc_in0);
         } else {
 #pragma unroll
           for (int kk = 0; kk < kKC / 16; ++kk)
             if (kk < ksteps)
-              umma_ws_f16(acc, smem_desc_add(vdesc0, kk * 32), smem_desc_add(gdesc0, kk * 2048), idesc,
+              umma_ws_f16_elect(acc, smem_desc_add(vdesc0, kk * 32), smem_desc_add(gdesc0, kk * 2048), idesc,
                           (ksteps_done + kk) > 0 ? 1u : 0u);
         }
-        umma_commit(empty0 + 8 * stage);
+        umma_commit_elect(empty0 + 8 * stage);
       }
       ksteps_done += ksteps;
       if (seg_last) {

@@ -583,7 +583,9 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp takes the waits (see mbar_wait_warp); lane 0 issues.
+    // The whole warp takes the waits (see mbar_wait_warp) and runs the MMA
+    // issue converged, one elected lane issuing each MMA and commit; lane 0
+    // writes the records for the epilogue.
     {
       constexpr uint32_t idesc = idesc_f16(IN_BF16, /*a_mn_major=*/true, /*b_mn_major=*/false, 128, kH);
       const bool leader = lane == 0;
@@ -622,7 +624,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
           s_at_f0 = (rec.flags & kRecChunkFirst) != 0;
         }
         const int ksteps = rec.ncols / 16;
-        if (leader) {
+        {
           fence_proxy_async_smem();  // the stage's cp.async writes -> async-proxy MMA reads
           tc_fence_after_sync();
           const uint32_t gath = smem_addr(smem + stage * C_::kStageBytes);  // MMA operand A (MN-major)
@@ -642,7 +644,7 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
               const uint64_t bdesc = smem_desc_add(bdesc0, kk * 32);
 #pragma unroll
               for (int a = 0; a < NACC; ++a)
-                umma_f16(acc + a * kH, smem_desc_add(adesc0, a * 2 * kChunkBytes + kk * 2048), bdesc, idesc,
+                umma_f16_elect(acc + a * kH, smem_desc_add(adesc0, a * 2 * kChunkBytes + kk * 2048), bdesc, idesc,
                          kk > 0 ? 1u : acc_in0);
             }
           } else {
@@ -653,13 +655,13 @@ __global__ void __launch_bounds__(32 * (PW + 1 + kEpiWarps), MINB)
 #pragma unroll
                 for (int a = 0; a < NACC; ++a) {
                   if (a < nacc)
-                    umma_f16(acc + a * kH, smem_desc_add(adesc0, a * 2 * kChunkBytes + kk * 2048), bdesc, idesc,
+                    umma_f16_elect(acc + a * kH, smem_desc_add(adesc0, a * 2 * kChunkBytes + kk * 2048), bdesc, idesc,
                              (ksteps_done + kk) > 0 ? 1u : 0u);
                 }
               }
             }
           }
-          umma_commit(empty0 + 8 * stage);
+          umma_commit_elect(empty0 + 8 * stage);
         }
         ksteps_done += ksteps;
         if (seg_last) {
