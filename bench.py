@@ -47,12 +47,12 @@ L2_FLUSH_BYTES = 256 << 20
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture,
 # valid only for the kernel source it was taken on (sha256 of the file).
 MEASURED_TRAFFIC = {
-    # bcsr_weight: 114.8 MB read + 261.6 MB written at N = 8192; B and C scale
-    # with N, A (13.6 MB) does not: 13.6 MB + 8 x 362.8 MB at N = 65536
-    "bcsr_kernel.cu": {"src_sha": "ac644b02a7b049cd", "bytes_per_launch": 2.916e9},
-    # wcsr_uniform at its benchmark size: 100.1 MB read + 9.1 MB written (part
+    # bcsr_weight: 114.9 MB read + 261.7 MB written at N = 8192; B and C scale
+    # with N, A (13.6 MB) does not: 13.6 MB + 8 x 363.1 MB at N = 65536
+    "bcsr_kernel.cu": {"src_sha": "158009bf8c3f0064", "bytes_per_launch": 2.918e9},
+    # wcsr_uniform at its benchmark size: 100.1 MB read + 9.2 MB written (part
     # of C still in L2 when the kernel ends)
-    "wcsr_kernel.cu": {"src_sha": "c22922174413da9b", "bytes_per_launch": 1.092e8},
+    "wcsr_kernel.cu": {"src_sha": "c78a22c320346a38", "bytes_per_launch": 1.093e8},
 }
 
 

@@ -6,7 +6,7 @@
 // producer/consumer pipeline over the stored blocks of one block row, full[Q]
 // and empty[Q] barriers with phase bits, the first MMA overwriting the
 // accumulator), Section III-B (each 64x64 block and its 64 rows of B are
-// 2-D TMA loads).  On sm_103a the consumer is a single thread issuing
+// 2-D TMA loads).  On sm_103a the consumer is one warp issuing
 // tcgen05.mma into TMEM:
 //   C[r, n] += sum_k blk[r, k] * B[k, n]
 // with the block as the M = 64 operand (K-major) and the B tile as the N
@@ -25,7 +25,8 @@
 //   warp 0      producer: reads the block-row pointers and block-column
 //               indices, waits for a free stage, writes the stage's tile
 //               record to shared memory and issues its TMA loads (lane 0)
-//   warp 1      TMEM allocator and MMA issuer (lane 0 issues); it learns the
+//   warp 1      TMEM allocator and MMA issuer (converged; one elected lane
+//               issues each MMA and commit); it learns the
 //               tile layout from the stage records, so it never waits on a
 //               global load, and hands each finished accumulator to the
 //               epilogue with a record of its own
@@ -395,7 +396,8 @@ __global__ void __launch_bounds__(Cfg<BN, Q, NBUF, PARTS, MINB, PW, KB, OUT_BF16
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp takes the waits (see mbar_wait_warp); lane 0 issues.
+    // The whole warp takes the waits (see mbar_wait_warp) and issues
+    // converged (one elected lane per MMA and commit); lane 0 writes records.
     constexpr uint32_t idesc = idesc_f16(IN_BF16, /*a_mn_major=*/false, /*b_mn_major=*/true, 64, C_::kNmma);
     const bool leader = lane == 0;
     uint32_t stage = 0, phase = 0;
