@@ -16,12 +16,6 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -120,6 +114,11 @@ __device__ __forceinline__ void umma_f16_elect(uint32_t d_tmem, uint64_t a_desc,
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The weight-stationary form (M = 32, 64 or 128; N = 64, 128 or 256).  On
+// GB300 an M = 64 x N = 256 x K = 16 bf16 MMA takes ~93 cycles in this form
+// against 128 in the plain one.  Its M = 64 accumulator holds rows 0..63 in
+// TMEM lanes 0..63 for columns 0..N/2-1 and in lanes 64..127 for columns
+// N/2..N-1, each in N/2 TMEM columns.
 __device__ __forceinline__ void umma_ws_f16_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                   uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -273,21 +272,6 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint6
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The weight-stationary form (M = 32, 64 or 128; N = 64, 128 or 256).  On
-// GB300 an M = 64 x N = 256 x K = 16 bf16 MMA takes ~93 cycles in this form
-// against 128 in the plain one.  Its M = 64 accumulator holds rows 0..63 in
-// TMEM lanes 0..63 for columns 0..N/2-1 and in lanes 64..127 for columns
-// N/2..N-1, each in N/2 TMEM columns.
-__device__ __forceinline__ void umma_ws_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.ws.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
