@@ -127,9 +127,13 @@ spmm_status spmm_wcsr_create(spmm_handle *out, int64_t m, int64_t k, const int64
  *   C  device pointer, m x N row-major, out_t, 16-byte aligned; fully
  *      overwritten (rows of A without entries give 0).
  *   N  number of columns of B and C, N > 0 and N % 8 == 0 (TMA row stride).
- * A WCSR handle adds the partial sums of windows cut between CTAs in a
- * second kernel, in a fixed order, using a workspace allocated at create;
- * results are bitwise reproducible run to run.
+ * A WCSR handle (and a BCSR one on the split schedule) adds the partial sums
+ * of groups cut between CTAs in a second kernel, in a fixed order, using a
+ * workspace allocated at create; results are bitwise reproducible run to run.
+ * That kernel is launched as a programmatic dependent of the first (it may
+ * be scheduled before the first finishes and waits for it on the device);
+ * to the caller the two behave as one stream-ordered operation, also under
+ * stream capture.
  * Errors: INVALID_ARG (null handle/pointers, N <= 0); UNSUPPORTED (N % 8,
  * alignment, format parameters the kernels do not take, device not sm_103);
  * OOM (workspace); CUDA (launch).  Asynchronous: see spmm_check.
